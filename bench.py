@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of one DSA layer step on GB300 (query-tokens/s per layer and the
+roofline fraction of the dominant kernel).
+
+A step is one call of the fused dsa_decode (indexer -> exact top-2048 ->
+sparse MLA) over one batch, on one layer's paged caches.  Consecutive steps
+rotate through `--layers` independent layer copies (24 by default, as in the
+24 full-attention layers of the model), so that the working set is far larger
+than the 129 MB L2 and every step reads its caches from HBM.
+
+Default workload: 8 requests, contexts drawn uniformly from [16384, 32768],
+one query token each (batched decode).  `--config` selects another:
+c0_tiny, c1_batched, c2_agentic, c3a_long_fp8, c3b_long_mxfp4.
+
+Arms
+  --impl ours       (default) the CUDA library through its C ABI.
+  --impl reference  the CPU oracle (plain fp64 C) as it stands, on the host
+                    cores, on a bounded sample of the same workload.
+
+Multi-GPU (torchrun, one process per GPU): replicas only -- each rank runs the
+same workload on its own GPU with no data-path collective (weak scaling); the
+timing takes the maximum over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DSA decode query-tokens/s per layer; achieved HBM GB/s vs GB300 roofline"
+UNIT = "query-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2400)
+    ap.add_argument("--warmup", type=int, default=48)
+    ap.add_argument("--config", default="c1_batched")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="bounded CPU-oracle sample for the cpu_baseline field")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-seconds", type=float, default=1.5,
+                    help="extra untimed replay while GPU clocks are sampled")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def config_shape(name):
+    import dsa_inputs as di
+    lens, nq, fmt, seed = di.config_shape(name)
+    q_counts = [nq] * len(lens) if isinstance(nq, int) else list(nq)
+    return lens, q_counts, fmt, seed
+
+
+# ---- CPU oracle (baseline and reference arm) --------------------------------
+
+def oracle_step(layer, rows):
+    import oracle
+    ob = oracle.Batch(layer.q_offsets, layer.seq_lens, layer.block_table, layer.num_pages)
+    t0 = time.perf_counter()
+    oracle.decode(ob, layer.q8, layer.qscale, layer.w, layer.index_pages, layer.key_format,
+                  layer.q_lat, layer.latent_pages, layer.kv_scale, layer.sm_scale, rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, seconds):
+    """The oracle on the host cores: whole layer steps (all query rows of the
+    batch, in parallel over rows) until about `seconds` of CPU work."""
+    import dsa_inputs as di
+    import oracle
+    lens, q_counts, fmt, seed = config_shape(cfg)
+    T = sum(q_counts)
+    rows_per_step = min(T, max(1, oracle.num_threads()))
+    layer = di.make_layer(lens, q_counts, fmt, seed)
+    done_rows, spent, steps = 0, 0.0, 0
+    while spent < seconds and steps < 64:
+        rows = [(done_rows + i) % T for i in range(rows_per_step)]
+        spent += oracle_step(layer, rows)
+        done_rows += rows_per_step
+        steps += 1
+    return {"value": done_rows / spent, "unit": UNIT,
+            "cores": min(rows_per_step, oracle.num_threads()), "kind": "oracle",
+            "sample": "%d oracle step(s) of %d query rows of one %s layer (ctx %d..%d), "
+                      "%.1f s" % (steps, rows_per_step, cfg, min(lens), max(lens), spent)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import dsa_inputs as di
+    import oracle
+    lens, q_counts, fmt, seed = config_shape(args.config)
+    T = sum(q_counts)
+    layer = di.make_layer(lens, q_counts, fmt, seed)
+    threads = oracle.num_threads()
+    rows_per_step = min(T, threads)
+    # size each step so that warm-up + timed steps end within ~150 s
+    probe = oracle_step(layer, list(range(rows_per_step)))
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    while rows_per_step > 1 and probe * rows_per_step / min(rows_per_step, threads) > budget:
+        rows_per_step = max(1, rows_per_step // 2)
+        probe = oracle_step(layer, list(range(rows_per_step)))
+    cursor = 0
+    for _ in range(args.warmup):
+        oracle_step(layer, [(cursor + i) % T for i in range(rows_per_step)])
+        cursor += rows_per_step
+    spent = 0.0
+    for _ in range(args.steps):
+        spent += oracle_step(layer, [(cursor + i) % T for i in range(rows_per_step)])
+        cursor += rows_per_step
+    rows = args.steps * rows_per_step
+    value = rows / spent
+    cores = min(rows_per_step, threads)
+    sample = "%d query rows of one %s layer per step (full indexer + top-k + MLA per row)" % (
+        rows_per_step, args.config)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * spent / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config, "requests": len(lens),
+                       "seq_lens": [min(lens), max(lens)], "query_tokens": T},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---- clocks -----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="dsa_clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- GPU arm ----------------------------------------------------------------
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dsa_sparse_attention_step_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, cfg):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec[kernel][cfg]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.config, args.cpu_seconds)
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import dsa_inputs as di
+    import dsa_sparse_attention_step_gb300 as dsa
+    from dsa_sparse_attention_step_gb300 import workload as wl
+    dsa.load()
+
+    lens, q_counts, fmt, seed = config_shape(args.config)
+    T = sum(q_counts)
+    L = max(1, args.layers)
+    dev = torch.device("cuda", local)
+    layers, batches = [], []
+    for l in range(L):
+        lay = di.make_layer(lens, q_counts, fmt, seed + 7919 * (l + 1) + 104729 * rank,
+                            device=dev)
+        layers.append(lay)
+        batches.append(dsa.Batch(lay.q_offsets, lay.seq_lens, lay.block_table, lay.num_pages,
+                                 lens, q_counts))
+    cache_bytes = sum(l.index_pages.numel() + l.latent_pages.numel() for l in layers)
+    out = torch.empty(T, 96, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, 96, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, dsa.TOPK, dtype=torch.int32, device=dev)
+    ws = torch.empty(dsa.dsa_decode_workspace_size(batches[0]), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s=None):
+        lay, b = layers[i % L], batches[i % L]
+        dsa.dsa_decode(b, lay.q8, lay.qscale, lay.w, lay.index_pages, fmt, lay.q_lat,
+                       lay.latent_pages, lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx,
+                       ws, status, stream=s)
+
+    # one CUDA graph = one pass over the L layers (L steps)
+    with torch.cuda.stream(stream):
+        for i in range(min(args.warmup, 2 * L) + 1):
+            step(i, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(L):
+            step(i, stream)
+
+    def run_steps(n, first):
+        """n steps starting at layer `first % L` (graph replays + singles)."""
+        with torch.cuda.stream(stream):
+            i = first
+            while n > 0 and i % L != 0:
+                step(i, stream); i += 1; n -= 1
+            while n >= L:
+                graph.replay(); i += L; n -= L
+            while n > 0:
+                step(i, stream); i += 1; n -= 1
+        return i
+
+    nxt = run_steps(args.warmup, 0)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    l0 = dsa.dsa_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ev0.record(stream)
+    nxt = run_steps(args.steps, nxt)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches_timed = dsa.dsa_launch_count() - l0
+    # graph replays do not pass through the library: count its kernels per step
+    per_step_launches = 3
+    gpu_launches = per_step_launches * args.steps
+    elapsed = ev0.elapsed_time(ev1) / 1000.0
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    # keep the GPU busy a little longer while the clock sampler runs
+    t_end = time.time() + args.soak_seconds
+    while time.time() < t_end:
+        nxt = run_steps(L * 8, nxt)
+        torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError("device status %d (%s)" % (st, dsa.dsa_status_string(st)))
+
+    # ---- per-kernel durations (graphs of L launches of one entry point) ----
+    ld = ((max(lens) + 127) // 128) * 128
+    scores = ws[:T * ld * 4].view(torch.float32).view(T, ld)
+    kern = {}
+
+    def time_graph(fn, reps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(L):
+                fn(i)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(L):
+                fn(i)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) / 1000.0 / (reps * L)
+
+    reps = max(3, min(200, args.steps // L))
+    kern["indexer"] = time_graph(
+        lambda i: dsa.dsa_index_scores(batches[i], layers[i].q8, layers[i].qscale, layers[i].w,
+                                       layers[i].index_pages, fmt, scores, ld, status,
+                                       stream=stream), reps)
+    kern["topk"] = time_graph(
+        lambda i: dsa.dsa_topk(batches[i], scores, ld, dsa.TOPK, idx, None, stream=stream), reps)
+    kern["sparse_mla"] = time_graph(
+        lambda i: dsa.dsa_sparse_mla(batches[i], layers[i].q_lat, layers[i].latent_pages,
+                                     layers[i].kv_scale, layers[i].sm_scale, idx, dsa.TOPK, out,
+                                     lse, None, status, stream=stream), reps)
+    kbytes = {"indexer": wl.indexer_bytes(lens, q_counts, fmt),
+              "topk": wl.topk_bytes(lens, q_counts),
+              "sparse_mla": wl.mla_bytes(lens, q_counts)}
+    dominant = max(kern, key=kern.get)
+    hbm, bf16, src = peaks()
+    achieved = kbytes[dominant] / kern[dominant] / 1e9
+    traffic = recorded_traffic(dominant, args.config)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                "peak_source": src + " (burst copy)",
+                "algorithmic_bytes_per_launch": kbytes[dominant],
+                "avg_launch_us": kern[dominant] * 1e6,
+                "kernels_us": {k: v * 1e6 for k, v in kern.items()}}
+
+    # ---- end to end through the public API with host buffers --------------
+    e2e = None
+    if rank == 0:
+        pin = lambda t: t.cpu().pin_memory()
+        hq = [(pin(l.q8), pin(l.qscale), pin(l.w), pin(l.q_lat)) for l in layers]
+        hmeta = [(pin(l.q_offsets), pin(l.seq_lens), pin(l.block_table)) for l in layers]
+        dq = [(torch.empty_like(l.q8), torch.empty_like(l.qscale), torch.empty_like(l.w),
+               torch.empty_like(l.q_lat)) for l in layers[:2]]
+        dmeta = [(torch.empty_like(l.q_offsets), torch.empty_like(l.seq_lens),
+                  torch.empty_like(l.block_table)) for l in layers[:2]]
+        dbatch = [dsa.Batch(m[0], m[1], m[2], layers[0].num_pages, lens, q_counts)
+                  for m in dmeta]
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hidx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hq[0] + hmeta[0])
+        d2h = hout.numel() * hout.element_size() + hidx.numel() * hidx.element_size()
+
+        def e2e_step(i):
+            j = i % L
+            slot = i % 2
+            lay = layers[j]
+            for d, h in zip(dq[slot] + dmeta[slot], hq[j] + hmeta[j]):
+                d.copy_(h, non_blocking=True)
+            q8, qs, w, ql = dq[slot]
+            # the block table copied in belongs to layer j's pools
+            dsa.dsa_decode(dbatch[slot], q8, qs, w, lay.index_pages, fmt, ql, lay.latent_pages,
+                           lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx, ws, status,
+                           stream=stream)
+            hout.copy_(out, non_blocking=True)
+            hidx.copy_(idx, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                e2e_step(i)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            a.record(stream)
+            n_e2e = min(args.steps, 480)
+            for i in range(n_e2e):
+                e2e_step(i)
+            b.record(stream)
+        stream.synchronize()
+        te = a.elapsed_time(b) / 1000.0
+        e2e = {"value": T * n_e2e / te, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "note": "per step: pinned H2D of queries and metadata, dsa_decode, D2H of "
+                       "output and indices; caches resident"}
+
+    if rank == 0:
+        step_b = wl.step_bytes(lens, q_counts, fmt)
+        value = world * T * args.steps / elapsed
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8/bf16->fp32",
+                "data": "synthetic",
+                "config": {"workload": args.config, "requests": len(lens),
+                           "seq_lens": [min(lens), max(lens)], "query_tokens": T,
+                           "layers_rotated": L, "cache_bytes_rotated": cache_bytes,
+                           "l2": "inputs larger than L2: %d layer copies, %.2f GB of caches "
+                                 "rotated" % (L, cache_bytes / 1e9),
+                           "parallelism": "replicas" if world > 1 else "single"},
+                "step_hbm_gbs": step_b / (elapsed / args.steps) / 1e9,
+                "step_bytes": step_b,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": gpu_launches, "clocks": clocks}
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

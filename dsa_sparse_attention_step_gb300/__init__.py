@@ -1,0 +1,228 @@
+"""GB300-native DSA sparse-attention step.
+
+Python binding of ``libdsa.so`` (the C ABI declared in ``include/dsa.h``):
+argument marshalling only.  Every step of the path runs in the library's CUDA
+kernels; PyTorch supplies device memory and streams.  There is no CPU
+fallback: importing works without a GPU, but every call needs the built
+library and a CUDA device, and raises otherwise.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path", "load",
+           "dsa_status_string", "dsa_launch_count", "dsa_index_scores", "dsa_topk",
+           "dsa_topk_workspace_size", "dsa_sparse_mla", "dsa_sparse_mla_workspace_size",
+           "dsa_decode", "dsa_decode_workspace_size", "dsa_append_cache"]
+
+KEYS_FP8 = 0
+KEYS_MXFP4 = 1
+TOPK = 2048
+PAGE = 64
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+def library_path():
+    return os.path.join(_PKG, "libdsa.so")
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _status_str(status), status))
+
+
+class _CBatch(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("total_q", ctypes.c_int32),
+                ("max_q_per_request", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("q_offsets", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p)]
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+_bp = ctypes.POINTER(_CBatch)
+
+_SIGS = {
+    "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dsa_launch_count": (ctypes.c_uint64, []),
+    "dsa_index_scores": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _i64, _vp, _vp]),
+    "dsa_topk_workspace_size": (_sz, [_bp, _i32]),
+    "dsa_topk": (ctypes.c_int, [_bp, _vp, _i64, _i32, _vp, _vp, _sz, _vp]),
+    "dsa_sparse_mla_workspace_size": (_sz, [_bp, _i32]),
+    "dsa_sparse_mla": (ctypes.c_int, [_bp, _vp, _vp, _f32, _f32, _vp, _i32, _vp, _vp, _vp, _sz,
+                                      _vp, _vp]),
+    "dsa_decode_workspace_size": (_sz, [_bp, _i32]),
+    "dsa_decode": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32, _f32,
+                                  _i32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "dsa_append_cache": (ctypes.c_int, [_bp, _vp, _vp, _f32, _vp, _vp, ctypes.c_int, _vp, _vp]),
+}
+
+
+def load():
+    """Load libdsa.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError("libdsa.so is not built (%s); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _status_str(s):
+    try:
+        return load().dsa_status_string(int(s)).decode()
+    except Exception:  # library missing while formatting an error
+        return "status"
+
+
+def dsa_status_string(s):
+    return load().dsa_status_string(int(s)).decode()
+
+
+def dsa_launch_count():
+    return int(load().dsa_launch_count())
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise DsaError(rc, what)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s has dtype %s" % (name, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Batch:
+    """Request metadata of one step: device int32 arrays plus the host copies
+    the library uses to size its grids."""
+
+    def __init__(self, q_offsets, seq_lens, block_table, num_pages, seq_lens_host=None,
+                 q_counts_host=None):
+        self.q_offsets = q_offsets.to(torch.int32).contiguous()
+        self.seq_lens = seq_lens.to(torch.int32).contiguous()
+        self.block_table = block_table.to(torch.int32).contiguous()
+        if seq_lens_host is None:
+            seq_lens_host = self.seq_lens.cpu().tolist()
+        if q_counts_host is None:
+            off = self.q_offsets.cpu().tolist()
+            q_counts_host = [off[i + 1] - off[i] for i in range(len(off) - 1)]
+        self.seq_lens_host = [int(v) for v in seq_lens_host]
+        self.q_counts_host = [int(v) for v in q_counts_host]
+        self.num_pages = int(num_pages)
+        self._c = _CBatch(len(self.seq_lens_host), sum(self.q_counts_host),
+                          max(self.q_counts_host), max(self.seq_lens_host), self.num_pages,
+                          int(self.block_table.shape[-1]), PAGE,
+                          self.q_offsets.data_ptr(), self.seq_lens.data_ptr(),
+                          self.block_table.data_ptr())
+
+    @property
+    def total_q(self):
+        return self._c.total_q
+
+    @property
+    def max_seq_len(self):
+        return self._c.max_seq_len
+
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
+def dsa_index_scores(batch, q_fp8, q_scale, w, index_pages, key_format, scores, score_ld=None,
+                     dev_status=None, stream=None):
+    if score_ld is None:
+        score_ld = scores.shape[-1]
+    rc = load().dsa_index_scores(batch.ref(), _ptr(q_fp8, torch.uint8, "q_fp8"),
+                                 _ptr(q_scale, torch.float32, "q_scale"),
+                                 _ptr(w, torch.float32, "w"),
+                                 _ptr(index_pages, torch.uint8, "index_pages"), int(key_format),
+                                 _ptr(scores, torch.float32, "scores"), int(score_ld),
+                                 _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_index_scores")
+
+
+def dsa_topk_workspace_size(batch, topk=TOPK):
+    return int(load().dsa_topk_workspace_size(batch.ref(), int(topk)))
+
+
+def dsa_topk(batch, scores, score_ld, topk, indices, ws=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().dsa_topk(batch.ref(), _ptr(scores, torch.float32, "scores"), int(score_ld),
+                         int(topk), _ptr(indices, torch.int32, "indices"), _ptr(ws), nbytes,
+                         _stream(stream))
+    _check(rc, "dsa_topk")
+
+
+def dsa_sparse_mla_workspace_size(batch, topk=TOPK):
+    return int(load().dsa_sparse_mla_workspace_size(batch.ref(), int(topk)))
+
+
+def dsa_sparse_mla(batch, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse=None,
+                   ws=None, dev_status=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().dsa_sparse_mla(batch.ref(), _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+                               _ptr(latent_pages, torch.uint8, "latent_pages"), float(kv_scale),
+                               float(sm_scale), _ptr(indices, torch.int32, "indices"), int(topk),
+                               _ptr(out, (torch.bfloat16, torch.int16), "out"),
+                               _ptr(lse, torch.float32, "lse"), _ptr(ws), nbytes,
+                               _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_sparse_mla")
+
+
+def dsa_decode_workspace_size(batch, topk=TOPK):
+    return int(load().dsa_decode_workspace_size(batch.ref(), int(topk)))
+
+
+def dsa_decode(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages, kv_scale,
+               sm_scale, topk, out, lse, indices, ws, dev_status=None, stream=None):
+    nbytes = ws.numel() * ws.element_size()
+    rc = load().dsa_decode(batch.ref(), _ptr(q_fp8, torch.uint8, "q_fp8"),
+                           _ptr(q_scale, torch.float32, "q_scale"), _ptr(w, torch.float32, "w"),
+                           _ptr(index_pages, torch.uint8, "index_pages"), int(key_format),
+                           _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+                           _ptr(latent_pages, torch.uint8, "latent_pages"), float(kv_scale),
+                           float(sm_scale), int(topk),
+                           _ptr(out, (torch.bfloat16, torch.int16), "out"),
+                           _ptr(lse, torch.float32, "lse"), _ptr(indices, torch.int32, "indices"),
+                           _ptr(ws), nbytes, _ptr(dev_status, torch.int32, "dev_status"),
+                           _stream(stream))
+    _check(rc, "dsa_decode")
+
+
+def dsa_append_cache(batch, new_keys, new_latent, kv_scale, index_pages, latent_pages, key_format,
+                     dev_status=None, stream=None):
+    rc = load().dsa_append_cache(batch.ref(), _ptr(new_keys, torch.float32, "new_keys"),
+                                 _ptr(new_latent, torch.float32, "new_latent"), float(kv_scale),
+                                 _ptr(index_pages, torch.uint8, "index_pages"),
+                                 _ptr(latent_pages, torch.uint8, "latent_pages"),
+                                 int(key_format), _ptr(dev_status, torch.int32, "dev_status"),
+                                 _stream(stream))
+    _check(rc, "dsa_append_cache")

@@ -1,0 +1,231 @@
+// api.cu -- the extern "C" boundary of libdsa.so: argument validation,
+// workspace arithmetic and kernel launches.  See include/dsa.h.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace dsa {
+cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
+                                const float* w, const void* pages, int key_format,
+                                float* scores, int64_t ld, int32_t* status, cudaStream_t stream);
+cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
+                        int32_t* out, cudaStream_t stream);
+cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
+                              float kv_scale, float sm_scale, const int32_t* indices, int K,
+                              uint16_t* out, float* lse, int32_t* status, cudaStream_t stream);
+cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const float* lat,
+                                float kv_scale, void* index_pages, void* latent_pages,
+                                int32_t* status, cudaStream_t stream);
+
+std::atomic<uint64_t> g_launches{0};
+}  // namespace dsa
+
+using namespace dsa;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dsa_status check_batch(const dsa_batch* bt) {
+    if (bt == nullptr) return DSA_ERR_INVALID_ARG;
+    if (bt->page_size != kPage) return DSA_ERR_UNSUPPORTED;
+    if (bt->num_requests < 1 || bt->total_q < 0 || bt->max_q_per_request < 0 ||
+        bt->max_seq_len < 1 || bt->num_pages < 1 || bt->max_pages < 1)
+        return DSA_ERR_INVALID_ARG;
+    if ((int64_t)bt->max_pages * kPage < bt->max_seq_len) return DSA_ERR_INVALID_ARG;
+    if (bt->max_q_per_request > bt->max_seq_len) return DSA_ERR_INVALID_ARG;
+    if ((int64_t)bt->total_q > (int64_t)bt->num_requests * bt->max_q_per_request)
+        return DSA_ERR_INVALID_ARG;
+    if (!bt->q_offsets || !bt->seq_lens || !bt->block_table) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+BatchArgs to_args(const dsa_batch* bt) {
+    BatchArgs a;
+    a.num_requests = bt->num_requests;
+    a.total_q = bt->total_q;
+    a.max_q = bt->max_q_per_request;
+    a.max_seq = bt->max_seq_len;
+    a.num_pages = bt->num_pages;
+    a.max_pages = bt->max_pages;
+    a.q_offsets = bt->q_offsets;
+    a.seq_lens = bt->seq_lens;
+    a.block_table = bt->block_table;
+    return a;
+}
+
+inline dsa_status cuda_status(cudaError_t e) {
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int64_t score_ld_for(const dsa_batch* bt) {
+    return (int64_t)align_up((size_t)bt->max_seq_len, 128);
+}
+
+dsa_status check_index_args(const dsa_batch* bt, const uint8_t* q8, const float* qscale,
+                            const float* w, const void* pages, dsa_key_format fmt,
+                            const float* scores, int64_t ld) {
+    if (fmt != DSA_KEYS_FP8_E4M3 && fmt != DSA_KEYS_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (!q8 || !qscale || !w || !pages || !scores) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q8) || !aligned16(pages) || !aligned16(scores) || !aligned16(qscale) ||
+        !aligned16(w))
+        return DSA_ERR_INVALID_ARG;
+    if (ld < bt->max_seq_len || (ld % 4) != 0) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+dsa_status check_mla_args(const dsa_batch* bt, const uint16_t* q_lat, const void* lat,
+                          const int32_t* indices, int32_t topk, const uint16_t* out,
+                          float kv_scale, float sm_scale) {
+    (void)bt;
+    if (topk != kTopK) return DSA_ERR_UNSUPPORTED;
+    if (!q_lat || !lat || !indices || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_lat) || !aligned16(lat) || !aligned16(indices) || !aligned16(out))
+        return DSA_ERR_INVALID_ARG;
+    if (!(kv_scale > 0.f) || !(sm_scale > 0.f)) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(dsa_status s) {
+    switch (s) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported shape or format";
+        case DSA_ERR_WORKSPACE: return "workspace too small";
+        case DSA_ERR_CUDA: return "CUDA error";
+        case DSA_ERR_DEVICE_CHECK: return "device check failed (page id or position out of range)";
+        case DSA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+uint64_t dsa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+dsa_status dsa_index_scores(const dsa_batch* batch, const uint8_t* q_fp8, const float* q_scale,
+                            const float* w, const void* index_pages, dsa_key_format key_format,
+                            float* scores, int64_t score_ld, int32_t* dev_status,
+                            dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    st = check_index_args(batch, q_fp8, q_scale, w, index_pages, key_format, scores, score_ld);
+    if (st != DSA_OK) return st;
+    if (batch->total_q == 0) return DSA_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(launch_index_scores(to_args(batch), q_fp8, q_scale, w, index_pages,
+                                           (int)key_format, scores, score_ld, dev_status,
+                                           (cudaStream_t)stream));
+}
+
+size_t dsa_topk_workspace_size(const dsa_batch* batch, int32_t topk) {
+    (void)batch;
+    (void)topk;
+    return 0;
+}
+
+dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_ld, int32_t topk,
+                    int32_t* indices, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (topk != kTopK) return DSA_ERR_UNSUPPORTED;
+    if (!scores || !indices) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(indices) || score_ld < batch->max_seq_len ||
+        (score_ld % 4) != 0)
+        return DSA_ERR_INVALID_ARG;
+    if (ws_bytes < dsa_topk_workspace_size(batch, topk)) return DSA_ERR_WORKSPACE;
+    (void)ws;
+    if (batch->total_q == 0) return DSA_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(launch_topk(to_args(batch), scores, score_ld, topk, indices,
+                                   (cudaStream_t)stream));
+}
+
+size_t dsa_sparse_mla_workspace_size(const dsa_batch* batch, int32_t topk) {
+    (void)batch;
+    (void)topk;
+    return 0;
+}
+
+dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const void* latent_pages,
+                          float kv_scale, float sm_scale, const int32_t* indices, int32_t topk,
+                          uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                          int32_t* dev_status, dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    st = check_mla_args(batch, q_lat, latent_pages, indices, topk, out, kv_scale, sm_scale);
+    if (st != DSA_OK) return st;
+    if (ws_bytes < dsa_sparse_mla_workspace_size(batch, topk)) return DSA_ERR_WORKSPACE;
+    (void)ws;
+    if (batch->total_q == 0) return DSA_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
+                                         indices, topk, out, lse, dev_status,
+                                         (cudaStream_t)stream));
+}
+
+size_t dsa_decode_workspace_size(const dsa_batch* batch, int32_t topk) {
+    if (check_batch(batch) != DSA_OK) return 0;
+    size_t scores = align_up((size_t)batch->total_q * score_ld_for(batch) * sizeof(float), 256);
+    return scores + align_up(dsa_topk_workspace_size(batch, topk), 256) +
+           align_up(dsa_sparse_mla_workspace_size(batch, topk), 256);
+}
+
+dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float* q_scale,
+                      const float* w, const void* index_pages, dsa_key_format key_format,
+                      const uint16_t* q_lat, const void* latent_pages, float kv_scale,
+                      float sm_scale, int32_t topk, uint16_t* out, float* lse, int32_t* indices,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    const int64_t ld = score_ld_for(batch);
+    float* scores = static_cast<float*>(ws);
+    st = check_index_args(batch, q_fp8, q_scale, w, index_pages, key_format,
+                          scores ? scores : reinterpret_cast<float*>(16), ld);
+    if (st != DSA_OK) return st;
+    st = check_mla_args(batch, q_lat, latent_pages, indices, topk, out, kv_scale, sm_scale);
+    if (st != DSA_OK) return st;
+    if (!ws || !aligned16(ws) || ws_bytes < dsa_decode_workspace_size(batch, topk))
+        return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0) return DSA_OK;
+    const BatchArgs a = to_args(batch);
+    cudaStream_t s = (cudaStream_t)stream;
+    g_launches.fetch_add(3, std::memory_order_relaxed);
+    cudaError_t e = launch_index_scores(a, q_fp8, q_scale, w, index_pages, (int)key_format,
+                                        scores, ld, dev_status, s);
+    if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, s);
+    if (e == cudaSuccess)
+        e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
+                              dev_status, s);
+    return cuda_status(e);
+}
+
+dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,
+                            const float* new_latent, float kv_scale, void* index_pages,
+                            void* latent_pages, dsa_key_format key_format, int32_t* dev_status,
+                            dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (new_keys && key_format != DSA_KEYS_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
+    if ((new_keys && !index_pages) || (new_latent && !latent_pages)) return DSA_ERR_INVALID_ARG;
+    if ((new_keys && (!aligned16(new_keys) || !aligned16(index_pages))) ||
+        (new_latent && (!aligned16(new_latent) || !aligned16(latent_pages))))
+        return DSA_ERR_INVALID_ARG;
+    if (new_latent && !(kv_scale > 0.f)) return DSA_ERR_INVALID_ARG;
+    if (batch->total_q == 0 || (!new_keys && !new_latent)) return DSA_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(launch_append_cache(to_args(batch), new_keys, new_latent, kv_scale,
+                                           index_pages, latent_pages, dev_status,
+                                           (cudaStream_t)stream));
+}
+
+}  // extern "C"

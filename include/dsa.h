@@ -1,0 +1,199 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA sparse-attention step library
+ * (libdsa.so).
+ *
+ * One layer of DeepSeek-style sparse attention as the web page "vLLM's Kimi
+ * K3.1 Pro day-0 support: sparse attention, DCP, zero-mismatch RL"
+ * (agentlenshq.com/ja/blogs/5e91cd0c...) describes it:
+ *   - section "What changed" (table and text): a light indexer with 32 heads
+ *     of 128 dims scores every earlier token of a query against one FP8 key per
+ *     token (132 bytes with its scale); the top 2048 tokens are kept and MLA
+ *     attention runs exactly on those tokens only;
+ *   - section "Sparse attention cuts long-context decode bandwidth": the full
+ *     576-byte FP8 latent is read only for the 2048 selected tokens;
+ *   - section "Packed KV cache": index keys are 132 B (FP8) or 68 B (MXFP4) per
+ *     token; kernels see small fixed-size pages through a block table that is
+ *     translated to page addresses before each step;
+ *   - section "Fused low-latency decode for DSA layers": a key-balanced scorer
+ *     and an exact top-k selection feed sparse attention; the new tokens' key
+ *     and latent are written into the caches.
+ * The pages do not state the indexer formula.  This library computes
+ *     score[t,s] = sum_h w[t,h] * ReLU( qhat[t,h,:] . khat[s,:] )
+ * with qhat = E4M3(q) * q_scale[t,h] and khat the dequantised key, and selects
+ * the top-k positions with ties broken toward the lower position.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers except the dsa_batch struct itself are DEVICE pointers owned
+ *     by the caller.  The library allocates nothing, keeps no state between
+ *     calls (apart from a launch counter) and is safe to call from several host
+ *     threads on different streams.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ *     NULL = legacy default stream).  Argument errors the host can see are
+ *     returned before anything is launched; nothing is written then.
+ *   - Device-side checks (a block-table entry outside [0, num_pages), a selected
+ *     position outside [0, seq_len)) skip the offending access and store the
+ *     first error code (DSA_ERR_DEVICE_CHECK) into *dev_status when dev_status
+ *     is not NULL.  The caller clears *dev_status to 0 and reads it after
+ *     synchronising.
+ *   - Query token t belongs to request b with q_offsets[b] <= t < q_offsets[b+1]
+ *     (n_b = q_offsets[b+1]-q_offsets[b] tokens).  Token j of request b sits at
+ *     position seq_lens[b] - n_b + j and sees positions
+ *     0 .. seq_lens[b] - n_b + j (causal multi-token rule; n_b = 1 is plain
+ *     decode, n_b new tokens is prefill-append).
+ *   - Position s of request b lives in physical page block_table[b*max_pages +
+ *     s/64], slot s%64.  page_size must be 64.
+ *   - Cache page layouts (one layer; a page id indexes both pools):
+ *       FP8 index page   (8448 B): 64 x 128 E4M3 key bytes, then 64 fp32 scales
+ *       MXFP4 index page (4352 B): 64 x 64 bytes of packed E2M1 (element 2i in
+ *                                  the low nibble), then 64 x 4 E8M0 scales,
+ *                                  one per block of 32 elements
+ *       latent page     (36864 B): 64 x 576 E4M3 bytes; one fp32 scale per layer
+ *     Pool bases must be 16-byte aligned.
+ *   - Only the shapes of the pages are supported: 32 indexer heads x 128 dims,
+ *     96 MLA heads x 576 latent dims with values = dims 0..511, top-k = 2048.
+ *     Other values return DSA_ERR_UNSUPPORTED.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,  /* NULL/misaligned pointer, inconsistent sizes */
+    DSA_ERR_UNSUPPORTED = 2,  /* a shape or format outside the supported set */
+    DSA_ERR_WORKSPACE = 3,    /* workspace too small */
+    DSA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    DSA_ERR_DEVICE_CHECK = 5, /* (device status word) page id or position out of range */
+    DSA_ERR_TIMEOUT = 6       /* (device status word) a bounded device wait expired */
+} dsa_status;
+
+typedef enum { DSA_KEYS_FP8_E4M3 = 0, DSA_KEYS_MXFP4 = 1 } dsa_key_format;
+
+enum {
+    DSA_PAGE_SIZE = 64,
+    DSA_INDEX_HEADS = 32,
+    DSA_INDEX_DIM = 128,
+    DSA_MLA_HEADS = 96,
+    DSA_LATENT_DIM = 576,
+    DSA_VALUE_DIM = 512,
+    DSA_TOPK = 2048,
+    DSA_FP8_INDEX_PAGE_BYTES = 8448,
+    DSA_MXFP4_INDEX_PAGE_BYTES = 4352,
+    DSA_LATENT_PAGE_BYTES = 36864
+};
+
+/* Request metadata of one step.  The struct lives in host memory; the three
+ * arrays are device pointers.  The host copies (total_q, max_q_per_request,
+ * max_seq_len) must agree with the device arrays; they size the grids. */
+typedef struct {
+    int32_t num_requests;       /* B >= 1 */
+    int32_t total_q;            /* T = q_offsets[B] */
+    int32_t max_q_per_request;  /* max_b n_b */
+    int32_t max_seq_len;        /* max_b seq_lens[b] */
+    int32_t num_pages;          /* pages in each cache pool */
+    int32_t max_pages;          /* row stride of block_table, >= ceil(max_seq_len/64) */
+    int32_t page_size;          /* must be 64 */
+    const int32_t* q_offsets;   /* device [B+1], q_offsets[0] = 0, non-decreasing */
+    const int32_t* seq_lens;    /* device [B], seq_lens[b] >= n_b */
+    const int32_t* block_table; /* device [B * max_pages] physical page ids */
+} dsa_batch;
+
+/* Human-readable name of a status code (static string). */
+const char* dsa_status_string(dsa_status s);
+
+/* Number of kernels this library has launched in this process (monotonic). */
+uint64_t dsa_launch_count(void);
+
+/* ---- indexer -------------------------------------------------------------
+ * Section "What changed" (32 heads x 128 dims, FP8 key with its scale, every
+ * earlier token scored) and, for MXFP4 keys, section "Native MXFP4 indexer"
+ * (fp32 accumulation, weighted reduction across heads).
+ *   q_fp8    [T,32,128] E4M3 bytes           (16-byte aligned)
+ *   q_scale  [T,32] fp32, > 0                (dequantisation of q per head)
+ *   w        [T,32] fp32                     (head weights)
+ *   index_pages: the FP8 or MXFP4 index pool
+ *   scores   [T, score_ld] fp32 output, score_ld >= max_seq_len and a multiple
+ *            of 4.  For token t of request b: scores[t,s] for s < visible(t);
+ *            -inf for visible(t) <= s < seq_lens[b]; entries s >= seq_lens[b]
+ *            are not written.
+ * The key scale (FP8) must be positive: the kernel applies it after the ReLU. */
+dsa_status dsa_index_scores(const dsa_batch* batch, const uint8_t* q_fp8,
+                            const float* q_scale, const float* w, const void* index_pages,
+                            dsa_key_format key_format, float* scores, int64_t score_ld,
+                            int32_t* dev_status, dsa_stream_t stream);
+
+/* ---- exact top-k -----------------------------------------------------------
+ * Section "What changed" (the top 2048 tokens are kept) and section "Fused
+ * low-latency decode" (exact top-k after the scorer).  For each query token t:
+ * the topk positions s < visible(t) with the largest scores[t,s], ties going to
+ * the lower position, written to indices[t, 0..topk) in ascending position
+ * order; when visible(t) <= topk all visible positions are written and the rest
+ * is -1.  Scores must not be NaN.  -0.0 and +0.0 are equal.
+ *   indices  [T, topk] int32 output (logical positions)
+ *   ws       device scratch of at least dsa_topk_workspace_size() bytes (may be
+ *            NULL when that size is 0)                                        */
+size_t dsa_topk_workspace_size(const dsa_batch* batch, int32_t topk);
+dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_ld,
+                    int32_t topk, int32_t* indices, void* ws, size_t ws_bytes,
+                    dsa_stream_t stream);
+
+/* ---- sparse MLA (absorbed form) --------------------------------------------
+ * Section "What changed" (MLA run exactly on the selected tokens) and section
+ * "Sparse attention cuts long-context decode bandwidth" (576-byte FP8 latents
+ * read for the selected tokens only).  For token t, head h (96 heads) over the
+ * selected positions I = {indices[t,i] >= 0}:
+ *   z[h,s] = sm_scale * kv_scale * (q_lat[t,h,:] . E4M3(latent[s,:]))  (576 dims)
+ *   out[t,h,:] = kv_scale * sum_s softmax_s(z[h,s]) * E4M3(latent[s,0:512])
+ *   lse[t,h]   = log sum_s exp(z[h,s])      (natural log; -inf if I is empty)
+ *   q_lat    [T,96,576] bf16 bits            (16-byte aligned)
+ *   indices  [T, topk] int32, entries -1 (skipped) or in [0, seq_lens[b])
+ *   out      [T,96,512] bf16 output (round to nearest even; 0 if I is empty)
+ *   lse      [T,96] fp32 output, may be NULL
+ *   ws       device scratch of at least dsa_sparse_mla_workspace_size() bytes */
+size_t dsa_sparse_mla_workspace_size(const dsa_batch* batch, int32_t topk);
+dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat,
+                          const void* latent_pages, float kv_scale, float sm_scale,
+                          const int32_t* indices, int32_t topk, uint16_t* out, float* lse,
+                          void* ws, size_t ws_bytes, int32_t* dev_status,
+                          dsa_stream_t stream);
+
+/* ---- the fused step ---------------------------------------------------------
+ * dsa_index_scores -> dsa_topk -> dsa_sparse_mla on one stream, the scores
+ * kept in the workspace (section "Fused low-latency decode for DSA layers").
+ * Arguments as above; indices [T, topk] is an output. */
+size_t dsa_decode_workspace_size(const dsa_batch* batch, int32_t topk);
+dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float* q_scale,
+                      const float* w, const void* index_pages, dsa_key_format key_format,
+                      const uint16_t* q_lat, const void* latent_pages, float kv_scale,
+                      float sm_scale, int32_t topk, uint16_t* out, float* lse,
+                      int32_t* indices, void* ws, size_t ws_bytes, int32_t* dev_status,
+                      dsa_stream_t stream);
+
+/* ---- cache append -------------------------------------------------------------
+ * Section "Fused low-latency decode for DSA layers" (the new token's index key
+ * and latent are written into the caches).  The T = q_offsets[B] new tokens
+ * are the query tokens of the batch; token j of request b goes to position
+ * seq_lens[b] - n_b + j.
+ *   new_keys   [T,128] fp32 (may be NULL: index pool untouched). FP8 pool only:
+ *              scale = amax/448 (1 if amax == 0), code = E4M3 round-to-nearest-
+ *              even saturating of (x / scale), both fp32 divisions.
+ *   new_latent [T,576] fp32 (may be NULL): code = E4M3 RNE satfinite (x / kv_scale).
+ * Only the new tokens' slots are written. */
+dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,
+                            const float* new_latent, float kv_scale, void* index_pages,
+                            void* latent_pages, dsa_key_format key_format,
+                            int32_t* dev_status, dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

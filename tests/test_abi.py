@@ -1,0 +1,82 @@
+"""The C-ABI library (CPU-only checks): it loads, exports every entry point
+that include/dsa.h declares, and rejects invalid host arguments before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dsa_sparse_attention_step_gb300 import _build
+    _build.build()
+    import dsa_sparse_attention_step_gb300 as dsa
+    return dsa.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"dsa_index_scores", "dsa_topk", "dsa_sparse_mla", "dsa_decode",
+            "dsa_append_cache"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    import dsa_sparse_attention_step_gb300 as dsa
+    assert dsa.dsa_status_string(0) == "ok"
+    assert "workspace" in dsa.dsa_status_string(3)
+
+
+def _cbatch(**kw):
+    import dsa_sparse_attention_step_gb300 as dsa
+    b = dsa._CBatch(1, 1, 1, 4096, 64, 64, 64, 16, 32, 48)
+    for k, v in kw.items():
+        setattr(b, k, v)
+    return b
+
+
+def test_invalid_host_arguments_return_before_launch(lib):
+    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    b = _cbatch()
+    # unsupported key format
+    assert lib.dsa_index_scores(ctypes.byref(b), fake, fake, fake, fake, 9, fake, 4096, None,
+                                None) == 2
+    # score row stride shorter than the longest sequence
+    assert lib.dsa_index_scores(ctypes.byref(b), fake, fake, fake, fake, 0, fake, 100, None,
+                                None) == 1
+    # misaligned query pointer
+    assert lib.dsa_index_scores(ctypes.byref(b), ctypes.c_void_p(4097), fake, fake, fake, 0,
+                                fake, 4096, None, None) == 1
+    # page size other than 64
+    b2 = _cbatch(page_size=32)
+    assert lib.dsa_topk(ctypes.byref(b2), fake, 4096, 2048, fake, None, 0, None) == 2
+    # top-k other than 2048
+    assert lib.dsa_topk(ctypes.byref(b), fake, 4096, 1000, fake, None, 0, None) == 2
+    # block table too short for the longest sequence
+    b3 = _cbatch(max_pages=10)
+    assert lib.dsa_topk(ctypes.byref(b3), fake, 4096, 2048, fake, None, 0, None) == 1
+    # NULL batch
+    assert lib.dsa_sparse_mla(None, fake, fake, 1.0, 1.0, fake, 2048, fake, None, None, 0,
+                              None, None) == 1
+    # non-positive latent scale
+    assert lib.dsa_sparse_mla(ctypes.byref(b), fake, fake, 0.0, 1.0, fake, 2048, fake, None,
+                              None, 0, None, None) == 1
+    # workspace too small for the fused step
+    need = lib.dsa_decode_workspace_size(ctypes.byref(b), 2048)
+    assert need >= 4096 * 4
+    assert lib.dsa_decode(ctypes.byref(b), fake, fake, fake, fake, 0, fake, fake, 1.0, 0.07,
+                          2048, fake, None, fake, fake, need - 1, None, None) == 3
+    # MXFP4 append is not provided
+    assert lib.dsa_append_cache(ctypes.byref(b), fake, None, 1.0, fake, None, 1, None,
+                                None) == 2

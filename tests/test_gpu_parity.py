@@ -1,0 +1,202 @@
+"""GPU parity of every C-ABI entry point against the CPU oracle, on seeded
+inputs that span several tiles and ragged tails, plus the edge cases: a
+single token, page and tile boundaries, contexts at and around 2048,
+multi-token causal rows, MXFP4 keys, page placement, batch invariance,
+determinism and device-side range checks."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_inputs as di
+import dsa_sparse_attention_step_gb300 as dsa
+import oracle
+from gpu_helpers import (GpuLayer, check_out, check_scores, check_topk_against_oracle,
+                         check_topk_against_scores)
+from oracle_helpers import batch_of, remap_pages
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "ctx1": ([1], 1, di.KEYS_FP8),
+    "page_edges": ([63, 64, 65, 127, 128, 129], 1, di.KEYS_FP8),
+    "around_topk": ([2047, 2048, 2049, 4096], 1, di.KEYS_FP8),
+    "multi_token": ([5000, 2300, 40], [5, 3, 2], di.KEYS_FP8),
+    "ragged_batch": ([9000, 3001, 130, 7777], [1, 2, 1, 4], di.KEYS_FP8),
+    "mxfp4": ([2047, 6000, 300], [1, 3, 1], di.KEYS_MXFP4),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    lens, nq, fmt = CASES[request.param]
+    layer = di.make_layer(lens, nq, fmt, seed=zlib.crc32(request.param.encode()) % 10000, extra_pages=3)
+    return layer, GpuLayer(layer)
+
+
+def test_index_scores(case):
+    layer, gl = case
+    st = gl.status()
+    S = gl.scores(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check_scores(layer, S)
+
+
+def test_topk_exact(case):
+    layer, gl = case
+    S_gpu = gl.scores()
+    idx = gl.topk(S_gpu)
+    rows = list(range(layer.total_q))
+    vis = batch_of(layer).visible(rows)
+    check_topk_against_scores(idx, S_gpu, vis, rows)
+    S, A, _ = check_scores(layer, S_gpu)
+    check_topk_against_oracle(idx, S, A, vis, rows)
+
+
+def test_sparse_mla(case):
+    layer, gl = case
+    S_gpu = gl.scores()
+    idx = gl.topk(S_gpu)
+    st = gl.status()
+    out, lse = gl.mla(idx, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_out, ref_lse = oracle.sparse_mla(batch_of(layer), layer.q_lat, layer.latent_pages,
+                                         layer.kv_scale, layer.sm_scale, idx.cpu().numpy())
+    check_out(out, lse, ref_out, ref_lse, list(range(layer.total_q)))
+
+
+def test_decode_fused(case):
+    layer, gl = case
+    st = gl.status()
+    out, lse, idx = gl.decode(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_idx, ref_out, ref_lse = oracle.decode(
+        batch_of(layer), layer.q8, layer.qscale, layer.w, layer.index_pages, layer.key_format,
+        layer.q_lat, layer.latent_pages, layer.kv_scale, layer.sm_scale)
+    rows = list(range(layer.total_q))
+    vis = batch_of(layer).visible(rows)
+    got = idx.cpu().numpy()
+    # the selections are identical unless a threshold near-tie fell the other
+    # way; in that case compare attention on the GPU's own selection
+    if not np.array_equal(got, ref_idx):
+        S, A, _ = check_scores(layer, gl.scores())
+        check_topk_against_oracle(idx, S, A, vis, rows)
+        ref_out, ref_lse = oracle.sparse_mla(batch_of(layer), layer.q_lat, layer.latent_pages,
+                                             layer.kv_scale, layer.sm_scale, got)
+    check_out(out, lse, ref_out, ref_lse, rows)
+
+
+def test_small_context_selects_everything():
+    layer = di.make_layer([1, 700, 2048], 1, seed=3)
+    gl = GpuLayer(layer)
+    _, _, idx = gl.decode()
+    got = idx.cpu().numpy()
+    for t, n in enumerate([1, 700, 2048]):
+        assert np.array_equal(got[t, :n], np.arange(n)) and (got[t, n:] == -1).all()
+
+
+def test_all_equal_scores_pick_lowest_positions():
+    """Adversarial ties: w = 0 makes every score 0; the lowest 2048 positions win."""
+    layer = di.make_layer([9000, 3000], [2, 1], seed=4)
+    layer.w.zero_()
+    gl = GpuLayer(layer)
+    S = gl.scores()
+    idx = gl.topk(S).cpu().numpy()
+    assert (idx == np.arange(2048)[None, :]).all()
+
+
+def test_page_placement_is_bit_identical():
+    layer = di.make_layer([6000, 2500], [2, 1], seed=8, extra_pages=5)
+    a = GpuLayer(layer).decode()
+    b = GpuLayer(remap_pages(layer, 77)).decode()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_deterministic_repeat():
+    layer = di.make_layer([20000, 17000], 1, seed=9)
+    gl = GpuLayer(layer)
+    a = gl.decode()
+    b = gl.decode()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_batch_invariance():
+    """A request's result does not depend on the other requests of the batch."""
+    lens = [18000, 25000, 31000]
+    layer = di.make_layer(lens, 1, seed=12)
+    full = GpuLayer(layer).decode()
+    for b in range(len(lens)):
+        d = dict(layer.__dict__)
+        d.update(q_offsets=torch.tensor([0, 1], dtype=torch.int32),
+                 seq_lens=layer.seq_lens[b:b + 1].clone(),
+                 block_table=layer.block_table[b:b + 1].clone(), q8=layer.q8[b:b + 1],
+                 qscale=layer.qscale[b:b + 1], w=layer.w[b:b + 1], q_lat=layer.q_lat[b:b + 1],
+                 seq_lens_host=[lens[b]], q_counts_host=[1])
+        one = GpuLayer(di.Layer(**d)).decode()
+        for x, y in zip(full, one):
+            assert torch.equal(x[b:b + 1], y)
+
+
+def test_bad_page_id_sets_device_status():
+    layer = di.make_layer([3000], 1, seed=13)
+    layer.block_table[0, 5] = layer.num_pages + 10
+    gl = GpuLayer(layer)
+    st = gl.status()
+    gl.decode(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5  # DSA_ERR_DEVICE_CHECK
+
+
+def test_bad_index_sets_device_status():
+    layer = di.make_layer([3000], 1, seed=14)
+    gl = GpuLayer(layer)
+    idx = torch.full((1, 2048), -1, dtype=torch.int32, device="cuda:0")
+    idx[0, 0] = 3000  # == seq_len: out of range
+    idx[0, 1] = 17
+    st = gl.status()
+    out, lse = gl.mla(idx, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5
+    ref_out, _ = oracle.sparse_mla(batch_of(layer), layer.q_lat, layer.latent_pages,
+                                   layer.kv_scale, layer.sm_scale,
+                                   np.array([[17] + [-1] * 2047], np.int32))
+    check_out(out, None, ref_out, None, [0])
+
+
+def test_append_cache_bit_exact():
+    layer = di.make_layer([130, 70, 64, 3000], [5, 1, 2, 7], seed=41, extra_pages=1)
+    keys, lat = di.append_payload(layer, seed=3)
+    keys[1] *= 1e-3
+    keys[2] = 0.0
+    gl = GpuLayer(layer)
+    st = gl.status()
+    dsa.dsa_append_cache(gl.batch, keys.cuda(), lat.cuda(), layer.kv_scale, gl.g.index_pages,
+                         gl.g.latent_pages, di.KEYS_FP8, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ip, lp = oracle.append_cache(batch_of(layer), keys, lat, layer.kv_scale, layer.index_pages,
+                                 layer.latent_pages)
+    assert np.array_equal(gl.g.index_pages.cpu().numpy(), ip)
+    assert np.array_equal(gl.g.latent_pages.cpu().numpy(), lp)
+
+
+def test_host_validation_errors():
+    layer = di.make_layer([100], 1, seed=1)
+    gl = GpuLayer(layer)
+    S = torch.empty(1, 128, dtype=torch.float32, device="cuda:0")
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_index_scores(gl.batch, gl.g.q8, gl.g.qscale, gl.g.w, gl.g.index_pages, 7, S, 128)
+    assert e.value.status == 2
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_index_scores(gl.batch, gl.g.q8, gl.g.qscale, gl.g.w, gl.g.index_pages, 0, S, 50)
+    assert e.value.status == 1
+    idx = torch.empty(1, 1024, dtype=torch.int32, device="cuda:0")
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_topk(gl.batch, S, 128, 1024, idx)
+    assert e.value.status == 2
