@@ -14,12 +14,14 @@ import torch
 __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path", "load",
            "dsa_status_string", "dsa_launch_count", "dsa_index_scores", "dsa_topk",
            "dsa_topk_workspace_size", "dsa_sparse_mla", "dsa_sparse_mla_workspace_size",
-           "dsa_decode", "dsa_decode_workspace_size", "dsa_append_cache"]
+           "dsa_decode", "dsa_decode_workspace_size", "dsa_decode_noalloc",
+           "NOALLOC_SCRATCH_BYTES", "dsa_append_cache"]
 
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
 TOPK = 2048
 PAGE = 64
+NOALLOC_SCRATCH_BYTES = 16 << 20  # DSA_NOALLOC_SCRATCH_BYTES of include/dsa.h
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -62,6 +64,8 @@ _SIGS = {
     "dsa_decode_workspace_size": (_sz, [_bp, _i32]),
     "dsa_decode": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32, _f32,
                                   _i32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "dsa_decode_noalloc": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32,
+                                          _f32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dsa_append_cache": (ctypes.c_int, [_bp, _vp, _vp, _f32, _vp, _vp, ctypes.c_int, _vp, _vp]),
 }
 
@@ -215,6 +219,27 @@ def dsa_decode(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_
                            _ptr(ws), nbytes, _ptr(dev_status, torch.int32, "dev_status"),
                            _stream(stream))
     _check(rc, "dsa_decode")
+
+
+def dsa_decode_noalloc(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages,
+                       kv_scale, sm_scale, topk, out, lse, indices, dev_status=None, stream=None):
+    """dsa_decode with no workspace argument, for callers that cannot allocate
+    device memory on the call path: the scratch is a fixed array of
+    NOALLOC_SCRATCH_BYTES inside the library, shared by all calls on a device
+    (calls that overlap on the GPU race on it).  Batches that need more scratch
+    raise DsaError with status 3."""
+    rc = load().dsa_decode_noalloc(batch.ref(), _ptr(q_fp8, torch.uint8, "q_fp8"),
+                                   _ptr(q_scale, torch.float32, "q_scale"),
+                                   _ptr(w, torch.float32, "w"),
+                                   _ptr(index_pages, torch.uint8, "index_pages"), int(key_format),
+                                   _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+                                   _ptr(latent_pages, torch.uint8, "latent_pages"),
+                                   float(kv_scale), float(sm_scale), int(topk),
+                                   _ptr(out, (torch.bfloat16, torch.int16), "out"),
+                                   _ptr(lse, torch.float32, "lse"),
+                                   _ptr(indices, torch.int32, "indices"),
+                                   _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_decode_noalloc")
 
 
 def dsa_append_cache(batch, new_keys, new_latent, kv_scale, index_pages, latent_pages, key_format,

@@ -1,0 +1,62 @@
+// noalloc.cu -- dsa_decode for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain device scratch on the call path: an
+// engine that pre-reserves all device memory for its own pool, or code that
+// must not run the device-synchronising cudaMalloc/cudaFree.  For them the
+// fused step takes its scratch from one file-scope device array of fixed size
+// instead of a caller workspace.  The pages have no counterpart of this entry
+// point; it is an addition of this library.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace {
+
+// The shared scratch of every dsa_decode_noalloc call on a device.  Each GPU
+// that loads the library holds one copy until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+// Device address of g_noalloc_scratch per device, looked up once per device.
+// In host code the symbol itself is only a host-side stand-in and must never
+// be handed to a kernel.
+std::atomic<void*> g_scratch_ptr[kMaxDevices];
+
+dsa_status scratch_for_current_device(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return DSA_ERR_CUDA;
+    }
+    void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        // set-up, with `dev` current: the device address of this device's copy
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return DSA_ERR_CUDA;
+        }
+        g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" dsa_status dsa_decode_noalloc(const dsa_batch* batch, const uint8_t* q_fp8,
+                                         const float* q_scale, const float* w,
+                                         const void* index_pages, dsa_key_format key_format,
+                                         const uint16_t* q_lat, const void* latent_pages,
+                                         float kv_scale, float sm_scale, int32_t topk,
+                                         uint16_t* out, float* lse, int32_t* indices,
+                                         int32_t* dev_status, dsa_stream_t stream) {
+    if (batch == nullptr) return DSA_ERR_INVALID_ARG;
+    const size_t need = dsa_decode_workspace_size(batch, topk);
+    if (need > (size_t)DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    dsa_status st = scratch_for_current_device(&scratch);
+    if (st != DSA_OK) return st;
+    return dsa_decode(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages,
+                      kv_scale, sm_scale, topk, out, lse, indices, scratch,
+                      (size_t)DSA_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+}

@@ -25,8 +25,9 @@
  * Conventions shared by every entry point
  *   - All pointers except the dsa_batch struct itself are DEVICE pointers owned
  *     by the caller.  The library allocates nothing, keeps no state between
- *     calls (apart from a launch counter) and is safe to call from several host
- *     threads on different streams.
+ *     calls (apart from a launch counter and the fixed scratch array of
+ *     dsa_decode_noalloc) and is safe to call from several host threads on
+ *     different streams.
  *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
  *     NULL = legacy default stream).  Argument errors the host can see are
  *     returned before anything is launched; nothing is written then.
@@ -176,6 +177,34 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
                       float sm_scale, int32_t topk, uint16_t* out, float* lse,
                       int32_t* indices, void* ws, size_t ws_bytes, int32_t* dev_status,
                       dsa_stream_t stream);
+
+/* ---- the fused step without caller scratch ------------------------------------
+ * No counterpart on the pages: an addition of this library.  Same arguments,
+ * outputs and results as dsa_decode, minus the workspace: its scratch (the
+ * score rows) lives in one file-scope device array of DSA_NOALLOC_SCRATCH_BYTES
+ * bytes inside the library, so the call itself allocates nothing.  It is meant
+ * for callers that cannot obtain device memory on the call path, such as an
+ * engine whose device memory is entirely pre-reserved by its own pool (the KV
+ * cache), or code running where the device-synchronising cudaMalloc/cudaFree
+ * may not be called.
+ *   - A batch whose dsa_decode_workspace_size() exceeds
+ *     DSA_NOALLOC_SCRATCH_BYTES is rejected with DSA_ERR_WORKSPACE before
+ *     anything is launched.
+ *   - The first call on each device looks up that device's copy of the array
+ *     (with the device current); make that first call before any stream
+ *     capture on the device.
+ *   - Every GPU that loads the library holds the array until the process exits.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents; nothing in it needs to start at zero.  Calls whose executions
+ *     overlap on the GPU (different streams, no ordering between them) race on
+ *     it and give undefined results: order them on one stream or with events. */
+enum { DSA_NOALLOC_SCRATCH_BYTES = 16 << 20 };
+dsa_status dsa_decode_noalloc(const dsa_batch* batch, const uint8_t* q_fp8,
+                              const float* q_scale, const float* w, const void* index_pages,
+                              dsa_key_format key_format, const uint16_t* q_lat,
+                              const void* latent_pages, float kv_scale, float sm_scale,
+                              int32_t topk, uint16_t* out, float* lse, int32_t* indices,
+                              int32_t* dev_status, dsa_stream_t stream);
 
 /* ---- cache append -------------------------------------------------------------
  * Section "Fused low-latency decode for DSA layers" (the new token's index key
