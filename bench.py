@@ -319,8 +319,11 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.barrier()
     launches_timed = dsa.dsa_launch_count() - l0
-    # graph replays do not pass through the library: count its kernels per step
-    per_step_launches = 3
+    # graph replays do not pass through the library's counter: count the
+    # kernels of one step by a direct call, then scale to the timed steps
+    c0 = dsa.dsa_launch_count()
+    run_steps(1, nxt)
+    per_step_launches = dsa.dsa_launch_count() - c0
     gpu_launches = per_step_launches * args.steps
     elapsed = ev0.elapsed_time(ev1) / 1000.0
     if world > 1:
@@ -369,10 +372,12 @@ def run_ours(args, rank, world, local):
                                        stream=stream), reps)
     kern["topk"] = time_graph(
         lambda i: dsa.dsa_topk(batches[i], scores, ld, dsa.TOPK, idx, None, stream=stream), reps)
+    mla_ws = torch.empty(max(16, dsa.dsa_sparse_mla_workspace_size(batches[0])),
+                         dtype=torch.uint8, device=dev)
     kern["sparse_mla"] = time_graph(
         lambda i: dsa.dsa_sparse_mla(batches[i], layers[i].q_lat, layers[i].latent_pages,
                                      layers[i].kv_scale, layers[i].sm_scale, idx, dsa.TOPK, out,
-                                     lse, None, status, stream=stream), reps)
+                                     lse, mla_ws, status, stream=stream), reps)
     kbytes = {"indexer": wl.indexer_bytes(lens, q_counts, fmt),
               "topk": wl.topk_bytes(lens, q_counts),
               "sparse_mla": wl.mla_bytes(lens, q_counts)}

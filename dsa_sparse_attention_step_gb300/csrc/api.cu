@@ -13,7 +13,9 @@ cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, in
                         int32_t* out, cudaStream_t stream);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
-                              uint16_t* out, float* lse, int32_t* status, cudaStream_t stream);
+                              uint16_t* out, float* lse, void* ws, int32_t* status,
+                              cudaStream_t stream);
+size_t sparse_mla_workspace_bytes(int total_q, int K);
 cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const float* lat,
                                 float kv_scale, void* index_pages, void* latent_pages,
                                 int32_t* status, cudaStream_t stream);
@@ -151,9 +153,8 @@ dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_l
 }
 
 size_t dsa_sparse_mla_workspace_size(const dsa_batch* batch, int32_t topk) {
-    (void)batch;
-    (void)topk;
-    return 0;
+    if (check_batch(batch) != DSA_OK || topk != kTopK) return 0;
+    return sparse_mla_workspace_bytes(batch->total_q, topk);
 }
 
 dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const void* latent_pages,
@@ -164,12 +165,12 @@ dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const v
     if (st != DSA_OK) return st;
     st = check_mla_args(batch, q_lat, latent_pages, indices, topk, out, kv_scale, sm_scale);
     if (st != DSA_OK) return st;
-    if (ws_bytes < dsa_sparse_mla_workspace_size(batch, topk)) return DSA_ERR_WORKSPACE;
-    (void)ws;
+    const size_t need = dsa_sparse_mla_workspace_size(batch, topk);
+    if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return DSA_ERR_WORKSPACE;
     if (batch->total_q == 0) return DSA_OK;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_launches.fetch_add(need > 0 ? 2 : 1, std::memory_order_relaxed);
     return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
-                                         indices, topk, out, lse, dev_status,
+                                         indices, topk, out, lse, ws, dev_status,
                                          (cudaStream_t)stream));
 }
 
@@ -199,13 +200,17 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
     if (batch->total_q == 0) return DSA_OK;
     const BatchArgs a = to_args(batch);
     cudaStream_t s = (cudaStream_t)stream;
-    g_launches.fetch_add(3, std::memory_order_relaxed);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const size_t off_topk = align_up((size_t)batch->total_q * ld * sizeof(float), 256);
+    const size_t off_mla = off_topk + align_up(dsa_topk_workspace_size(batch, topk), 256);
+    const bool combine = dsa_sparse_mla_workspace_size(batch, topk) > 0;
+    g_launches.fetch_add(combine ? 4 : 3, std::memory_order_relaxed);
     cudaError_t e = launch_index_scores(a, q_fp8, q_scale, w, index_pages, (int)key_format,
                                         scores, ld, dev_status, s);
     if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, s);
     if (e == cudaSuccess)
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
-                              dev_status, s);
+                              base + off_mla, dev_status, s);
     return cuda_status(e);
 }
 
