@@ -149,10 +149,17 @@ indexer_scores_kernel(BatchArgs bt, const uint8_t* __restrict__ q8,
 
 }  // namespace
 
+bool indexer_tc_supported(const BatchArgs& bt);
+cudaError_t launch_index_scores_fp8_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
+                                       const float* w, const void* pages, float* scores,
+                                       int64_t ld, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
                                 const float* w, const void* pages, int key_format,
                                 float* scores, int64_t ld, int32_t* status,
                                 cudaStream_t stream) {
+    if (key_format == DSA_KEYS_FP8_E4M3 && indexer_tc_supported(bt))
+        return launch_index_scores_fp8_tc(bt, q8, qscale, w, pages, scores, ld, status, stream);
     dim3 grid((bt.max_seq + kTileKeys - 1) / kTileKeys, bt.num_requests,
               (bt.max_q + kTokChunk - 1) / kTokChunk);
     if (key_format == DSA_KEYS_FP8_E4M3)

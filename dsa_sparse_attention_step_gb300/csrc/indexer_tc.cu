@@ -1,0 +1,431 @@
+// indexer_tc.cu -- DSA indexer scores for FP8 keys on tcgen05 tensor cores.
+//
+//   score[t,s] = kscale[s] * sum_h (w[t,h] * q_scale[t,h]) * ReLU(q8[t,h,:] . k8[s,:])
+// i.e. sum_h w[t,h] ReLU(qhat[t,h,:] . khat[s,:]) with the positive key and
+// query scales pulled through the ReLU.
+// "vLLM's Kimi K3.1 Pro day-0 support", section "What changed": 32 indexer
+// heads x 128 dims, one FP8 key of 132 bytes with its scale per token, every
+// earlier token scored; section "Fused low-latency decode for DSA layers": a
+// key-balanced scorer.
+//
+// The work is a list of units (request b, query group g of up to G tokens,
+// tile of 128 keys = two 64-token pages); every group of a request covers all
+// of the request's tiles (positions past a token's causal limit get -inf).
+// A persistent grid splits the unit list into equal contiguous ranges, so the
+// keys, not the queries, are balanced across SMs.  Per unit:
+//   D[128 keys x N] = K8[128 x 128] . Q8[N x 128]^T,  N = 32 heads x G tokens,
+// tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM, double
+// buffered).  Key pages arrive by TMA (128-byte swizzle) into a 6-stage ring,
+// the query group by TMA into a double buffer.  Eight epilogue warps read the
+// accumulator (thread = key), apply ReLU, the weighted head sum, the key scale
+// and the causal mask, and store fp32 scores.
+//
+// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocation and the
+// MMA-issuing thread, warps 2-9 epilogue.  Every wait is bounded.
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kTile = 128;                     // keys per unit
+constexpr int kStages = 6;
+constexpr int kStageBytes = kTile * kIdxDim;   // 16384
+constexpr int kMaxG = 8;                       // tokens per group
+constexpr int kMaxN = kIdxHeads * kMaxG;       // 256
+constexpr int kQBufBytes = kMaxN * kIdxDim;    // 32768
+constexpr int kMaxReq = 4096;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+
+constexpr int kOffStage = 0;
+constexpr int kOffQ = kOffStage + kStages * kStageBytes;        // 98304
+constexpr int kOffW = kOffQ + 2 * kQBufBytes;                    // 163840
+constexpr int kOffReq = kOffW + 2 * kMaxG * kIdxHeads * 4;       // 165888
+constexpr int kOffBar = kOffReq + (kMaxReq + 1) * 4 + 12;        // 182292 -> keep 8-aligned
+constexpr int kOffBarA = (kOffBar + 7) / 8 * 8;
+constexpr int kSmemBytes = kOffBarA + 512;
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+
+struct Bars {
+    uint64_t full[kStages];   // TMA -> MMA: key tile landed
+    uint64_t empty[kStages];  // MMA -> TMA: stage free (commit)
+    uint64_t tfull[2];        // MMA -> epilogue: accumulator ready (commit)
+    uint64_t tempty[2];       // epilogue -> MMA: accumulator drained (256 arrivals)
+    uint64_t qfull[2];        // TMA -> MMA: query group landed
+    uint64_t qempty[2];       // MMA -> TMA: query buffer free (commit)
+    uint64_t done;            // MMA issuer: all its MMAs have completed
+    uint32_t tmem_base;
+    int abort_flag;
+    int total_units;
+};
+
+struct IdxParams {
+    BatchArgs bt;
+    const float* qscale;
+    const float* w;
+    const uint8_t* pages;
+    float* scores;
+    int64_t ld;
+    int G;                    // tokens per group (1..8)
+    int N;                    // 32 * G
+    int32_t* status;
+};
+
+// Per-request unit count: groups x tiles.
+__device__ __forceinline__ int request_units(const BatchArgs& bt, int b, int G) {
+    if (!request_ok(bt, b, nullptr)) return 0;
+    const int nb = __ldg(bt.q_offsets + b + 1) - __ldg(bt.q_offsets + b);
+    const int seq = __ldg(bt.seq_lens + b);
+    return ((nb + G - 1) / G) * ((seq + kTile - 1) / kTile);
+}
+
+// Cursor over the unit list of this CTA.
+struct Cursor {
+    int b, g, tile;     // current unit
+    int ntile;          // tiles of request b
+    int ngroup;         // groups of request b
+    int q0, nb, seq;    // request metadata
+};
+
+__device__ __forceinline__ void cursor_load_request(Cursor& c, const BatchArgs& bt, int G) {
+    c.q0 = __ldg(bt.q_offsets + c.b);
+    c.nb = __ldg(bt.q_offsets + c.b + 1) - c.q0;
+    c.seq = __ldg(bt.seq_lens + c.b);
+    const bool ok = request_ok(bt, c.b, nullptr);
+    c.ngroup = ok ? (c.nb + G - 1) / G : 0;
+    c.ntile = ok ? (c.seq + kTile - 1) / kTile : 0;
+}
+
+// Position the cursor on global unit u (req_units = exclusive prefix, B+1).
+__device__ __forceinline__ void cursor_seek(Cursor& c, const BatchArgs& bt, const int* req_units,
+                                            int G, int u) {
+    int lo = 0, hi = bt.num_requests - 1;
+    while (lo < hi) {  // last b with req_units[b] <= u
+        const int mid = (lo + hi + 1) >> 1;
+        if (req_units[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    c.b = lo;
+    cursor_load_request(c, bt, G);
+    const int r = u - req_units[lo];
+    c.g = (c.ntile > 0) ? r / c.ntile : 0;
+    c.tile = (c.ntile > 0) ? r % c.ntile : 0;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const BatchArgs& bt, int G) {
+    if (++c.tile < c.ntile) return;
+    c.tile = 0;
+    if (++c.g < c.ngroup) return;
+    c.g = 0;
+    do {
+        ++c.b;
+        if (c.b >= bt.num_requests) return;
+        cursor_load_request(c, bt, G);
+    } while (c.ngroup == 0 || c.ntile == 0);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
+                      const __grid_constant__ CUtensorMap tm_q, const IdxParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    uint8_t* sStage = sm + kOffStage;
+    uint8_t* sQ = sm + kOffQ;
+    float* sW = reinterpret_cast<float*>(sm + kOffW);        // [2][8][32]
+    int* sReq = reinterpret_cast<int*>(sm + kOffReq);         // [B+1]
+    Bars* bars = reinterpret_cast<Bars*>(sm + kOffBarA);
+    __shared__ int s_warp_sum[kThreads / 32];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const BatchArgs& bt = p.bt;
+    const int G = p.G, N = p.N;
+    volatile int* abort_flag = &bars->abort_flag;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bars->full[i], 1);
+            mbar_init(&bars->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->tfull[i], 1);
+            mbar_init(&bars->tempty[i], kEpiThreads);
+            mbar_init(&bars->qfull[i], 1);
+            mbar_init(&bars->qempty[i], 1);
+        }
+        mbar_init(&bars->done, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_keys);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    // ---- unit table: exclusive prefix of per-request unit counts ----
+    int carry = 0;
+    for (int b0 = 0; b0 < bt.num_requests; b0 += kThreads) {
+        const int b = b0 + tid;
+        const int u = (b < bt.num_requests) ? request_units(bt, b, G) : 0;
+        int incl = u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp_sum[warp] = incl;
+        __syncthreads();
+        int before = 0, chunk = 0;
+        for (int w2 = 0; w2 < kThreads / 32; ++w2) {
+            const int s2 = s_warp_sum[w2];
+            if (w2 < warp) before += s2;
+            chunk += s2;
+        }
+        if (b < bt.num_requests) sReq[b] = carry + before + incl - u;
+        carry += chunk;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        sReq[bt.num_requests] = carry;
+        bars->total_units = carry;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const int total = bars->total_units;
+    const uint32_t tmem = bars->tmem_base;
+    const int u_begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+    const int u_end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+    const int n_units = u_end - u_begin;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0 && n_units > 0) {
+            Cursor c;
+            cursor_seek(c, bt, sReq, G, u_begin);
+            int gcount = 0, pb = -1, pg = -1;
+            for (int i = 0; i < n_units; ++i) {
+                if (c.b != pb || c.g != pg) {
+                    const int x = gcount & 1;
+                    if (gcount >= 2 &&
+                        !mbar_wait(&bars->qempty[x], ((gcount >> 1) - 1) & 1, abort_flag))
+                        break;
+                    mbar_arrive_expect_tx(&bars->qfull[x], (uint32_t)N * kIdxDim);
+                    tma_load_2d(sQ + x * kQBufBytes, &tm_q, 0, (c.q0 + c.g * G) * kIdxHeads,
+                                &bars->qfull[x]);
+                    ++gcount;
+                    pb = c.b;
+                    pg = c.g;
+                }
+                const int st = i % kStages;
+                const int k = i / kStages;
+                if (k >= 1 && !mbar_wait(&bars->empty[st], (k - 1) & 1, abort_flag)) break;
+                uint32_t bytes = 0;
+                int pages[2] = {-1, -1};
+                for (int h = 0; h < 2; ++h) {
+                    const int s0 = c.tile * kTile + h * kPage;
+                    if (s0 < c.seq) {
+                        pages[h] = page_lookup(bt, c.b, s0 / kPage, p.status);
+                        if (pages[h] >= 0) bytes += kPage * kIdxDim;
+                    }
+                }
+                mbar_arrive_expect_tx(&bars->full[st], bytes);
+                for (int h = 0; h < 2; ++h)
+                    if (pages[h] >= 0)
+                        tma_load_2d(sStage + st * kStageBytes + h * (kPage * kIdxDim), &tm_keys, 0,
+                                    pages[h] * (kFp8PageBytes / kIdxDim), &bars->full[st]);
+                cursor_next(c, bt, G);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issue ----------------
+        if (lane == 0 && n_units > 0) {
+            Cursor c;
+            cursor_seek(c, bt, sReq, G, u_begin);
+            const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 128, N, false, false);
+            const uint32_t sa = smem_u32(sStage), sq = smem_u32(sQ);
+            int gcount = 0, pb = -1, pg = -1;
+            bool ok = true;
+            for (int i = 0; i < n_units && ok; ++i) {
+                if (c.b != pb || c.g != pg) {
+                    if (gcount >= 1) mma_commit(&bars->qempty[(gcount - 1) & 1]);
+                    ok = mbar_wait(&bars->qfull[gcount & 1], (gcount >> 1) & 1, abort_flag);
+                    ++gcount;
+                    pb = c.b;
+                    pg = c.g;
+                }
+                const int st = i % kStages;
+                const int acc = i & 1;
+                if (ok) ok = mbar_wait(&bars->full[st], (i / kStages) & 1, abort_flag);
+                if (ok && i >= 2) ok = mbar_wait(&bars->tempty[acc], ((i >> 1) - 1) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t qa = sq + ((gcount - 1) & 1) * kQBufBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = smem_desc(sa + st * kStageBytes + kk * 32, 16, 1024,
+                                                  kSwizzle128B);
+                    const uint64_t bd = smem_desc(qa + kk * 32, 16, 1024, kSwizzle128B);
+                    mma_f8f6f4(tmem + acc * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->empty[st]);
+                mma_commit(&bars->tfull[acc]);
+                cursor_next(c, bt, G);
+            }
+        }
+        if (lane == 0) {
+            // nothing may still write TMEM when it is released
+            mma_commit(&bars->done);
+            mbar_wait(&bars->done, 0, abort_flag);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (thread = key) ----------------
+        const int etid = tid - 64;            // 0..255
+        const int quarter = warp & 3;         // TMEM lanes 32*quarter..+31
+        const int half = (warp - 2) >> 2;     // token parity handled by this warp
+        if (n_units > 0) {
+            Cursor c;
+            cursor_seek(c, bt, sReq, G, u_begin);
+            int gcount = 0, pb = -1, pg = -1;
+            for (int i = 0; i < n_units; ++i) {
+                const int gtok0 = c.g * G;                    // first token of the group
+                const int gr = min(G, c.nb - gtok0);          // real tokens in the group
+                if (c.b != pb || c.g != pg) {
+                    float* wdst = sW + (gcount & 1) * (kMaxG * kIdxHeads);
+                    for (int e = etid; e < gr * kIdxHeads; e += kEpiThreads) {
+                        const int64_t t = c.q0 + gtok0 + e / kIdxHeads;
+                        const int h = e % kIdxHeads;
+                        wdst[e] = __ldg(p.w + t * kIdxHeads + h) * __ldg(p.qscale + t * kIdxHeads + h);
+                    }
+                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                    ++gcount;
+                    pb = c.b;
+                    pg = c.g;
+                }
+                const float* wq = sW + ((gcount - 1) & 1) * (kMaxG * kIdxHeads);
+                const int s = c.tile * kTile + quarter * 32 + lane;
+                const bool in_seq = s < c.seq;
+                float kscale = 0.f;
+                bool page_ok = false;
+                if (in_seq) {
+                    const int pg2 = __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + s / kPage);
+                    if (pg2 >= 0 && pg2 < bt.num_pages) {
+                        page_ok = true;
+                        kscale = __ldg(reinterpret_cast<const float*>(
+                                           p.pages + (int64_t)pg2 * kFp8PageBytes + kPage * kIdxDim) +
+                                       (s % kPage));
+                    }
+                }
+                const int acc = i & 1;
+                if (!mbar_wait(&bars->tfull[acc], (i >> 1) & 1, abort_flag)) break;
+                tc_fence_after();
+                for (int j = half; j < gr; j += 2) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v);
+                    tmem_wait_ld();
+                    const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
+                    float sc = 0.f;
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; ++h4) {
+                        const float4 ww = w4[h4];
+                        sc = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), sc);
+                        sc = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), sc);
+                        sc = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), sc);
+                        sc = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sc);
+                    }
+                    if (in_seq) {
+                        const int vis = c.seq - c.nb + gtok0 + j + 1;
+                        p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
+                            (s < vis && page_ok) ? sc * kscale : -INFINITY;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars->tempty[acc]);
+                cursor_next(c, bt, G);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && tid == 0) record_error(p.status, DSA_ERR_TIMEOUT);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D byte tensor [rows, 128] with 128-byte rows, box [box_rows, 128], 128-B swizzle.
+bool encode_rows128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool indexer_tc_supported(const BatchArgs& bt) { return bt.num_requests <= kMaxReq; }
+
+cudaError_t launch_index_scores_fp8_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
+                                       const float* w, const void* pages, float* scores,
+                                       int64_t ld, int32_t* status, cudaStream_t stream) {
+    IdxParams p;
+    p.bt = bt;
+    p.qscale = qscale;
+    p.w = w;
+    p.pages = static_cast<const uint8_t*>(pages);
+    p.scores = scores;
+    p.ld = ld;
+    p.G = bt.max_q < kMaxG ? (bt.max_q > 0 ? bt.max_q : 1) : kMaxG;
+    p.N = kIdxHeads * p.G;
+    p.status = status;
+    CUtensorMap tm_keys, tm_q;
+    // the index pool as rows of 128 bytes: page p = rows [66p, 66p + 64) + 2 scale rows
+    if (!encode_rows128(&tm_keys, pages, (uint64_t)bt.num_pages * (kFp8PageBytes / kIdxDim),
+                        kPage) ||
+        !encode_rows128(&tm_q, q8, (uint64_t)bt.total_q * kIdxHeads, (uint32_t)p.N))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(indexer_fp8_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    indexer_fp8_tc_kernel<<<sms, kThreads, kSmemAlloc, stream>>>(tm_keys, tm_q, p);
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

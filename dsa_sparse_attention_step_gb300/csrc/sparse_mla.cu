@@ -157,7 +157,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         tmem_relinquish();
     }
 
-    // ---- preamble: row ids of the selected tokens, query into shared memory
+    // ---- preamble ------------------------------------------------------------
+    // (1) the bf16 query, 96 x 576 = 6912 vectors of 16 bytes, copied
+    //     asynchronously into its f16 positions (converted in place below)
+    const __nv_bfloat16* qsrc = p.q_lat + (int64_t)t * kMlaHeads * kLatDim;
+    if (ok_tok) {
+        for (int v = tid; v < kMlaHeads * kLatDim / 8; v += kThreads) {
+            const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
+            cp_async16(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16), qsrc + 8 * v);
+        }
+    }
+    cp_async_commit();
+    // (2) row ids (page * 64 + slot) of this CTA's index slots
     for (int k = tid; k < p.split_keys; k += kThreads) {
         int row = -1;
         if (ok_tok) {
@@ -171,115 +182,124 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         }
         sRow[k] = row;
     }
-    float amax = 0.f;
-    if (warp < 8) {
-        // 96 x 576 bf16 = 6912 vectors of 8, stored raw (bf16 bits) at their
-        // f16 positions and converted in place once the scale is known
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.q_lat + (int64_t)t * kMlaHeads * kLatDim);
-        for (int v = tid; v < kMlaHeads * kLatDim / 8; v += 256) {
-            const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
-            const uint4 raw = ok_tok ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] << 16)));
-                amax = fmaxf(amax, fabsf(__uint_as_float(wv[i] & 0xFFFF0000u)));
-            }
-            const int slab = c / 8, col = (c % 8) * 16;
-            *reinterpret_cast<uint4*>(sQ + slab * kQSlabBytes + sw128(h, col)) = raw;
-        }
-    }
-    amax = warp_max(amax);
-    if (lane == 0) s_amax[warp] = amax;
     if (tid < 2 * 128) sF[tid] = 1.f;
+    cp_async_wait_all();
     __syncthreads();
-    for (int i = tid; i < n_tiles; i += kThreads) {
-        uint32_t m = 0;
-        for (int j = 0; j < kTileKeys; ++j) m |= (sRow[i * kTileKeys + j] >= 0 ? 1u : 0u) << j;
-        sMask[i] = m;
-    }
-    float qmax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qmax = fmaxf(qmax, s_amax[i]);
-    // scale 2^-e with max|q| * 2^-e < 2^15: nothing overflows f16 and every
-    // element within 2^-14 of the largest keeps its 8 bf16 significant bits
+
+    const bool producer = (warp >= 4 && warp < 8);
     int e = 0;
-    if (qmax > 0.f) {
-        int ex;
-        frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
-        e = ex - 15;
-    }
-    const float qmul = ldexpf(1.0f, -e);
-    if (warp < 8) {
-        for (int v = tid; v < kMlaHeads * kLatDim / 8; v += 256) {
+    if (!producer) {
+        // (3) warps 0-3 and 8: valid-slot masks, then the query bf16 -> f16 in
+        //     place while the producers already gather latents.  First try
+        //     scale 1; if the largest |q| is >= 2^15 or < 2^-8, convert again
+        //     from global memory with a power-of-two scale 2^-e chosen so that
+        //     max|q| * 2^-e lies in [2^14, 2^15).
+        const int ctid = (warp == 8) ? 128 + lane : tid;  // 0..159
+        for (int i = ctid; i < n_tiles; i += 160) {
+            uint32_t m = 0;
+            for (int j = 0; j < kTileKeys; ++j) m |= (sRow[i * kTileKeys + j] >= 0 ? 1u : 0u) << j;
+            sMask[i] = m;
+        }
+        float amax = 0.f;
+        for (int v = ctid; v < kMlaHeads * kLatDim / 8; v += 160) {
             const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
-            const int slab = c / 8, col = (c % 8) * 16;
-            uint4* dst = reinterpret_cast<uint4*>(sQ + slab * kQSlabBytes + sw128(h, col));
-            const uint4 raw = *dst;
+            uint4* dst = reinterpret_cast<uint4*>(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16));
+            const uint4 raw = ok_tok ? *dst : make_uint4(0, 0, 0, 0);
             const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
             uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
-                                  __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
+            for (int i = 0; i < 4; ++i) {
+                const float a = __uint_as_float(wv[i] << 16);
+                const float c2 = __uint_as_float(wv[i] & 0xFFFF0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c2)));
+                o[i] = pack_half2(a, c2);
+            }
             *dst = make_uint4(o[0], o[1], o[2], o[3]);
         }
+        amax = warp_max(amax);
+        if (lane == 0) s_amax[warp] = amax;
+        asm volatile("bar.sync 2, 160;" ::: "memory");
+        float qmax = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
+        qmax = fmaxf(qmax, s_amax[8]);
+        if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
+            int ex;
+            frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
+            e = ex - 15;
+            const float qmul = ldexpf(1.0f, -e);
+            for (int v = ctid; v < kMlaHeads * kLatDim / 8; v += 160) {
+                const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qsrc) + v);
+                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
+                                      __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
+                *reinterpret_cast<uint4*>(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
         fence_proxy_async_smem();
+        tc_fence_before();
+        asm volatile("bar.sync 2, 160;" ::: "memory");
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     // z in log2 units per unit of the f16 accumulator
     const float zscale = p.sm_scale * p.kv_scale * ldexpf(1.0f, e) * 1.4426950408889634f;
 
-    if (warp >= 4 && warp < 8) {
+    if (producer) {
         // ---------------- producers: gather + E4M3 -> f16 ----------------
+        // 32 rows x 36 vectors of 16 bytes = 1152 vectors -> 9 per thread per
+        // tile; two tiles of loads are kept in flight (registers A and B)
         const int ptid = tid - 128;
-        // 32 rows x 36 vectors of 16 bytes = 1152 vectors -> 9 per thread
-        uint4 raw[9];
-#define DSA_MLA_LOAD_TILE(i_)                                                            \
+        uint4 rawA[9], rawB[9];
+#define DSA_MLA_LOAD(raw_, i_)                                                           \
     _Pragma("unroll") for (int u = 0; u < 9; ++u) {                                      \
         const int v = ptid + 128 * u;                                                     \
         const int r = v / 36, c = v % 36;                                                 \
         const int row = sRow[(i_) * kTileKeys + r];                                       \
-        raw[u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(                       \
-                                        p.latent_pages + (int64_t)row * kLatDim) + c)     \
-                            : make_uint4(0, 0, 0, 0);                                     \
+        raw_[u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(                      \
+                                         p.latent_pages + (int64_t)row * kLatDim) + c)    \
+                             : make_uint4(0, 0, 0, 0);                                    \
     }
-        if (n_tiles > 0) { DSA_MLA_LOAD_TILE(0) }
-        for (int i = 0; i < n_tiles; ++i) {
-            const int st = i & 1;
-            if (i >= 2 && !mbar_wait(&bars->empty[st], ((i - 2) >> 1) & 1, abort_flag)) break;
-            uint8_t* dstL = sL + st * kLBytes;
-#pragma unroll
-            for (int u = 0; u < 9; ++u) {
-                const int v = ptid + 128 * u;
-                const int r = v / 36, c = v % 36;
-                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-                uint32_t hv[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                        (__nv_fp8x2_storage_t)(wv[k] & 0xFFFF), __NV_E4M3);
-                    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                        (__nv_fp8x2_storage_t)(wv[k] >> 16), __NV_E4M3);
-                    hv[2 * k] = *reinterpret_cast<uint32_t*>(&lo);
-                    hv[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hi);
-                }
-                const int slab = c / 4, col = (c % 4) * 32;
-                uint8_t* base = dstL + slab * kLSlabBytes;
-                *reinterpret_cast<uint4*>(base + sw128(r, col)) =
-                    make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                *reinterpret_cast<uint4*>(base + sw128(r, col + 16)) =
-                    make_uint4(hv[4], hv[5], hv[6], hv[7]);
-            }
+#define DSA_MLA_STORE(raw_, st_)                                                         \
+    _Pragma("unroll") for (int u = 0; u < 9; ++u) {                                      \
+        const int v = ptid + 128 * u;                                                     \
+        const int r = v / 36, c = v % 36;                                                 \
+        const uint32_t wv[4] = {raw_[u].x, raw_[u].y, raw_[u].z, raw_[u].w};              \
+        uint32_t hv[8];                                                                   \
+        _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                   \
+            __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(                                  \
+                (__nv_fp8x2_storage_t)(wv[k] & 0xFFFF), __NV_E4M3);                       \
+            __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(                                  \
+                (__nv_fp8x2_storage_t)(wv[k] >> 16), __NV_E4M3);                          \
+            hv[2 * k] = *reinterpret_cast<uint32_t*>(&lo);                                \
+            hv[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hi);                            \
+        }                                                                                 \
+        uint8_t* base = sL + (st_) * kLBytes + (c / 4) * kLSlabBytes;                     \
+        *reinterpret_cast<uint4*>(base + sw128(r, (c % 4) * 32)) =                        \
+            make_uint4(hv[0], hv[1], hv[2], hv[3]);                                       \
+        *reinterpret_cast<uint4*>(base + sw128(r, (c % 4) * 32 + 16)) =                   \
+            make_uint4(hv[4], hv[5], hv[6], hv[7]);                                       \
+    }
+        if (n_tiles > 0) { DSA_MLA_LOAD(rawA, 0) }
+        if (n_tiles > 1) { DSA_MLA_LOAD(rawB, 1) }
+        for (int i = 0; i < n_tiles; i += 2) {
+            if (i >= 2 && !mbar_wait(&bars->empty[0], ((i - 2) >> 1) & 1, abort_flag)) break;
+            DSA_MLA_STORE(rawA, 0)
             fence_proxy_async_smem();
-            mbar_arrive(&bars->full[st]);
-            if (i + 1 < n_tiles) { DSA_MLA_LOAD_TILE(i + 1) }
+            mbar_arrive(&bars->full[0]);
+            if (i + 2 < n_tiles) { DSA_MLA_LOAD(rawA, i + 2) }
+            if (i + 1 >= n_tiles) break;
+            if (i + 1 >= 2 && !mbar_wait(&bars->empty[1], ((i - 1) >> 1) & 1, abort_flag)) break;
+            DSA_MLA_STORE(rawB, 1)
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->full[1]);
+            if (i + 3 < n_tiles) { DSA_MLA_LOAD(rawB, i + 3) }
         }
-#undef DSA_MLA_LOAD_TILE
+#undef DSA_MLA_LOAD
+#undef DSA_MLA_STORE
     } else if (warp == 8) {
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
@@ -397,40 +417,55 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             tc_fence_before();
             mbar_arrive(&bars->pfull[st]);
         }
-        // ---------------- epilogue ----------------
-        const bool ok = mbar_wait(&bars->done, 0, abort_flag) && !*abort_flag;
+        // ---------------- end of softmax: per-head normaliser ----------------
+        const bool ok = mbar_wait(&bars->done, 0, abort_flag);
         tc_fence_after();
-        sF[256 + h] = m_ref;
-        sF[384 + h] = l;
-        softmax_sync();
-        if (ok && ok_tok) {
-            for (int mtile = 0; mtile < 4; ++mtile) {
-                const int d = 128 * mtile + 32 * warp + lane;
-                for (int c = 0; c < 3; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tmem_addr(tmem, 32 * warp, kColO + 96 * mtile + 32 * c), o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int hh = 32 * c + j;
-                        const float lh = sF[384 + hh];
-                        const float v = (lh > 0.f) ? __uint_as_float(o[j]) / lh : 0.f;
-                        if (p.splits == 1) {
-                            p.out[((int64_t)t * kMlaHeads + hh) * kVDim + d] =
-                                __float2bfloat16_rn(v * p.kv_scale);
-                        } else {
-                            p.part_o[(((int64_t)t * p.splits + split) * kMlaHeads + hh) * kVDim +
-                                     d] = __float2half_rn(v);
-                        }
-                    }
-                }
+        const float scale_out = (p.splits == 1) ? p.kv_scale : 1.f;
+        sF[256 + h] = (l > 0.f) ? scale_out / l : 0.f;
+        if (ok && ok_tok && real) {
+            const float lse2 = (l > 0.f) ? m_ref + log2f(l) : -INFINITY;
+            if (p.splits == 1) {
+                if (p.lse) p.lse[(int64_t)t * kMlaHeads + h] = lse2 * 0.6931471805599453f;
+            } else {
+                p.part_lse[((int64_t)t * p.splits + split) * kMlaHeads + h] = lse2;
             }
-            if (real) {
-                const float lse2 = (l > 0.f) ? m_ref + log2f(l) : -INFINITY;
-                if (p.splits == 1) {
-                    if (p.lse) p.lse[(int64_t)t * kMlaHeads + h] = lse2 * 0.6931471805599453f;
-                } else {
-                    p.part_lse[((int64_t)t * p.splits + split) * kMlaHeads + h] = lse2;
+        }
+        tc_fence_before();
+    }
+
+    // ---------------- epilogue: O^T / l -> bf16 output or f16 partial ----------
+    // warps 0-3 take latent-dim tiles 0-1, warps 4-7 tiles 2-3 (a warp reads
+    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads
+    if (warp < 8) {
+        asm volatile("bar.sync 3, 256;" ::: "memory");
+        tc_fence_after();
+        if (!*abort_flag && ok_tok) {
+            const int lq = warp & 3;
+            const int mt0 = (warp < 4) ? 0 : 2;
+            for (int c = 0; c < 3; ++c) {
+                float inv[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(sF + 256 + 32 * c + j);
+                    inv[j] = v4.x; inv[j + 1] = v4.y; inv[j + 2] = v4.z; inv[j + 3] = v4.w;
+                }
+                for (int mt = mt0; mt < mt0 + 2; ++mt) {
+                    const int d = 128 * mt + 32 * lq + lane;
+                    uint32_t o[32];
+                    tmem_ld32(tmem_addr(tmem, 32 * lq, kColO + 96 * mt + 32 * c), o);
+                    tmem_wait_ld();
+                    if (p.splits == 1) {
+                        __nv_bfloat16* dst = p.out + ((int64_t)t * kMlaHeads + 32 * c) * kVDim + d;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            dst[(int64_t)j * kVDim] = __float2bfloat16_rn(__uint_as_float(o[j]) * inv[j]);
+                    } else {
+                        __half* dst = p.part_o +
+                                      (((int64_t)t * p.splits + split) * kMlaHeads + 32 * c) * kVDim + d;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            dst[(int64_t)j * kVDim] = __float2half_rn(__uint_as_float(o[j]) * inv[j]);
+                    }
                 }
             }
         }
