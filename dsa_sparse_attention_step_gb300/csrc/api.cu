@@ -11,6 +11,7 @@ cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const fl
                                 float* scores, int64_t ld, int32_t* status, cudaStream_t stream);
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
                         int32_t* out, cudaStream_t stream);
+bool topk_supported(int max_seq);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status,
@@ -139,7 +140,7 @@ dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_l
                     int32_t* indices, void* ws, size_t ws_bytes, dsa_stream_t stream) {
     dsa_status st = check_batch(batch);
     if (st != DSA_OK) return st;
-    if (topk != kTopK) return DSA_ERR_UNSUPPORTED;
+    if (topk != kTopK || !topk_supported(batch->max_seq_len)) return DSA_ERR_UNSUPPORTED;
     if (!scores || !indices) return DSA_ERR_INVALID_ARG;
     if (!aligned16(scores) || !aligned16(indices) || score_ld < batch->max_seq_len ||
         (score_ld % 4) != 0)
@@ -195,6 +196,7 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
     if (st != DSA_OK) return st;
     st = check_mla_args(batch, q_lat, latent_pages, indices, topk, out, kv_scale, sm_scale);
     if (st != DSA_OK) return st;
+    if (!topk_supported(batch->max_seq_len)) return DSA_ERR_UNSUPPORTED;
     if (!ws || !aligned16(ws) || ws_bytes < dsa_decode_workspace_size(batch, topk))
         return DSA_ERR_WORKSPACE;
     if (batch->total_q == 0) return DSA_OK;

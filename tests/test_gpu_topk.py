@@ -1,0 +1,84 @@
+"""dsa_topk on crafted score matrices (independent of the indexer), bit-exact
+against the oracle's selection on the same fp32 scores: heavy ties, signed
+zeros, negative scores, rows of every length class, batch sizes that select
+different cluster sizes, and inputs that force the streaming fallback."""
+import numpy as np
+import pytest
+import torch
+
+import dsa_sparse_attention_step_gb300 as dsa
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _batch(seq_lens, q_counts):
+    dev = "cuda:0"
+    off = [0]
+    for n in q_counts:
+        off.append(off[-1] + n)
+    max_pages = (max(seq_lens) + 63) // 64
+    return dsa.Batch(torch.tensor(off, dtype=torch.int32, device=dev),
+                     torch.tensor(seq_lens, dtype=torch.int32, device=dev),
+                     torch.zeros(len(seq_lens), max_pages, dtype=torch.int32, device=dev), 1,
+                     seq_lens, q_counts)
+
+
+def _visible(seq_lens, q_counts):
+    vis = []
+    for s, n in zip(seq_lens, q_counts):
+        vis += [s - n + j + 1 for j in range(n)]
+    return np.array(vis, np.int64)
+
+
+def _run(seq_lens, q_counts, scores):
+    b = _batch(seq_lens, q_counts)
+    ld = scores.shape[1]
+    S = torch.from_numpy(scores.astype(np.float32)).cuda()
+    idx = torch.full((b.total_q, dsa.TOPK), -7, dtype=torch.int32, device="cuda:0")
+    dsa.dsa_topk(b, S, ld, dsa.TOPK, idx)
+    torch.cuda.synchronize()
+    want = oracle.topk(scores.astype(np.float32).astype(np.float64),
+                       _visible(seq_lens, q_counts), dsa.TOPK)
+    got = idx.cpu().numpy()
+    for r in range(got.shape[0]):
+        assert np.array_equal(got[r], want[r]), "row %d" % r
+
+
+def _scores(rng, T, ld, kind):
+    if kind == "normal":
+        return rng.standard_normal((T, ld))
+    if kind == "few_levels":          # heavy ties everywhere
+        return rng.integers(-3, 4, size=(T, ld)).astype(np.float64) * 0.5
+    if kind == "signed_zero":         # +0 / -0 and a few positives
+        s = np.where(rng.random((T, ld)) < 0.5, 0.0, -0.0)
+        s[rng.random((T, ld)) < 0.01] = 1.0
+        return s
+    if kind == "offset":              # narrow band far from zero (one first-digit bin)
+        return 1000.0 + rng.random((T, ld)) * 1e-3
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["normal", "few_levels", "signed_zero", "offset"])
+@pytest.mark.parametrize("shape", [([30000, 2049, 4096], [1, 1, 2]),     # few tokens: clusters
+                                   ([131072], [1]),                      # one long row
+                                   ([9000] * 40, [2] * 40)])             # 80 tokens: one CTA each
+def test_topk_crafted(kind, shape):
+    lens, counts = shape
+    rng = np.random.default_rng(len(lens) * 7 + sum(counts))
+    T = sum(counts)
+    ld = ((max(lens) + 127) // 128) * 128
+    _run(lens, counts, _scores(rng, T, ld, kind))
+
+
+def test_topk_all_equal_long_rows_use_streaming_selection():
+    # the threshold bin holds far more keys than the candidate buffers
+    lens, counts = [70000, 300000], [1, 1]
+    ld = ((max(lens) + 127) // 128) * 128
+    _run(lens, counts, np.full((2, ld), 2.5))
+
+
+def test_topk_one_million_positions():
+    rng = np.random.default_rng(11)
+    lens = [1 << 20]
+    _run(lens, [1], rng.standard_normal((1, 1 << 20)))
