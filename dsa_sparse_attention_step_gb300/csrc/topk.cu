@@ -5,25 +5,31 @@
 // layers": an exact top-k selection follows the scorer.
 //
 // For query token t with `vis` visible positions (vis > k): the k positions
-// with the largest scores, ties to the lower position, in ascending order.
-// Scores are mapped to order-preserving uint32 keys (-0 folded onto +0) and the
-// k-th largest key tau is found by a most-significant-digit radix select with
-// digits of 12, 10 and 10 bits.
+// with the largest scores, ties to the lower position, written in ascending
+// position order.  Scores are mapped to order-preserving uint32 keys (-0
+// folded onto +0); tau denotes the k-th largest key.
 //
-// One thread-block cluster of `cs` CTAs per query token; CTA r owns a
-// contiguous, 32-aligned slice of the positions and keeps its slice's results
-// in shared memory.  Per digit the CTAs build histograms of their slice
-// (streaming the scores from global memory), the cluster sums them through
-// distributed shared memory, and every CTA derives the same digit.  As soon as
-// the keys sharing the threshold prefix fit the candidate buffers, one more
-// streaming pass marks the positions above the prefix in a bitmap and copies
-// the candidates (key, position) into shared memory; the remaining digits are
-// resolved on the candidates only.  Keys equal to tau are taken lowest
-// position first across the cluster (prefix of per-CTA counts), and each CTA
-// writes its selected positions in order at its offset in the output row.
-// Inputs whose threshold bin keeps more keys than the buffers hold (e.g. huge
-// runs of equal scores) resolve all digits by streaming and select in a final
-// ordered streaming pass.
+// One thread-block cluster of `cs` CTAs per query token (cs = 1 for rows that
+// fit in shared memory, which are then kept resident there); CTA r owns a
+// contiguous, 32-aligned slice of the positions.
+//   1. Threshold estimate.  A histogram over the top 12 key bits of a sample
+//      (every 16th 32-position chunk of the slice; every position when the row
+//      is resident) is summed over the cluster through distributed shared
+//      memory, and the bin b_lo holding the sample's ~1.25k-th largest key
+//      (exactly the k-th when every position is sampled) is chosen.
+//   2. One pass over the slice copies every key in a bin >= b_lo, with its
+//      position, into shared memory (warp-aggregated appends).
+//   3. If the cluster holds at least k candidates (so every key >= tau is
+//      among them) and nothing overflowed, CTA 0 gathers the candidates,
+//      resolves tau exactly by radix select (digits of 12, 10, 10 bits) and
+//      tells every CTA how many of its keys equal to tau it takes (lowest
+//      positions first).  Otherwise an exact fallback resolves the digits by
+//      passes over the whole slice.
+//   4. Each CTA marks its selected positions in a bitmap and writes them in
+//      order at its offset in the output row (block-wide scan).
+// Global reads are 16-byte vectors, four in flight per thread.
+#include <cstddef>
+
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -37,28 +43,38 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
-constexpr int kBins = 4096;                  // first digit: 12 bits
-constexpr int kCandCap = 8192;               // candidates per CTA
-constexpr int kSliceMax = 1 << 18;           // positions per CTA (bitmap capacity)
-constexpr int kWords = kSliceMax / 32;       // 8192 bitmap words
+constexpr int kBins = 4096;                   // first digit: 12 bits
+constexpr int kSampleStride = 16;             // sample one 32-position chunk in 16
+constexpr int kResidentMax = 32768;           // rows kept in shared memory
+constexpr int kSliceMax = 1 << 18;            // streaming positions per CTA
 
-struct TopkShared {
-    uint32_t hist[kBins];       // this CTA's histogram (read remotely by the cluster)
-    uint32_t tot[kBins];        // cluster-wide histogram
-    uint32_t bits[kWords];      // selected positions of the slice
-    uint32_t cand_key[kCandCap];
-    int32_t cand_pos[kCandCap];
-    int32_t warp_tot[kWarps + 1];
-    uint32_t xchg[4];           // per-CTA values read by the cluster
-    uint32_t s_digit, s_rem, s_count;
+template <bool kRes>
+struct Cfg {
+    static constexpr int kWords = kRes ? kResidentMax / 32 : kSliceMax / 32;
+    static constexpr int kCand = kRes ? 4096 : 8192;
+    static constexpr int kKeys = kRes ? kResidentMax : 4;
 };
+
+template <bool kRes>
+struct TopkSmem {
+    uint32_t hist[kBins];                      // this CTA's histogram (cluster-visible)
+    uint32_t tot[kBins];                       // cluster-wide histogram
+    uint32_t bits[Cfg<kRes>::kWords];          // selected positions of the slice
+    uint32_t eqbits[Cfg<kRes>::kWords];        // positions whose key equals tau
+    uint32_t cand_key[Cfg<kRes>::kCand];
+    int32_t cand_pos[Cfg<kRes>::kCand];
+    int32_t warp_tot[kWarps + 1];
+    uint32_t xchg[16];                         // per-CTA values read or written by the cluster
+    uint32_t s_digit, s_rem, s_count, s_flag;
+    alignas(16) uint32_t keys[Cfg<kRes>::kKeys];  // resident rows: the order keys (16-B loads)
+};
+static_assert(offsetof(TopkSmem<true>, keys) % 16 == 0, "vector loads of the resident keys");
 
 // Radix digits: bits 31..20, 19..10, 9..0 of the order key.
 __device__ __forceinline__ int dig_shift(int level) { return level == 0 ? 20 : (level == 1 ? 10 : 0); }
 __device__ __forceinline__ uint32_t dig_mask(int level) { return level == 0 ? 0xFFFu : 0x3FFu; }
 
-// Block-wide exclusive prefix sum of v (1024 threads); returns the prefix and
-// the total through *total.
+// Block-wide exclusive prefix sum (1024 threads); *total gets the block sum.
 __device__ __forceinline__ int block_excl_sum(int v, int* warp_tot, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -87,76 +103,134 @@ __device__ __forceinline__ int block_excl_sum(int v, int* warp_tot, int* total) 
     return r;
 }
 
-// Warp-aggregated shared-memory histogram increment.
+// Shared-memory histogram increment (the atomic unit serialises only lanes
+// of a warp that hit the same bin).
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
-    const unsigned act = __ballot_sync(0xffffffffu, active);
-    if (!active) return;
-    const unsigned peers = __match_any_sync(act, bin);
-    if ((__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(peers));
+    if (active) atomicAdd(&hist[bin], 1u);
 }
 
-// Sum the cluster's histograms (nb bins) into tot, then find the digit d such
-// that count(digits > d) < rem <= count(digits >= d); stores the digit, the
-// remaining count within it and the count of the digit's bin.
-__device__ void cluster_digit(TopkShared& S, cg::cluster_group& cluster, int nb, uint32_t rem) {
-    const int cs = (int)cluster.num_blocks();
-    cluster.sync();  // every histogram of the cluster is complete
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
-        uint32_t v = 0;
-        for (int r = 0; r < cs; ++r) v += cluster.map_shared_rank(S.hist, r)[i];
-        S.tot[i] = v;
-    }
-    cluster.sync();  // remote reads done before any histogram is reset
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const int per = nb / 32;
-        uint32_t c = 0;
-        for (int i = 0; i < per; ++i) c += S.tot[per * lane + i];
-        uint32_t incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t u = __shfl_down_sync(0xffffffffu, incl, o);
-            if (lane + o < 32) incl += u;
-        }
-        const uint32_t above = incl - c;
-        if (above < rem && rem <= above + c) {
-            uint32_t run = above;
-            for (int i = per - 1; i >= 0; --i) {
-                const uint32_t h = S.tot[per * lane + i];
-                if (run + h >= rem) {
-                    S.s_digit = (uint32_t)(per * lane + i);
-                    S.s_rem = rem - run;
-                    S.s_count = h;
-                    break;
-                }
-                run += h;
+// Find digit d over nb bins of h with count(> d) < rem <= count(>= d): sets
+// s_digit and s_rem (= rem minus the count above d).  All threads call it.
+template <bool kRes>
+__device__ void find_digit(TopkSmem<kRes>& S, const uint32_t* h, int nb, uint32_t rem) {
+    const int per = nb / kThreads;  // 4 or 1
+    const int tid = threadIdx.x;
+    // thread tid owns the bins of descending rank [per*tid, per*tid + per)
+    uint32_t part = 0;
+    for (int i = 0; i < per; ++i) part += h[nb - 1 - (per * tid + i)];
+    int tot;
+    const uint32_t above = (uint32_t)block_excl_sum((int)part, S.warp_tot, &tot);
+    if (above < rem && rem <= above + part) {
+        uint32_t run = above;
+        for (int i = 0; i < per; ++i) {
+            const int bin = nb - 1 - (per * tid + i);
+            if (run + h[bin] >= rem) {
+                S.s_digit = (uint32_t)bin;
+                S.s_rem = rem - run;
+                break;
             }
+            run += h[bin];
         }
     }
     __syncthreads();
 }
 
-// Exclusive prefix over the cluster ranks of the per-CTA value in xchg[slot];
-// also returns the cluster total.
-__device__ uint32_t cluster_prefix(TopkShared& S, cg::cluster_group& cluster, int slot,
-                                   uint32_t* total) {
-    cluster.sync();
-    const int cs = (int)cluster.num_blocks(), me = (int)cluster.block_rank();
-    uint32_t before = 0, tot = 0;
-    for (int r = 0; r < cs; ++r) {
-        const uint32_t v = cluster.map_shared_rank(S.xchg, r)[slot];
-        if (r < me) before += v;
-        tot += v;
+// Sum the cluster's histograms into tot (cs > 1) or use the local one.
+template <bool kRes>
+__device__ const uint32_t* cluster_hist(TopkSmem<kRes>& S, cg::cluster_group& cluster, int cs,
+                                        int nb) {
+    if (cs == 1) {
+        __syncthreads();
+        return S.hist;
     }
-    *total = tot;
-    return before;
+    cluster.sync();
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
+        uint32_t v[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+            v[r] = (r < cs) ? cluster.map_shared_rank(S.hist, r)[i] : 0u;
+        uint32_t s = 0;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) s += v[r];
+        S.tot[i] = s;
+    }
+    cluster.sync();
+    return S.tot;
 }
 
+// Visit the slice [lo, hi) in steps of 32 positions per thread: f(i, kv)
+// gets, for u = 0..7, the keys of positions i[u] .. i[u]+3 (kv[u]); positions
+// >= hi carry key 0 and must be masked by the caller.  Eight 16-byte loads per
+// thread are in flight per step.  Called by every thread (warp-uniform).
+constexpr int kVec = 8;
+template <bool kRes, typename F>
+__device__ __forceinline__ void sweep(const float* row, const uint32_t* keys, int lo, int hi,
+                                      F&& f) {
+    const int tid = threadIdx.x;
+    for (int base = lo; base < hi; base += 4 * kVec * kThreads) {
+        uint4 kv[kVec];
+        int i[kVec];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            i[u] = base + u * 4 * kThreads + 4 * tid;
+            if (kRes) {
+                kv[u] = (i[u] < hi) ? *reinterpret_cast<const uint4*>(keys + (i[u] - lo))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const float4 x = (i[u] < hi) ? __ldg(reinterpret_cast<const float4*>(row + i[u]))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                kv[u] = make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+            }
+        }
+        f(i, kv);
+    }
+}
+
+// Per-position form of sweep: g(pos, key, valid) for every position.
+template <bool kRes, typename G>
+__device__ __forceinline__ void sweep_each(const float* row, const uint32_t* keys, int lo, int hi,
+                                           G&& g) {
+    sweep<kRes>(row, keys, lo, hi, [&](const int (&i)[kVec], const uint4 (&kv)[kVec]) {
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            g(i[u] + 0, kv[u].x, i[u] + 0 < hi);
+            g(i[u] + 1, kv[u].y, i[u] + 1 < hi);
+            g(i[u] + 2, kv[u].z, i[u] + 2 < hi);
+            g(i[u] + 3, kv[u].w, i[u] + 3 < hi);
+        }
+    });
+}
+
+// Block-ordered pass over the eq bitmap: keep the first `take` set bits (in
+// position order) and add them to the selection bitmap.
+template <bool kRes>
+__device__ void take_lowest_eq(TopkSmem<kRes>& S, int nwords, int take) {
+    int seen = 0;
+    for (int w0 = 0; w0 < nwords; w0 += kThreads) {
+        const int w = w0 + threadIdx.x;
+        const uint32_t m0 = (w < nwords) ? S.eqbits[w] : 0u;
+        int cnt;
+        int r = seen + block_excl_sum(__popc(m0), S.warp_tot, &cnt);
+        if (m0 && r < take) {
+            uint32_t m = m0, keep = 0;
+            while (m && r < take) {
+                keep |= m & (~m + 1u);  // lowest set bit
+                m &= m - 1;
+                ++r;
+            }
+            S.bits[w] |= keep;
+        }
+        seen += cnt;
+    }
+    __syncthreads();
+}
+
+template <bool kRes>
 __global__ void __launch_bounds__(kThreads, 1)
-topk_cluster_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
-                    int32_t* __restrict__ out) {
+topk_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
+            int32_t* __restrict__ out) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    TopkShared& S = *reinterpret_cast<TopkShared*>(smem_raw);
+    TopkSmem<kRes>& S = *reinterpret_cast<TopkSmem<kRes>*>(smem_raw);
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -164,7 +238,7 @@ topk_cluster_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = request_of(bt, t);
     int32_t* o = out + (int64_t)t * K;
-    // uniform over the cluster: every CTA of token t takes the same branch
+    // uniform over the cluster: every CTA of token t takes the same branches
     const bool ok = token_ok(bt, b, t, nullptr);
     const int vis = ok ? visible_of(bt, b, t) : 0;
     if (vis <= K) {
@@ -173,177 +247,276 @@ topk_cluster_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, 
         return;
     }
     const float* row = scores + (int64_t)t * ld;
-    // 32-aligned slice [lo, hi) of the visible positions
-    const int per = ((vis + cs - 1) / cs + 31) & ~31;
+    const int per = ((vis + cs - 1) / cs + 31) & ~31;  // 32-aligned slices
     const int lo = min(vis, rank * per);
     const int hi = min(vis, lo + per);
     const int nwords = (hi - lo + 31) / 32;
+    constexpr int kCand = Cfg<kRes>::kCand;
 
-    uint32_t prefix = 0, pmask = 0, rem = (uint32_t)K;
-    int level = 0;
-    bool collected = false;
-    int ncand = 0;
-    // ---- streaming digits until the threshold prefix is small enough ----
-    while (level < 3) {
-        const int nb = (level == 0) ? kBins : 1024;
-        for (int i = tid; i < nb; i += kThreads) S.hist[i] = 0;
-        __syncthreads();
-        for (int s0 = lo + warp * 32; s0 < hi; s0 += kThreads) {
-            const int s = s0 + lane;
-            const bool in = s < hi;
-            const uint32_t key = in ? order_key(__ldg(row + s)) : 0u;
-            const bool match = in && (key & pmask) == prefix;
-            hist_add(S.hist, (key >> dig_shift(level)) & dig_mask(level), match);
-        }
-        cluster_digit(S, cluster, nb, rem);
-        const uint32_t d = S.s_digit;
-        // the local count of the threshold digit decides whether candidates fit
-        S.xchg[0] = S.hist[d];
-        prefix |= d << dig_shift(level);
-        pmask |= dig_mask(level) << dig_shift(level);
-        rem = S.s_rem;
-        ++level;
-        // largest local count over the cluster (all CTAs agree on the branch)
-        cluster.sync();
-        uint32_t mx = 0;
-        for (int r = 0; r < cs; ++r) mx = max(mx, cluster.map_shared_rank(S.xchg, r)[0]);
-        cluster.sync();
-        if (level < 3 && mx <= (uint32_t)kCandCap) break;
+    if (kRes) {
+        sweep_each<false>(row, nullptr, lo, hi, [&](int pos, uint32_t key, bool valid) {
+            if (valid) S.keys[pos - lo] = key;
+        });
     }
+    for (int i = tid; i < kBins; i += kThreads) S.hist[i] = 0;
+    if (tid == 0) S.s_count = 0;
+    __syncthreads();
 
-    if (level < 3) {
-        // ---- collection pass: bitmap of positions above the prefix, candidates ----
-        if (tid == 0) S.s_count = 0;
-        __syncthreads();
-        for (int s0 = lo + warp * 32; s0 < hi; s0 += kThreads) {
-            const int s = s0 + lane;
-            const bool in = s < hi;
-            const uint32_t key = in ? order_key(__ldg(row + s)) : 0u;
-            const uint32_t top = key & pmask;
-            const unsigned above = __ballot_sync(0xffffffffu, in && top > prefix);
-            const bool cand = in && top == prefix;
-            const unsigned cm = __ballot_sync(0xffffffffu, cand);
-            if (lane == 0) S.bits[(s0 - lo) >> 5] = above;
-            int base = 0;
-            if (lane == 0 && cm) base = atomicAdd(&S.s_count, __popc(cm));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (cand) {
-                const int c = base + __popc(cm & ((1u << lane) - 1u));
-                S.cand_key[c] = key;
-                S.cand_pos[c] = s;
+    // ---- 1. threshold estimate from a sample -------------------------------
+    int sampled = 0;
+    if (kRes) {
+        sweep_each<true>(row, S.keys, lo, hi, [&](int, uint32_t key, bool valid) {
+            hist_add(S.hist, key >> 20, valid);
+        });
+        sampled = hi - lo;
+    } else {
+        // chunks 16*w + 512*u + 4096*j: every 16th chunk exactly once
+        for (int c0 = warp * kSampleStride; c0 < nwords; c0 += kWarps * kSampleStride * 8) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int pos = lo + 32 * (c0 + u * kWarps * kSampleStride) + lane;
+                x[u] = (pos < hi) ? __ldg(row + pos) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int pos = lo + 32 * (c0 + u * kWarps * kSampleStride) + lane;
+                hist_add(S.hist, order_key(x[u]) >> 20, pos < hi);
             }
         }
-        __syncthreads();
-        ncand = (int)S.s_count;
-        collected = true;
-        // ---- remaining digits on the candidates ----
-        while (level < 3) {
-            for (int i = tid; i < 1024; i += kThreads) S.hist[i] = 0;
-            __syncthreads();
-            for (int c0 = 0; c0 < ncand; c0 += kThreads) {
-                const int c = c0 + tid;
-                const bool in = c < ncand;
-                const uint32_t key = in ? S.cand_key[c] : 0u;
-                const bool match = in && (key & pmask) == prefix;
-                hist_add(S.hist, (key >> dig_shift(level)) & dig_mask(level), match);
+        for (int c = 0; c < nwords; c += kSampleStride) sampled += min(32, hi - (lo + 32 * c));
+    }
+    S.xchg[4] = (uint32_t)sampled;
+    const uint32_t* th = cluster_hist(S, cluster, cs, kBins);
+    uint32_t sampled_all = (uint32_t)sampled;
+    if (cs > 1) {
+        sampled_all = 0;
+        for (int r = 0; r < cs; ++r) sampled_all += cluster.map_shared_rank(S.xchg, r)[4];
+    }
+    uint32_t need_s;
+    if (sampled_all >= (uint32_t)vis) {
+        need_s = (uint32_t)K;  // every position sampled: the exact threshold bin
+    } else {
+        const double f = (double)sampled_all / (double)vis;
+        need_s = (uint32_t)fmin((double)sampled_all, ceil(1.25 * K * f) + 16.0);
+    }
+    find_digit(S, th, kBins, need_s);
+    const uint32_t key_lo = S.s_digit << 20;
+
+    // ---- 2. candidates: every key in a bin >= b_lo -------------------------
+    sweep<kRes>(row, kRes ? S.keys : nullptr, lo, hi,
+                [&](const int (&i)[kVec], const uint4 (&kv)[kVec]) {
+        uint32_t mask = 0;  // bit 4u+e: element e of vector u is a candidate
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                mask |= (i[u] + e < hi && k4[e] >= key_lo) ? (1u << (4 * u + e)) : 0u;
+        }
+        const int n = __popc(mask);
+        int incl = n;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o2);
+            if (lane >= o2) incl += v;
+        }
+        const int wsum = __shfl_sync(0xffffffffu, incl, 31);
+        if (wsum == 0) return;
+        int base = 0;
+        if (lane == 31) base = (int)atomicAdd(&S.s_count, (uint32_t)wsum);
+        base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (mask & (1u << (4 * u + e))) {
+                    if (base < kCand) {
+                        S.cand_key[base] = k4[e];
+                        S.cand_pos[base] = i[u] + e;
+                    }
+                    ++base;
+                }
             }
-            cluster_digit(S, cluster, 1024, rem);
+        }
+    });
+    __syncthreads();
+    const uint32_t ncand_raw = S.s_count;
+    S.xchg[0] = ncand_raw;
+    uint32_t total = ncand_raw, maxc = ncand_raw;
+    if (cs > 1) {
+        cluster.sync();
+        total = 0;
+        maxc = 0;
+        for (int r = 0; r < cs; ++r) {
+            const uint32_t v = cluster.map_shared_rank(S.xchg, r)[0];
+            total += v;
+            maxc = max(maxc, v);
+        }
+    }
+    const bool fast = total >= (uint32_t)K && maxc <= (uint32_t)kCand && total <= (uint32_t)kCand;
+    const int ncand = (int)min(ncand_raw, (uint32_t)kCand);
+
+    int take = 0;
+    if (fast) {
+        // ---- 3. exact tau on the candidates (gathered in CTA 0) -------------
+        if (cs > 1) {
+            cluster.sync();  // every candidate list is complete
+            if (rank == 0) {
+                uint32_t off = (uint32_t)ncand;
+                for (int r = 1; r < cs; ++r) {
+                    const uint32_t n = cluster.map_shared_rank(S.xchg, r)[0];
+                    const uint32_t* rk = cluster.map_shared_rank(S.cand_key, r);
+                    const int32_t* rp = cluster.map_shared_rank(S.cand_pos, r);
+                    for (uint32_t i = tid; i < n; i += kThreads) {
+                        S.cand_key[off + i] = rk[i];
+                        S.cand_pos[off + i] = rp[i];
+                    }
+                    off += n;
+                }
+            }
+        }
+        if (rank == 0) {
+            __syncthreads();
+            const int n_all = (int)total;
+            uint32_t prefix = 0, pmask = 0, rem = (uint32_t)K;
+            for (int level = 0; level < 3; ++level) {
+                const int nb = (level == 0) ? kBins : 1024;
+                for (int i = tid; i < nb; i += kThreads) S.hist[i] = 0;
+                __syncthreads();
+                for (int c0 = 0; c0 < n_all; c0 += kThreads) {
+                    const int c = c0 + tid;
+                    const uint32_t key = (c < n_all) ? S.cand_key[c] : 0u;
+                    hist_add(S.hist, (key >> dig_shift(level)) & dig_mask(level),
+                             c < n_all && (key & pmask) == prefix);
+                }
+                __syncthreads();
+                find_digit(S, S.hist, nb, rem);
+                prefix |= S.s_digit << dig_shift(level);
+                pmask |= dig_mask(level) << dig_shift(level);
+                rem = S.s_rem;
+            }
+            // keys equal to tau per source CTA (candidates are in rank order);
+            // tot is free at this point: [0,8) counts, [8,16) first candidate
+            if (tid < kMaxCluster) {
+                S.tot[tid] = 0u;
+                uint32_t first = 0;
+                for (int r = 0; r < tid && r < cs; ++r)
+                    first += (cs > 1) ? cluster.map_shared_rank(S.xchg, r)[0] : (uint32_t)ncand;
+                S.tot[8 + tid] = (tid < cs) ? first : 0xFFFFFFFFu;
+            }
+            __syncthreads();
+            for (int c = tid; c < n_all; c += kThreads) {
+                if (S.cand_key[c] == prefix) {
+                    int r = 0;
+                    while (r + 1 < cs && (uint32_t)c >= S.tot[8 + r + 1]) ++r;
+                    atomicAdd(&S.tot[r], 1u);
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t before = 0;
+                for (int r = 0; r < cs; ++r) {
+                    const uint32_t e = S.tot[r];
+                    const uint32_t tk = rem > before ? min(e, rem - before) : 0u;
+                    before += e;
+                    uint32_t* x = (cs > 1) ? cluster.map_shared_rank(S.xchg, r) : S.xchg;
+                    x[1] = prefix;
+                    x[2] = tk;
+                }
+            }
+        }
+        if (cs > 1) cluster.sync();
+        else __syncthreads();
+        const uint32_t tau = S.xchg[1];
+        take = (int)S.xchg[2];
+        // ---- 4a. bitmap from this CTA's own candidates -----------------------
+        for (int w = tid; w < nwords; w += kThreads) {
+            S.bits[w] = 0u;
+            S.eqbits[w] = 0u;
+        }
+        __syncthreads();
+        for (int c = tid; c < ncand; c += kThreads) {
+            const uint32_t key = S.cand_key[c];
+            const int p = S.cand_pos[c] - lo;
+            if (key > tau) atomicOr(&S.bits[p >> 5], 1u << (p & 31));
+            else if (key == tau) atomicOr(&S.eqbits[p >> 5], 1u << (p & 31));
+        }
+        __syncthreads();
+        take_lowest_eq(S, nwords, take);
+    } else {
+        // ---- 3'. exact fallback: digits by passes over the slice -------------
+        uint32_t prefix = 0, pmask = 0, rem = (uint32_t)K;
+        for (int level = 0; level < 3; ++level) {
+            const int nb = (level == 0) ? kBins : 1024;
+            if (cs > 1) cluster.sync();  // remote readers of the last histogram are done
+            for (int i = tid; i < nb; i += kThreads) S.hist[i] = 0;
+            __syncthreads();
+            sweep_each<kRes>(row, kRes ? S.keys : nullptr, lo, hi,
+                             [&](int, uint32_t key, bool valid) {
+                hist_add(S.hist, (key >> dig_shift(level)) & dig_mask(level),
+                         valid && (key & pmask) == prefix);
+            });
+            const uint32_t* h = cluster_hist(S, cluster, cs, nb);
+            find_digit(S, h, nb, rem);
             prefix |= S.s_digit << dig_shift(level);
             pmask |= dig_mask(level) << dig_shift(level);
             rem = S.s_rem;
-            ++level;
         }
-    }
-    // prefix is now the k-th largest key tau; `rem` keys equal to tau are taken,
-    // lowest positions first across the cluster
-    const uint32_t tau = prefix;
-    const uint32_t need_eq = rem;
-
-    if (collected) {
-        // count this CTA's keys equal to tau, exchange, take the lowest ones
+        const uint32_t tau = prefix;
+        // bitmaps of the keys above / equal to tau: a 32-position word spans 8
+        // lanes of 4 positions; their nibbles are OR-combined by shuffles
         int eq_local = 0;
-        for (int c = tid; c < ncand; c += kThreads) eq_local += (S.cand_key[c] == tau) ? 1 : 0;
+        sweep_each<kRes>(row, kRes ? S.keys : nullptr, lo, hi,
+                         [&](int pos, uint32_t key, bool valid) {
+            const int e = pos & 3;
+            const int sh = 4 * (lane & 7) + e;
+            unsigned gw = (valid && key > tau) ? (1u << sh) : 0u;
+            unsigned ew = (valid && key == tau) ? (1u << sh) : 0u;
+            eq_local += ew ? 1 : 0;
+#pragma unroll
+            for (int o2 = 1; o2 < 8; o2 <<= 1) {
+                gw |= __shfl_xor_sync(0xffffffffu, gw, o2);
+                ew |= __shfl_xor_sync(0xffffffffu, ew, o2);
+            }
+            const int word_pos = (pos & ~3) - 4 * (lane & 7);  // first position of the word
+            if ((lane & 7) == 0 && word_pos < hi) {
+                const int w = (word_pos - lo) >> 5;
+                if (e == 0) {
+                    S.bits[w] = gw;
+                    S.eqbits[w] = ew;
+                } else {
+                    S.bits[w] |= gw;
+                    S.eqbits[w] |= ew;
+                }
+            }
+        });
+        __syncthreads();
         int eq_tot;
         (void)block_excl_sum(eq_local, S.warp_tot, &eq_tot);
-        S.xchg[1] = (uint32_t)eq_tot;
-        uint32_t eq_all;
-        const uint32_t eq_before = cluster_prefix(S, cluster, 1, &eq_all);
-        const int take = (int)min((uint32_t)eq_tot, need_eq > eq_before ? need_eq - eq_before : 0u);
-        // candidates above tau are selected; equal ones by position rank
-        for (int c0 = 0; c0 < ncand; c0 += kThreads) {
-            const int c = c0 + tid;
-            if (c < ncand) {
-                const uint32_t key = S.cand_key[c];
-                const int pos = S.cand_pos[c];
-                bool sel = key > tau;
-                if (key == tau && take > 0) {
-                    // rank among this CTA's tau-equal candidates by position
-                    int rank_eq = 0;
-                    for (int j = 0; j < ncand; ++j)
-                        rank_eq += (S.cand_key[j] == tau && S.cand_pos[j] < pos) ? 1 : 0;
-                    sel = rank_eq < take;
-                }
-                if (sel) atomicOr(&S.bits[(pos - lo) >> 5], 1u << ((pos - lo) & 31));
-            }
+        S.xchg[3] = (uint32_t)eq_tot;
+        uint32_t eq_before = 0;
+        if (cs > 1) {
+            cluster.sync();
+            for (int r = 0; r < rank; ++r) eq_before += cluster.map_shared_rank(S.xchg, r)[3];
         }
-        __syncthreads();
-    } else {
-        // ---- fallback: selection by streaming with the full key known ----
-        // keys above tau: one bitmap word per warp iteration
-        int eq = 0;
-        for (int s0 = lo + warp * 32; s0 < hi; s0 += kThreads) {
-            const int s = s0 + lane;
-            const bool in = s < hi;
-            const uint32_t key = in ? order_key(__ldg(row + s)) : 0u;
-            const unsigned gtm = __ballot_sync(0xffffffffu, in && key > tau);
-            eq += (in && key == tau) ? 1 : 0;
-            if (lane == 0) S.bits[(s0 - lo) >> 5] = gtm;
-        }
-        int eq_tot;
-        (void)block_excl_sum(eq, S.warp_tot, &eq_tot);
-        S.xchg[1] = (uint32_t)eq_tot;
-        uint32_t eq_all;
-        const uint32_t eq_before = cluster_prefix(S, cluster, 1, &eq_all);
-        const int take =
-            (int)min((uint32_t)eq_tot, need_eq > eq_before ? need_eq - eq_before : 0u);
-        // keys equal to tau, lowest positions first: a block-ordered pass over words
-        int eq_seen = 0;
-        for (int w0 = 0; w0 < nwords; w0 += kThreads) {
-            const int w = w0 + tid;
-            uint32_t eqm = 0;
-            if (w < nwords) {
-                const int s0 = lo + 32 * w;
-                for (int j = 0; j < 32 && s0 + j < hi; ++j)
-                    eqm |= (order_key(__ldg(row + s0 + j)) == tau ? 1u : 0u) << j;
-            }
-            int cnt;
-            const int before = eq_seen + block_excl_sum(__popc(eqm), S.warp_tot, &cnt);
-            if (eqm) {
-                int r = before;
-                uint32_t m = eqm, keep = 0;
-                while (m) {
-                    const int j = __ffs(m) - 1;
-                    if (r < take) keep |= 1u << j;
-                    ++r;
-                    m &= m - 1;
-                }
-                S.bits[w] |= keep;
-            }
-            eq_seen += cnt;
-        }
-        __syncthreads();
+        take = (int)(rem > eq_before ? min((uint32_t)eq_tot, rem - eq_before) : 0u);
+        take_lowest_eq(S, nwords, take);
     }
 
-    // ---- ordered output: this CTA's selected positions at its cluster offset ----
+    // ---- 4b. ordered output: this CTA's positions at its cluster offset ------
     int sel_local = 0;
     for (int w = tid; w < nwords; w += kThreads) sel_local += __popc(S.bits[w]);
     int sel_tot;
     (void)block_excl_sum(sel_local, S.warp_tot, &sel_tot);
-    S.xchg[2] = (uint32_t)sel_tot;
-    uint32_t all;
-    const uint32_t off = cluster_prefix(S, cluster, 2, &all);
-    // words are assigned to threads in contiguous runs so the order is kept
-    const int wpt = (nwords + kThreads - 1) / kThreads;
+    S.xchg[5] = (uint32_t)sel_tot;
+    uint32_t off = 0;
+    if (cs > 1) {
+        cluster.sync();
+        for (int r = 0; r < rank; ++r) off += cluster.map_shared_rank(S.xchg, r)[5];
+    }
+    const int wpt = (nwords + kThreads - 1) / kThreads;  // contiguous runs keep the order
     const int w_begin = min(nwords, tid * wpt), w_end = min(nwords, w_begin + wpt);
     int mine = 0;
     for (int w = w_begin; w < w_end; ++w) mine += __popc(S.bits[w]);
@@ -358,28 +531,14 @@ topk_cluster_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, 
             m &= m - 1;
         }
     }
-    cluster.sync();  // no CTA leaves while others may still read its shared memory
+    if (cs > 1) cluster.sync();  // no CTA leaves while others may read its shared memory
 }
 
-}  // namespace
-
-// CTAs per query token: spread few tokens over more SMs, and keep every
-// slice within the per-CTA bitmap.
-int topk_cluster_size(int total_q, int max_seq) {
-    int cs = 1;
-    while (cs < kMaxCluster && total_q * cs * 2 <= 152) cs <<= 1;
-    while (cs < kMaxCluster && (max_seq + cs - 1) / cs > kSliceMax) cs <<= 1;
-    return cs;
-}
-
-bool topk_supported(int max_seq) { return max_seq <= kSliceMax * kMaxCluster; }
-
-cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
-                        int32_t* out, cudaStream_t stream) {
-    if (bt.total_q == 0) return cudaSuccess;
-    const int cs = topk_cluster_size(bt.total_q, bt.max_seq);
-    const size_t smem = sizeof(TopkShared);
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel,
+template <bool kRes>
+cudaError_t launch(const BatchArgs& bt, const float* scores, int64_t ld, int K, int32_t* out,
+                   int cs, cudaStream_t stream) {
+    const size_t smem = sizeof(TopkSmem<kRes>);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kRes>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -394,7 +553,28 @@ cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, bt, scores, ld, K, out);
+    return cudaLaunchKernelEx(&cfg, topk_kernel<kRes>, bt, scores, ld, K, out);
+}
+
+}  // namespace
+
+// CTAs per query token for rows that stream from global memory: spread few
+// tokens over more SMs, and keep every slice within the per-CTA bitmap.
+int topk_cluster_size(int total_q, int max_seq) {
+    int cs = 1;
+    while (cs < kMaxCluster && total_q * cs * 2 <= 152) cs <<= 1;
+    while (cs < kMaxCluster && (max_seq + cs - 1) / cs > kSliceMax) cs <<= 1;
+    return cs;
+}
+
+bool topk_supported(int max_seq) { return max_seq <= kSliceMax * kMaxCluster; }
+
+cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
+                        int32_t* out, cudaStream_t stream) {
+    if (bt.total_q == 0) return cudaSuccess;
+    if (bt.max_seq <= kResidentMax) return launch<true>(bt, scores, ld, K, out, 1, stream);
+    return launch<false>(bt, scores, ld, K, out, topk_cluster_size(bt.total_q, bt.max_seq),
+                         stream);
 }
 
 }  // namespace dsa

@@ -78,6 +78,19 @@ def test_topk_all_equal_long_rows_use_streaming_selection():
     _run(lens, counts, np.full((2, ld), 2.5))
 
 
+def test_topk_sample_misses_the_top():
+    """The large scores sit exactly in the sampled chunks (every 16th run of 32
+    positions), so the sampled threshold is far too high: the candidate pass
+    finds fewer than k keys and the exact fallback must take over."""
+    lens = [131072, 200000]
+    ld = ((max(lens) + 127) // 128) * 128
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal((2, ld))
+    pos = np.arange(ld)
+    s[:, (pos // 32) % 16 == 0] += 100.0
+    _run(lens, [1, 1], s)
+
+
 def test_topk_one_million_positions():
     rng = np.random.default_rng(11)
     lens = [1 << 20]
