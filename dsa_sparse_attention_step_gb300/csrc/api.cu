@@ -17,6 +17,7 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
                               uint16_t* out, float* lse, void* ws, int32_t* status,
                               cudaStream_t stream);
 size_t sparse_mla_workspace_bytes(int total_q, int K);
+int sparse_mla_launches(int total_q, int K);
 cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const float* lat,
                                 float kv_scale, void* index_pages, void* latent_pages,
                                 int32_t* status, cudaStream_t stream);
@@ -169,7 +170,8 @@ dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const v
     const size_t need = dsa_sparse_mla_workspace_size(batch, topk);
     if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return DSA_ERR_WORKSPACE;
     if (batch->total_q == 0) return DSA_OK;
-    g_launches.fetch_add(need > 0 ? 2 : 1, std::memory_order_relaxed);
+    g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk),
+                         std::memory_order_relaxed);
     return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
                                          indices, topk, out, lse, ws, dev_status,
                                          (cudaStream_t)stream));
@@ -205,8 +207,8 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
     uint8_t* base = static_cast<uint8_t*>(ws);
     const size_t off_topk = align_up((size_t)batch->total_q * ld * sizeof(float), 256);
     const size_t off_mla = off_topk + align_up(dsa_topk_workspace_size(batch, topk), 256);
-    const bool combine = dsa_sparse_mla_workspace_size(batch, topk) > 0;
-    g_launches.fetch_add(combine ? 4 : 3, std::memory_order_relaxed);
+    g_launches.fetch_add(2 + (uint64_t)sparse_mla_launches(batch->total_q, topk),
+                         std::memory_order_relaxed);
     cudaError_t e = launch_index_scores(a, q_fp8, q_scale, w, index_pages, (int)key_format,
                                         scores, ld, dev_status, s);
     if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, s);

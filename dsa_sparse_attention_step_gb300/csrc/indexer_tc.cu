@@ -337,15 +337,17 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v);
                     tmem_wait_ld();
                     const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
-                    float sc = 0.f;
+                    // four independent partial sums keep the FMA pipe busy
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int h4 = 0; h4 < 8; ++h4) {
                         const float4 ww = w4[h4];
-                        sc = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), sc);
-                        sc = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), sc);
-                        sc = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), sc);
-                        sc = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), sc);
+                        s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), s0);
+                        s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), s1);
+                        s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), s2);
+                        s3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), s3);
                     }
+                    const float sc = (s0 + s1) + (s2 + s3);
                     if (in_seq) {
                         const int vis = c.seq - c.nb + gtok0 + j + 1;
                         p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =

@@ -23,9 +23,10 @@
 // moves when a new maximum exceeds it by more than 2^8, and the O^T columns
 // are then rescaled in TMEM.
 //
-// Warp roles (288 threads): warps 0-3 softmax and epilogue (thread = head for
-// S, = latent dim for O^T), warps 4-7 gather/convert producers, warp 8 TMEM
-// allocation and the single MMA-issuing thread.  Every wait is bounded.
+// Warp roles (256 threads, so a thread may hold up to 255 registers): warps
+// 0-3 softmax (thread = head), warps 4-6 gather/convert producers, warp 7 TMEM
+// allocation and the single MMA-issuing thread; all eight warps share the
+// epilogue (thread = latent dim).  Every wait is bounded.
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -36,7 +37,9 @@ using namespace sm100;
 namespace {
 
 constexpr int kTileKeys = 32;
-constexpr int kThreads = 288;
+constexpr int kThreads = 256;
+constexpr int kProducers = 96;                                // warps 4-6
+constexpr int kVecPerProducer = kTileKeys * (kLatDim / 16) / kProducers;  // 12
 constexpr int kQRows = 96;
 constexpr int kSlabs = kLatDim / 64;                          // 9 K-slabs of 64 dims
 constexpr int kQSlabBytes = kQRows * 128;                     // 12288
@@ -69,12 +72,13 @@ constexpr uint32_t kIdescQK = make_idesc(kFmtF16, kFmtF16, 128, kTileKeys, false
 constexpr uint32_t kIdescPV = make_idesc(kFmtF16, kFmtF16, 128, kQRows, true, false);
 
 struct Bars {
-    uint64_t full[2];    // producer -> MMA: latent stage filled (128 arrivals)
+    uint64_t full[2];    // producer -> MMA: latent stage filled (96 arrivals)
     uint64_t empty[2];   // MMA -> producer: stage free (commit after PV)
     uint64_t sfull[2];   // MMA -> softmax: S buffer ready (commit after QK)
     uint64_t pfull[2];   // softmax -> MMA: P buffer written, S buffer read (128 arrivals)
     uint64_t pempty[2];  // MMA -> softmax: PV done with P buffer (commit)
     uint64_t done;       // MMA -> epilogue: everything finished
+    uint64_t qbar;       // bulk copy of the prepared query landed
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -101,7 +105,8 @@ __device__ __forceinline__ bool softmax_any(bool pred) {
 
 struct MlaParams {
     BatchArgs bt;
-    const __nv_bfloat16* q_lat;
+    const uint8_t* qf16;   // [T][110592] prepared query (f16, swizzled slabs)
+    const int* qexp;       // [T] power-of-two exponent e of the query scale 2^-e
     const uint8_t* latent_pages;
     const int32_t* indices;
     int K;                 // index slots per token
@@ -128,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     // [0,256): rescale factors (two buffers of 128), [256,384): m, [384,512): l
     float* sF = reinterpret_cast<float*>(sm + kOffF);
     Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
-    __shared__ float s_amax[kThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = blockIdx.x / p.splits;
@@ -142,33 +146,30 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->full[i], 128);
+            mbar_init(&bars->full[i], kProducers);
             mbar_init(&bars->empty[i], 1);
             mbar_init(&bars->sfull[i], 1);
             mbar_init(&bars->pfull[i], 128);
             mbar_init(&bars->pempty[i], 1);
         }
         mbar_init(&bars->done, 1);
+        mbar_init(&bars->qbar, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
+        // the prepared query: one bulk copy into its shared-memory slabs
+        if (ok_tok) {
+            mbar_arrive_expect_tx(&bars->qbar, (uint32_t)kQBytes);
+            bulk_copy_g2s(sQ, p.qf16 + (int64_t)t * kQBytes, (uint32_t)kQBytes, &bars->qbar);
+        } else {
+            mbar_arrive(&bars->qbar);
+        }
     }
-    if (warp == 8) {
+    if (warp == 7) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
 
-    // ---- preamble ------------------------------------------------------------
-    // (1) the bf16 query, 96 x 576 = 6912 vectors of 16 bytes, copied
-    //     asynchronously into its f16 positions (converted in place below)
-    const __nv_bfloat16* qsrc = p.q_lat + (int64_t)t * kMlaHeads * kLatDim;
-    if (ok_tok) {
-        for (int v = tid; v < kMlaHeads * kLatDim / 8; v += kThreads) {
-            const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
-            cp_async16(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16), qsrc + 8 * v);
-        }
-    }
-    cp_async_commit();
-    // (2) row ids (page * 64 + slot) of this CTA's index slots
+    // ---- preamble: row ids (page * 64 + slot) of this CTA's index slots -------
     for (int k = tid; k < p.split_keys; k += kThreads) {
         int row = -1;
         if (ok_tok) {
@@ -183,66 +184,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         sRow[k] = row;
     }
     if (tid < 2 * 128) sF[tid] = 1.f;
-    cp_async_wait_all();
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
 
-    const bool producer = (warp >= 4 && warp < 8);
-    int e = 0;
+    const bool producer = (warp >= 4 && warp < 7);
+    const int e = ok_tok ? __ldg(p.qexp + t) : 0;
     if (!producer) {
-        // (3) warps 0-3 and 8: valid-slot masks, then the query bf16 -> f16 in
-        //     place while the producers already gather latents.  First try
-        //     scale 1; if the largest |q| is >= 2^15 or < 2^-8, convert again
-        //     from global memory with a power-of-two scale 2^-e chosen so that
-        //     max|q| * 2^-e lies in [2^14, 2^15).
-        const int ctid = (warp == 8) ? 128 + lane : tid;  // 0..159
+        // warps 0-3 and 7: valid-slot masks while the producers start gathering
+        const int ctid = (warp == 7) ? 128 + lane : tid;  // 0..159
         for (int i = ctid; i < n_tiles; i += 160) {
             uint32_t m = 0;
             for (int j = 0; j < kTileKeys; ++j) m |= (sRow[i * kTileKeys + j] >= 0 ? 1u : 0u) << j;
             sMask[i] = m;
         }
-        float amax = 0.f;
-        for (int v = ctid; v < kMlaHeads * kLatDim / 8; v += 160) {
-            const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
-            uint4* dst = reinterpret_cast<uint4*>(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16));
-            const uint4 raw = ok_tok ? *dst : make_uint4(0, 0, 0, 0);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float a = __uint_as_float(wv[i] << 16);
-                const float c2 = __uint_as_float(wv[i] & 0xFFFF0000u);
-                amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(c2)));
-                o[i] = pack_half2(a, c2);
-            }
-            *dst = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        amax = warp_max(amax);
-        if (lane == 0) s_amax[warp] = amax;
         asm volatile("bar.sync 2, 160;" ::: "memory");
-        float qmax = fmaxf(fmaxf(s_amax[0], s_amax[1]), fmaxf(s_amax[2], s_amax[3]));
-        qmax = fmaxf(qmax, s_amax[8]);
-        if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
-            int ex;
-            frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
-            e = ex - 15;
-            const float qmul = ldexpf(1.0f, -e);
-            for (int v = ctid; v < kMlaHeads * kLatDim / 8; v += 160) {
-                const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
-                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qsrc) + v);
-                const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
-                                      __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
-                *reinterpret_cast<uint4*>(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        asm volatile("bar.sync 2, 160;" ::: "memory");
-        tc_fence_after();
     }
     const uint32_t tmem = bars->tmem_base;
     // z in log2 units per unit of the f16 accumulator
@@ -250,13 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 
     if (producer) {
         // ---------------- producers: gather + E4M3 -> f16 ----------------
-        // 32 rows x 36 vectors of 16 bytes = 1152 vectors -> 9 per thread per
+        // 32 rows x 36 vectors of 16 bytes = 1152 vectors -> 12 per thread per
         // tile; two tiles of loads are kept in flight (registers A and B)
         const int ptid = tid - 128;
-        uint4 rawA[9], rawB[9];
+        uint4 rawA[kVecPerProducer], rawB[kVecPerProducer];
 #define DSA_MLA_LOAD(raw_, i_)                                                           \
-    _Pragma("unroll") for (int u = 0; u < 9; ++u) {                                      \
-        const int v = ptid + 128 * u;                                                     \
+    _Pragma("unroll") for (int u = 0; u < kVecPerProducer; ++u) {                        \
+        const int v = ptid + kProducers * u;                                              \
         const int r = v / 36, c = v % 36;                                                 \
         const int row = sRow[(i_) * kTileKeys + r];                                       \
         raw_[u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(                      \
@@ -264,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                              : make_uint4(0, 0, 0, 0);                                    \
     }
 #define DSA_MLA_STORE(raw_, st_)                                                         \
-    _Pragma("unroll") for (int u = 0; u < 9; ++u) {                                      \
-        const int v = ptid + 128 * u;                                                     \
+    _Pragma("unroll") for (int u = 0; u < kVecPerProducer; ++u) {                        \
+        const int v = ptid + kProducers * u;                                              \
         const int r = v / 36, c = v % 36;                                                 \
         const uint32_t wv[4] = {raw_[u].x, raw_[u].y, raw_[u].z, raw_[u].w};              \
         uint32_t hv[8];                                                                   \
@@ -300,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         }
 #undef DSA_MLA_LOAD
 #undef DSA_MLA_STORE
-    } else if (warp == 8) {
+    } else if (warp == 7) {
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             const uint32_t qa = smem_u32(sQ), pa = smem_u32(sP), la = smem_u32(sL);
@@ -324,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 mma_commit(&bars->pempty[st]);
                 return true;
             };
-            bool ok = true;
+            bool ok = mbar_wait(&bars->qbar, 0, abort_flag);
             for (int i = 0; i < n_tiles && ok; ++i) {
                 const int st = i & 1;
                 ok = mbar_wait(&bars->full[st], (i >> 1) & 1, abort_flag);
@@ -362,12 +318,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             tmem_wait_ld();
             const uint32_t mask = sMask[i];
             float z[32];
-            float mt = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 32; ++j)
                 z[j] = ((mask >> j) & 1u) ? __uint_as_float(r[j]) * zscale : -INFINITY;
-                mt = fmaxf(mt, z[j]);
-            }
+            // pairwise trees keep the dependency chains short
+            float mx[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx[j] = fmaxf(z[2 * j], z[2 * j + 1]);
+#pragma unroll
+            for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
+            const float mt = mx[0];
             float factor = 1.f;
             bool resc = false;
             if (real && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog2)) {
@@ -375,15 +337,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 m_ref = mt;
                 resc = (i > 0);
             }
-            float psum = 0.f;
             uint32_t ph[16];
+            float ps[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float p0 = ((mask >> (2 * j)) & 1u) ? exp2f(z[2 * j] - m_ref) : 0.f;
                 const float p1 = ((mask >> (2 * j + 1)) & 1u) ? exp2f(z[2 * j + 1] - m_ref) : 0.f;
-                psum += p0 + p1;
+                ps[j] = p0 + p1;
                 ph[j] = pack_half2(p0, p1);
             }
+#pragma unroll
+            for (int w2 = 8; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                for (int j = 0; j < w2; ++j) ps[j] += ps[j + w2];
+            const float psum = ps[0];
             l = l * factor + psum;
             float* fac = sF + 128 * (i & 1);
             fac[h] = resc ? factor : 1.f;
@@ -474,7 +441,59 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && tid == 0) record_error(p.status, DSA_ERR_TIMEOUT);
-    if (warp == 8) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 7) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Prepare each token's query once: bf16 -> f16 with a power-of-two scale 2^-e
+// (e = 0 unless max|q| >= 2^15 or < 2^-8; then max|q| * 2^-e lies in
+// [2^14, 2^15)), written in the 128-byte-swizzled slab layout the MMA reads,
+// so every CTA of the token loads it with one bulk copy.
+__global__ void __launch_bounds__(256)
+sparse_mla_prep_q_kernel(const __nv_bfloat16* __restrict__ q_lat, uint8_t* __restrict__ qf16,
+                         int* __restrict__ qexp) {
+    constexpr int kVec = kMlaHeads * kLatDim / 8 / 256;  // 27 vectors of 8 per thread
+    __shared__ float s_max[8];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(q_lat + (int64_t)t * kMlaHeads * kLatDim);
+    uint4 raw[kVec];
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+        raw[u] = __ldg(src + tid + 256 * u);
+        const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[i] << 16)),
+                                     fabsf(__uint_as_float(wv[i] & 0xFFFF0000u))));
+    }
+    amax = warp_max(amax);
+    if ((tid & 31) == 0) s_max[tid >> 5] = amax;
+    __syncthreads();
+    float qmax = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) qmax = fmaxf(qmax, s_max[w]);
+    int e = 0;
+    if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
+        int ex;
+        frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
+        e = ex - 15;
+    }
+    const float qmul = ldexpf(1.0f, -e);
+    uint8_t* dst = qf16 + (int64_t)t * kQBytes;
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+        const int v = tid + 256 * u;
+        const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
+        const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
+                              __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
+        *reinterpret_cast<uint4*>(dst + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid == 0) qexp[t] = e;
 }
 
 // Merge the split partials: out = sum_s 2^(lse_s - L) o_s with
@@ -529,13 +548,31 @@ int sparse_mla_splits(int total_q, int K) {
     return splits;
 }
 
-size_t sparse_mla_workspace_bytes(int total_q, int K) {
+// Workspace: prepared queries [T][110592], exponents [T], then for split
+// batches the f16 partial outputs [T, splits, 96, 512] and lse [T, splits, 96].
+struct MlaWs {
+    size_t q, qexp, part_o, part_lse, total;
+};
+
+MlaWs mla_ws_layout(int total_q, int K) {
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     const int splits = sparse_mla_splits(total_q, K);
-    if (splits == 1) return 0;
-    const size_t po = (size_t)total_q * splits * kMlaHeads * kVDim * sizeof(__half);
-    const size_t pl = (size_t)total_q * splits * kMlaHeads * sizeof(float);
-    return ((po + 255) / 256) * 256 + pl;
+    MlaWs w;
+    w.q = 0;
+    w.qexp = up((size_t)total_q * kQBytes);
+    w.part_o = w.qexp + up((size_t)total_q * sizeof(int));
+    const size_t po = splits > 1 ? (size_t)total_q * splits * kMlaHeads * kVDim * sizeof(__half) : 0;
+    w.part_lse = w.part_o + up(po);
+    const size_t pl = splits > 1 ? (size_t)total_q * splits * kMlaHeads * sizeof(float) : 0;
+    w.total = w.part_lse + up(pl);
+    return w;
 }
+
+size_t sparse_mla_workspace_bytes(int total_q, int K) { return mla_ws_layout(total_q, K).total; }
+
+// Kernels one sparse-MLA call launches: query preparation, the MMA kernel and,
+// for split batches, the combine.
+int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, K) > 1 ? 3 : 2; }
 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
@@ -544,7 +581,10 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     if (bt.total_q == 0) return cudaSuccess;
     MlaParams p;
     p.bt = bt;
-    p.q_lat = reinterpret_cast<const __nv_bfloat16*>(q_lat);
+    const MlaWs w = mla_ws_layout(bt.total_q, K);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    p.qf16 = wsb + w.q;
+    p.qexp = reinterpret_cast<const int*>(wsb + w.qexp);
     p.latent_pages = static_cast<const uint8_t*>(latent_pages);
     p.indices = indices;
     p.K = K;
@@ -555,9 +595,10 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.out = reinterpret_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     p.status = status;
-    const size_t po = (size_t)bt.total_q * p.splits * kMlaHeads * kVDim * sizeof(__half);
-    p.part_o = static_cast<__half*>(ws);
-    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((po + 255) / 256) * 256);
+    p.part_o = reinterpret_cast<__half*>(wsb + w.part_o);
+    p.part_lse = reinterpret_cast<float*>(wsb + w.part_lse);
+    sparse_mla_prep_q_kernel<<<bt.total_q, 256, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(q_lat), wsb + w.q, reinterpret_cast<int*>(wsb + w.qexp));
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
