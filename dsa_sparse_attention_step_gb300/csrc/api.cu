@@ -9,6 +9,7 @@ namespace dsa {
 cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
                                 const float* w, const void* pages, int key_format,
                                 float* scores, int64_t ld, int32_t* status, cudaStream_t stream);
+bool indexer_supported(const BatchArgs& bt);
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
                         int32_t* out, cudaStream_t stream);
 bool topk_supported(int max_seq);
@@ -77,6 +78,7 @@ dsa_status check_index_args(const dsa_batch* bt, const uint8_t* q8, const float*
                             const float* w, const void* pages, dsa_key_format fmt,
                             const float* scores, int64_t ld) {
     if (fmt != DSA_KEYS_FP8_E4M3 && fmt != DSA_KEYS_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (!indexer_supported(to_args(bt))) return DSA_ERR_UNSUPPORTED;
     if (!q8 || !qscale || !w || !pages || !scores) return DSA_ERR_INVALID_ARG;
     if (!aligned16(q8) || !aligned16(pages) || !aligned16(scores) || !aligned16(qscale) ||
         !aligned16(w))

@@ -22,6 +22,7 @@
 //
 // Roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocation and the
 // MMA-issuing thread, warps 2-9 epilogue.  Every wait is bounded.
+#include <cstring>
 #include <mutex>
 
 #include <cuda.h>
@@ -38,31 +39,43 @@ namespace {
 
 constexpr int kTile = 128;                     // keys per unit
 constexpr int kStages = 6;
-constexpr int kStageBytes = kTile * kIdxDim;   // 16384
-constexpr int kMaxG = 8;                       // tokens per group
-constexpr int kMaxN = kIdxHeads * kMaxG;       // 256
-constexpr int kQBufBytes = kMaxN * kIdxDim;    // 32768
+constexpr int kStageBytes = kTile * kIdxDim;   // 16384: E4M3 A operand of one unit
+constexpr int kQBufBytes = 8 * kIdxHeads * kIdxDim;  // 32768: up to 8 tokens x 32 heads
 constexpr int kMaxReq = 4096;
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
+constexpr int kEpiThreads = 256;               // 8 epilogue warps
+constexpr int kStgSlots = 4;                   // MXFP4: packed-key staging ring
+constexpr int kStgBytes = 2 * kPage * kIdxDim / 2;   // 8192: two pages of packed E2M1
 
-constexpr int kOffStage = 0;
-constexpr int kOffQ = kOffStage + kStages * kStageBytes;        // 98304
-constexpr int kOffW = kOffQ + 2 * kQBufBytes;                    // 163840
-constexpr int kOffReq = kOffW + 2 * kMaxG * kIdxHeads * 4;       // 165888
-constexpr int kOffBar = kOffReq + (kMaxReq + 1) * 4 + 12;        // 182292 -> keep 8-aligned
-constexpr int kOffBarA = (kOffBar + 7) / 8 * 8;
-constexpr int kSmemBytes = kOffBarA + 512;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+// Per-format layout of the kernel.  FP8 keys go straight from TMA to the MMA;
+// MXFP4 keys are staged packed and expanded to E4M3 by four converter warps,
+// and each 32-element block gets its own accumulator (its E8M0 scale is
+// applied in the epilogue), which limits a query group to 2 tokens.
+template <int kFmt>
+struct IdxCfg {
+    static constexpr bool kMx = (kFmt == DSA_KEYS_MXFP4);
+    static constexpr int kConvWarps = kMx ? 4 : 0;
+    static constexpr int kEpiWarp0 = 2 + kConvWarps;
+    static constexpr int kThreads = (kEpiWarp0 + 8) * 32;      // 320 or 448
+    static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
+    static constexpr int kOffStage = 0;
+    static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
+    static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
+    static constexpr int kOffReq = kOffW + 2 * 8 * kIdxHeads * 4;
+    static constexpr int kOffStg = (kOffReq + (kMaxReq + 1) * 4 + 1023) / 1024 * 1024;
+    static constexpr int kOffBar = kOffStg + (kMx ? kStgSlots * kStgBytes : 0);
+    static constexpr int kSmemAlloc = kOffBar + 512 + 1024;
+    static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+};
 
 struct Bars {
-    uint64_t full[kStages];   // TMA -> MMA: key tile landed
-    uint64_t empty[kStages];  // MMA -> TMA: stage free (commit)
+    uint64_t full[kStages];   // TMA / converters -> MMA: key tile ready
+    uint64_t empty[kStages];  // MMA -> TMA / converters: stage free (commit)
     uint64_t tfull[2];        // MMA -> epilogue: accumulator ready (commit)
     uint64_t tempty[2];       // epilogue -> MMA: accumulator drained (256 arrivals)
     uint64_t qfull[2];        // TMA -> MMA: query group landed
     uint64_t qempty[2];       // MMA -> TMA: query buffer free (commit)
+    uint64_t sfull[kStgSlots];   // MXFP4: packed keys landed (bulk copy)
+    uint64_t sempty[kStgSlots];  // MXFP4: staging slot converted (128 arrivals)
     uint64_t done;            // MMA issuer: all its MMAs have completed
     uint32_t tmem_base;
     int abort_flag;
@@ -134,17 +147,49 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const BatchArgs& bt, int 
     } while (c.ngroup == 0 || c.ntile == 0);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
-                      const __grid_constant__ CUtensorMap tm_q, const IdxParams p) {
+// E2M1 magnitude code -> E4M3 code of the same value (0, 0.5, 1, 1.5, 2, 3,
+// 4, 6), as byte lanes of two words for PRMT lookups.
+constexpr uint32_t kE2m1ToE4m3Lo = 0x3C383000u;  // codes 0..3
+constexpr uint32_t kE2m1ToE4m3Hi = 0x4C484440u;  // codes 4..7
+
+// Eight packed E2M1 elements (element 2i in the low nibble of byte i) -> eight
+// E4M3 bytes (exact: every E2M1 value is an E4M3 value).
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w) {
+    uint2 r;
+    const uint32_t mag = w & 0x77777777u;      // 3-bit magnitude codes
+    const uint32_t sgn = w & 0x88888888u;      // sign bits (bit 3 of each nibble)
+    // PRMT selector nibbles pick a byte among the 8 table bytes
+    const uint32_t sel_lo = (mag & 0x7u) | ((mag >> 4) & 0x7u) << 4 | ((mag >> 8) & 0x7u) << 8 |
+                            ((mag >> 12) & 0x7u) << 12;
+    const uint32_t sel_hi = ((mag >> 16) & 0x7u) | ((mag >> 20) & 0x7u) << 4 |
+                            ((mag >> 24) & 0x7u) << 8 | ((mag >> 28) & 0x7u) << 12;
+    r.x = __byte_perm(kE2m1ToE4m3Lo, kE2m1ToE4m3Hi, sel_lo);
+    r.y = __byte_perm(kE2m1ToE4m3Lo, kE2m1ToE4m3Hi, sel_hi);
+    // sign of nibble k -> bit 7 of output byte k
+    const uint32_t s_lo = sgn & 0xFFFFu, s_hi = sgn >> 16;
+    r.x |= ((s_lo >> 3) & 1u) << 7 | ((s_lo >> 7) & 1u) << 15 | ((s_lo >> 11) & 1u) << 23 |
+           ((s_lo >> 15) & 1u) << 31;
+    r.y |= ((s_hi >> 3) & 1u) << 7 | ((s_hi >> 7) & 1u) << 15 | ((s_hi >> 11) & 1u) << 23 |
+           ((s_hi >> 15) & 1u) << 31;
+    return r;
+}
+
+template <int kFmt>
+__global__ void __launch_bounds__(IdxCfg<kFmt>::kThreads, 1)
+indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
+                  const __grid_constant__ CUtensorMap tm_q, const IdxParams p) {
+    using C = IdxCfg<kFmt>;
+    constexpr bool kMx = C::kMx;
+    constexpr int kThreads = C::kThreads;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-    uint8_t* sStage = sm + kOffStage;
-    uint8_t* sQ = sm + kOffQ;
-    float* sW = reinterpret_cast<float*>(sm + kOffW);        // [2][8][32]
-    int* sReq = reinterpret_cast<int*>(sm + kOffReq);         // [B+1]
-    Bars* bars = reinterpret_cast<Bars*>(sm + kOffBarA);
+    uint8_t* sStage = sm + C::kOffStage;
+    uint8_t* sQ = sm + C::kOffQ;
+    float* sW = reinterpret_cast<float*>(sm + C::kOffW);     // [2][8][32]
+    int* sReq = reinterpret_cast<int*>(sm + C::kOffReq);      // [B+1]
+    uint8_t* sStg = sm + C::kOffStg;                          // MXFP4 staging ring
+    Bars* bars = reinterpret_cast<Bars*>(sm + C::kOffBar);
     __shared__ int s_warp_sum[kThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -154,7 +199,7 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&bars->full[i], 1);
+            mbar_init(&bars->full[i], kMx ? 128 : 1);
             mbar_init(&bars->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -163,10 +208,14 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], 1);
         }
+        for (int i = 0; i < kStgSlots; ++i) {
+            mbar_init(&bars->sfull[i], 1);
+            mbar_init(&bars->sempty[i], 128);
+        }
         mbar_init(&bars->done, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tm_keys);
+        if (!kMx) tma_prefetch_desc(&tm_keys);
         tma_prefetch_desc(&tm_q);
     }
     if (warp == 1) {
@@ -210,7 +259,7 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     const int n_units = u_end - u_begin;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- producer: query groups and key pages ----------------
         if (lane == 0 && n_units > 0) {
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
@@ -228,23 +277,34 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     pb = c.b;
                     pg = c.g;
                 }
-                const int st = i % kStages;
-                const int k = i / kStages;
-                if (k >= 1 && !mbar_wait(&bars->empty[st], (k - 1) & 1, abort_flag)) break;
-                uint32_t bytes = 0;
                 int pages[2] = {-1, -1};
+                uint32_t bytes = 0;
                 for (int h = 0; h < 2; ++h) {
                     const int s0 = c.tile * kTile + h * kPage;
                     if (s0 < c.seq) {
                         pages[h] = page_lookup(bt, c.b, s0 / kPage, p.status);
-                        if (pages[h] >= 0) bytes += kPage * kIdxDim;
+                        if (pages[h] >= 0) bytes += kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim;
                     }
                 }
-                mbar_arrive_expect_tx(&bars->full[st], bytes);
-                for (int h = 0; h < 2; ++h)
-                    if (pages[h] >= 0)
-                        tma_load_2d(sStage + st * kStageBytes + h * (kPage * kIdxDim), &tm_keys, 0,
-                                    pages[h] * (kFp8PageBytes / kIdxDim), &bars->full[st]);
+                if (!kMx) {
+                    const int st = i % kStages, k = i / kStages;
+                    if (k >= 1 && !mbar_wait(&bars->empty[st], (k - 1) & 1, abort_flag)) break;
+                    mbar_arrive_expect_tx(&bars->full[st], bytes);
+                    for (int h = 0; h < 2; ++h)
+                        if (pages[h] >= 0)
+                            tma_load_2d(sStage + st * kStageBytes + h * (kPage * kIdxDim), &tm_keys,
+                                        0, pages[h] * (kFp8PageBytes / kIdxDim), &bars->full[st]);
+                } else {
+                    // packed E2M1 bytes of the two pages into a staging slot
+                    const int ss = i % kStgSlots, k = i / kStgSlots;
+                    if (k >= 1 && !mbar_wait(&bars->sempty[ss], (k - 1) & 1, abort_flag)) break;
+                    mbar_arrive_expect_tx(&bars->sfull[ss], bytes);
+                    for (int h = 0; h < 2; ++h)
+                        if (pages[h] >= 0)
+                            bulk_copy_g2s(sStg + ss * kStgBytes + h * (kPage * kIdxDim / 2),
+                                          p.pages + (int64_t)pages[h] * kMxPageBytes,
+                                          (uint32_t)(kPage * kIdxDim / 2), &bars->sfull[ss]);
+                }
                 cursor_next(c, bt, G);
             }
         }
@@ -278,7 +338,10 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     const uint64_t ad = smem_desc(sa + st * kStageBytes + kk * 32, 16, 1024,
                                                   kSwizzle128B);
                     const uint64_t bd = smem_desc(qa + kk * 32, 16, 1024, kSwizzle128B);
-                    mma_f8f6f4(tmem + acc * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    if (kMx)  // one accumulator per 32-element block
+                        mma_f8f6f4(tmem + acc * 4 * N + kk * N, ad, bd, idesc, 0u);
+                    else
+                        mma_f8f6f4(tmem + acc * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars->empty[st]);
                 mma_commit(&bars->tfull[acc]);
@@ -291,11 +354,35 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             mbar_wait(&bars->done, 0, abort_flag);
         }
         __syncwarp();
+    } else if (warp < C::kEpiWarp0) {
+        // ---------------- MXFP4 converters: E2M1 -> E4M3 A-operand tiles ----------
+        const int ctid = tid - 64;  // 0..127
+        for (int i = 0; i < n_units; ++i) {
+            const int ss = i % kStgSlots, st = i % kStages;
+            if (!mbar_wait(&bars->sfull[ss], (i / kStgSlots) & 1, abort_flag)) break;
+            if (i >= kStages && !mbar_wait(&bars->empty[st], ((i / kStages) - 1) & 1, abort_flag))
+                break;
+            const uint8_t* src = sStg + ss * kStgBytes;
+            uint8_t* dst = sStage + st * kStageBytes;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                // 1024 chunks of 16 elements: key r, elements 16c .. 16c+15
+                const int q = ctid + 128 * k;
+                const int r = q >> 3, cidx = q & 7;
+                const uint2 packed = *reinterpret_cast<const uint2*>(src + r * 64 + cidx * 8);
+                const uint2 a = e2m1x8_to_e4m3x8(packed.x);
+                const uint2 b2 = e2m1x8_to_e4m3x8(packed.y);
+                *reinterpret_cast<uint4*>(dst + sw128(r, cidx * 16)) = make_uint4(a.x, a.y, b2.x, b2.y);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->full[st]);
+            mbar_arrive(&bars->sempty[ss]);
+        }
     } else {
         // ---------------- epilogue (thread = key) ----------------
-        const int etid = tid - 64;            // 0..255
-        const int quarter = warp & 3;         // TMEM lanes 32*quarter..+31
-        const int half = (warp - 2) >> 2;     // token parity handled by this warp
+        const int etid = tid - 32 * C::kEpiWarp0;     // 0..255
+        const int quarter = warp & 3;                 // TMEM lanes 32*quarter..+31
+        const int half = (warp - C::kEpiWarp0) >> 2;  // token parity handled by this warp
         if (n_units > 0) {
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
@@ -304,7 +391,7 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 const int gtok0 = c.g * G;                    // first token of the group
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
                 if (c.b != pb || c.g != pg) {
-                    float* wdst = sW + (gcount & 1) * (kMaxG * kIdxHeads);
+                    float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
                     for (int e = etid; e < gr * kIdxHeads; e += kEpiThreads) {
                         const int64_t t = c.q0 + gtok0 + e / kIdxHeads;
                         const int h = e % kIdxHeads;
@@ -315,18 +402,31 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     pb = c.b;
                     pg = c.g;
                 }
-                const float* wq = sW + ((gcount - 1) & 1) * (kMaxG * kIdxHeads);
+                const float* wq = sW + ((gcount - 1) & 1) * (8 * kIdxHeads);
                 const int s = c.tile * kTile + quarter * 32 + lane;
                 const bool in_seq = s < c.seq;
-                float kscale = 0.f;
+                float kscale = 0.f;                   // FP8: per-key scale
+                float bsc[4] = {0.f, 0.f, 0.f, 0.f};  // MXFP4: block scales 2^(e-127)
                 bool page_ok = false;
                 if (in_seq) {
                     const int pg2 = __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + s / kPage);
                     if (pg2 >= 0 && pg2 < bt.num_pages) {
                         page_ok = true;
-                        kscale = __ldg(reinterpret_cast<const float*>(
-                                           p.pages + (int64_t)pg2 * kFp8PageBytes + kPage * kIdxDim) +
-                                       (s % kPage));
+                        if (!kMx) {
+                            kscale = __ldg(reinterpret_cast<const float*>(
+                                               p.pages + (int64_t)pg2 * kFp8PageBytes +
+                                               kPage * kIdxDim) + (s % kPage));
+                        } else {
+                            const uint32_t e4 = __ldg(reinterpret_cast<const uint32_t*>(
+                                p.pages + (int64_t)pg2 * kMxPageBytes + kPage * kIdxDim / 2) +
+                                (s % kPage));
+#pragma unroll
+                            for (int bb = 0; bb < 4; ++bb) {
+                                const int ev = (e4 >> (8 * bb)) & 0xFF;
+                                bsc[bb] = (ev == 0xFF) ? __int_as_float(0x7fffffff)
+                                                       : ldexpf(1.0f, ev - 127);
+                            }
+                        }
                     }
                 }
                 const int acc = i & 1;
@@ -334,24 +434,40 @@ indexer_fp8_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 tc_fence_after();
                 for (int j = half; j < gr; j += 2) {
                     uint32_t v[32];
-                    tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v);
-                    tmem_wait_ld();
+                    float x[32];
+                    if (!kMx) {
+                        tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(v[h]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 32; ++h) x[h] = 0.f;
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb) {
+                            tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * 4 * N + bb * N + 32 * j), v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int h = 0; h < 32; ++h) x[h] = fmaf(bsc[bb], __uint_as_float(v[h]), x[h]);
+                        }
+                    }
                     const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
                     // four independent partial sums keep the FMA pipe busy
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
                     for (int h4 = 0; h4 < 8; ++h4) {
                         const float4 ww = w4[h4];
-                        s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), s0);
-                        s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), s1);
-                        s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), s2);
-                        s3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), s3);
+                        s0 = fmaf(ww.x, fmaxf(x[4 * h4 + 0], 0.f), s0);
+                        s1 = fmaf(ww.y, fmaxf(x[4 * h4 + 1], 0.f), s1);
+                        s2 = fmaf(ww.z, fmaxf(x[4 * h4 + 2], 0.f), s2);
+                        s3 = fmaf(ww.w, fmaxf(x[4 * h4 + 3], 0.f), s3);
                     }
-                    const float sc = (s0 + s1) + (s2 + s3);
+                    float sc = (s0 + s1) + (s2 + s3);
+                    if (!kMx) sc *= kscale;
                     if (in_seq) {
                         const int vis = c.seq - c.nb + gtok0 + j + 1;
                         p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
-                            (s < vis && page_ok) ? sc * kscale : -INFINITY;
+                            (s < vis && page_ok) ? sc : -INFINITY;
                     }
                 }
                 tc_fence_before();
@@ -396,13 +512,12 @@ bool encode_rows128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t b
     return r == CUDA_SUCCESS;
 }
 
-}  // namespace
 
-bool indexer_tc_supported(const BatchArgs& bt) { return bt.num_requests <= kMaxReq; }
-
-cudaError_t launch_index_scores_fp8_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
-                                       const float* w, const void* pages, float* scores,
-                                       int64_t ld, int32_t* status, cudaStream_t stream) {
+template <int kFmt>
+cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscale, const float* w,
+                      const void* pages, float* scores, int64_t ld, int32_t* status,
+                      cudaStream_t stream) {
+    using C = IdxCfg<kFmt>;
     IdxParams p;
     p.bt = bt;
     p.qscale = qscale;
@@ -410,24 +525,39 @@ cudaError_t launch_index_scores_fp8_tc(const BatchArgs& bt, const uint8_t* q8, c
     p.pages = static_cast<const uint8_t*>(pages);
     p.scores = scores;
     p.ld = ld;
-    p.G = bt.max_q < kMaxG ? (bt.max_q > 0 ? bt.max_q : 1) : kMaxG;
+    p.G = bt.max_q < C::kMaxG ? (bt.max_q > 0 ? bt.max_q : 1) : C::kMaxG;
     p.N = kIdxHeads * p.G;
     p.status = status;
     CUtensorMap tm_keys, tm_q;
-    // the index pool as rows of 128 bytes: page p = rows [66p, 66p + 64) + 2 scale rows
-    if (!encode_rows128(&tm_keys, pages, (uint64_t)bt.num_pages * (kFp8PageBytes / kIdxDim),
-                        kPage) ||
-        !encode_rows128(&tm_q, q8, (uint64_t)bt.total_q * kIdxHeads, (uint32_t)p.N))
+    memset(&tm_keys, 0, sizeof(tm_keys));
+    // FP8 index pool as rows of 128 bytes: page p = rows [66p, 66p + 64) + 2 scale rows
+    if (!C::kMx && !encode_rows128(&tm_keys, pages,
+                                   (uint64_t)bt.num_pages * (kFp8PageBytes / kIdxDim), kPage))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(indexer_fp8_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (!encode_rows128(&tm_q, q8, (uint64_t)bt.total_q * kIdxHeads, (uint32_t)p.N))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<kFmt>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    indexer_fp8_tc_kernel<<<sms, kThreads, kSmemAlloc, stream>>>(tm_keys, tm_q, p);
+    indexer_tc_kernel<kFmt><<<sms, C::kThreads, C::kSmemAlloc, stream>>>(tm_keys, tm_q, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+bool indexer_supported(const BatchArgs& bt) { return bt.num_requests <= kMaxReq; }
+
+cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
+                                const float* w, const void* pages, int key_format,
+                                float* scores, int64_t ld, int32_t* status,
+                                cudaStream_t stream) {
+    if (key_format == DSA_KEYS_MXFP4)
+        return launch_tc<DSA_KEYS_MXFP4>(bt, q8, qscale, w, pages, scores, ld, status, stream);
+    return launch_tc<DSA_KEYS_FP8_E4M3>(bt, q8, qscale, w, pages, scores, ld, status, stream);
 }
 
 }  // namespace dsa

@@ -125,7 +125,8 @@ uint64_t dsa_launch_count(void);
  *            of 4.  For token t of request b: scores[t,s] for s < visible(t);
  *            -inf for visible(t) <= s < seq_lens[b]; entries s >= seq_lens[b]
  *            are not written.
- * The key scale (FP8) must be positive: the kernel applies it after the ReLU. */
+ * The key scale (FP8) must be positive: the kernel applies it after the ReLU.
+ * Batches of more than 4096 requests return DSA_ERR_UNSUPPORTED. */
 dsa_status dsa_index_scores(const dsa_batch* batch, const uint8_t* q_fp8,
                             const float* q_scale, const float* w, const void* index_pages,
                             dsa_key_format key_format, float* scores, int64_t score_ld,
