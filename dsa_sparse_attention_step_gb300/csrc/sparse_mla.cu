@@ -8,25 +8,35 @@
 // long-context decode bandwidth" (the 576-byte FP8 latents are read for the
 // selected tokens only).
 //
-// One CTA = one query token x one contiguous split of its index slots.
+// One CTA = one query token x one contiguous split of its index slots, taken
+// in tiles of 64 selected tokens.
 //   S   = Q . L^T    tcgen05 kind::f16, M = 128 (96 heads + 32 unused rows),
-//                    N = 32 selected tokens, K = 576; accumulator in TMEM
-//                    (double buffered, 2 x 32 columns)
+//                    N = 64 selected tokens, K = 576; accumulator in TMEM
 //   O^T = V^T . P^T  M = 128 latent dims (4 tiles cover 512), N = 96 heads,
-//                    K = 32 tokens; accumulator in TMEM (4 x 96 columns)
-// Latents are gathered row by row with 16-byte loads from the paged cache and
-// lifted E4M3 -> f16 exactly into a 128-byte-swizzled tile that serves both as
-// the K-major B operand of S and as the MN-major A operand of O^T.  The bf16
-// query is converted to f16 after a per-token power-of-two scale (exact for
-// every element within 2^-14 of the largest).  Softmax runs online in the
-// log2 domain with conditional rescaling: a head's reference maximum only
-// moves when a new maximum exceeds it by more than 2^8, and the O^T columns
-// are then rescaled in TMEM.
+//                    K = 64 tokens; accumulator in TMEM (4 x 96 columns)
+// An MMA with N <= 64 costs about as much as one with N = 128, so the tile is
+// as wide as shared memory allows: the query (110.6 KB of f16) and one latent
+// tile (73.7 KB of f16) leave no room for a second latent stage.  Instead the
+// tile is refilled in five slab groups (latent dims 0-127, 128-255, 256-383,
+// 384-511 and 512-575): a group is overwritten with the next tile's latents as
+// soon as the MMAs reading it have completed, so the next S = Q . L^T starts
+// while the current O^T update is still running.
+//
+// Latents are gathered with 16-byte loads from the paged cache (each group one
+// tile ahead, in registers) and lifted E4M3 -> f16 exactly into a
+// 128-byte-swizzled tile that serves both as the K-major B operand of S and as
+// the MN-major A operand of O^T.  The bf16 query is converted in the kernel to
+// f16 after a per-token power-of-two scale (exact for every element within
+// 2^-14 of the largest).  Softmax runs online in the log2 domain with
+// conditional rescaling: a head's reference maximum only moves when a new
+// maximum exceeds it by more than 2^8, and the O^T columns are then rescaled
+// in TMEM.
 //
 // Warp roles (256 threads, so a thread may hold up to 255 registers): warps
 // 0-3 softmax (thread = head), warps 4-6 gather/convert producers, warp 7 TMEM
 // allocation and the single MMA-issuing thread; all eight warps share the
-// epilogue (thread = latent dim).  Every wait is bounded.
+// epilogue (thread = latent dim), which stages the result in shared memory and
+// writes it with one bulk copy.  Every wait is bounded.
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -36,33 +46,37 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kTileKeys = 32;
+constexpr int kTileKeys = 64;
 constexpr int kThreads = 256;
 constexpr int kProducers = 96;                                // warps 4-6
-constexpr int kVecPerProducer = kTileKeys * (kLatDim / 16) / kProducers;  // 12
+constexpr int kMmaWarp = 7;
 constexpr int kQRows = 96;
 constexpr int kSlabs = kLatDim / 64;                          // 9 K-slabs of 64 dims
+constexpr int kGroups = 5;                                    // slab groups of a latent tile
 constexpr int kQSlabBytes = kQRows * 128;                     // 12288
 constexpr int kQBytes = kSlabs * kQSlabBytes;                 // 110592
-constexpr int kPBytes = kQRows * 128;                         // 12288 per buffer
-constexpr int kLSlabBytes = kTileKeys * 128;                  // 4096
-constexpr int kLBytes = kSlabs * kLSlabBytes;                 // 36864 per stage
+constexpr int kPBytes = kQRows * 128;                         // 12288: 96 heads x 64 keys f16
+constexpr int kLSlabBytes = kTileKeys * 128;                  // 8192
+constexpr int kLBytes = kSlabs * kLSlabBytes;                 // 73728
+constexpr int kOutBytes = kMlaHeads * kVDim * 2;              // 98304 (bf16 or f16)
 constexpr int kMaxSplitKeys = kTopK;                          // index slots per CTA, max
 constexpr int kOffQ = 0;
 // The M = 128 reads of a 96-row Q slab run 4 KB past it; for the last slab
-// that lands in the P buffers (valid shared memory, unused accumulator rows).
+// that lands in the P buffer (valid shared memory, unused accumulator rows).
 constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffL = kOffP + 2 * kPBytes;
-constexpr int kOffRow = kOffL + 2 * kLBytes;                  // int32 row ids
+constexpr int kOffL = kOffP + kPBytes;
+constexpr int kOffRow = kOffL + kLBytes;                      // int32 row ids
 constexpr int kOffMask = kOffRow + kMaxSplitKeys * 4;         // valid-slot mask per tile
-constexpr int kOffF = kOffMask + (kMaxSplitKeys / kTileKeys) * 4;  // per-head floats
+constexpr int kOffF = kOffMask + (kMaxSplitKeys / kTileKeys) * 8;  // per-head floats
 constexpr int kOffBar = kOffF + 512 * 4;
 constexpr int kSmemBytes = kOffBar + 256;
 constexpr int kSmemAlloc = kSmemBytes + 1024;                 // slack for 1024-B alignment
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+static_assert(kOffP % 1024 == 0 && kOffL % 1024 == 0, "swizzled tiles are 1024-B aligned");
+static_assert(kOutBytes <= kQBytes, "the epilogue stages the output in the query buffer");
 
 // TMEM columns
-constexpr uint32_t kColS = 0;     // two 32-column S buffers
+constexpr uint32_t kColS = 0;     // one 64-column S buffer
 constexpr uint32_t kColO = 64;    // four 96-column O^T tiles
 constexpr uint32_t kTmemCols = 512;
 
@@ -72,26 +86,29 @@ constexpr uint32_t kIdescQK = make_idesc(kFmtF16, kFmtF16, 128, kTileKeys, false
 constexpr uint32_t kIdescPV = make_idesc(kFmtF16, kFmtF16, 128, kQRows, true, false);
 
 struct Bars {
-    uint64_t full[2];    // producer -> MMA: latent stage filled (96 arrivals)
-    uint64_t empty[2];   // MMA -> producer: stage free (commit after PV)
-    uint64_t sfull[2];   // MMA -> softmax: S buffer ready (commit after QK)
-    uint64_t pfull[2];   // softmax -> MMA: P buffer written, S buffer read (128 arrivals)
-    uint64_t pempty[2];  // MMA -> softmax: PV done with P buffer (commit)
-    uint64_t done;       // MMA -> epilogue: everything finished
-    uint64_t qbar;       // bulk copy of the prepared query landed
+    uint64_t lfull[kGroups];   // producers -> MMA: slab group of the latent tile written
+    uint64_t lempty[kGroups];  // MMA -> producers: slab group free (commit)
+    uint64_t sfull;            // MMA -> softmax: S ready, every earlier O^T update done
+    uint64_t pfull;            // softmax -> MMA: P written, S read (128 arrivals)
+    uint64_t done;             // MMA -> epilogue: everything finished
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// 2^x by the special-function unit (flushes results below 2^-126 to zero;
+// 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Named barrier over the 128 softmax threads (warps 0-3).
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Same barrier, returning whether any of the 128 threads passed `pred`.
+// Barrier over the 128 softmax threads (warps 0-3), returning whether any of the 128 threads passed `pred`.
 __device__ __forceinline__ bool softmax_any(bool pred) {
     uint32_t r;
     asm volatile(
@@ -103,15 +120,36 @@ __device__ __forceinline__ bool softmax_any(bool pred) {
     return r != 0;
 }
 
+// Shared -> global bulk copy of `bytes` (16-byte aligned, multiple of 16),
+// waited for until the source has been read.
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Four f16 pairs from eight E4M3 bytes (exact).
+__device__ __forceinline__ void e4m3x8_to_f16x8(uint32_t w0, uint32_t w1, uint32_t (&h)[4]) {
+    const uint32_t wv[2] = {w0, w1};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wv[k] & 0xFFFF), __NV_E4M3);
+        __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wv[k] >> 16), __NV_E4M3);
+        h[2 * k] = *reinterpret_cast<uint32_t*>(&lo);
+        h[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hi);
+    }
+}
+
 struct MlaParams {
     BatchArgs bt;
-    const uint8_t* qf16;   // [T][110592] prepared query (f16, swizzled slabs)
-    const int* qexp;       // [T] power-of-two exponent e of the query scale 2^-e
+    const __nv_bfloat16* q_lat;  // [T][96][576]
     const uint8_t* latent_pages;
     const int32_t* indices;
     int K;                 // index slots per token
     int splits;            // CTAs per token
-    int split_keys;        // index slots per CTA (multiple of 32)
+    int split_keys;        // index slots per CTA (multiple of 64)
     float kv_scale;
     float sm_scale;
     __nv_bfloat16* out;    // final output (splits == 1)
@@ -129,8 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     uint8_t* sP = sm + kOffP;
     uint8_t* sL = sm + kOffL;
     int32_t* sRow = reinterpret_cast<int32_t*>(sm + kOffRow);
-    uint32_t* sMask = reinterpret_cast<uint32_t*>(sm + kOffMask);
-    // [0,256): rescale factors (two buffers of 128), [256,384): m, [384,512): l
+    uint64_t* sMask = reinterpret_cast<uint64_t*>(sm + kOffMask);
+    // [0,128): rescale factors, [256,384): output scale per head, [384,400): reductions
     float* sF = reinterpret_cast<float*>(sm + kOffF);
     Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
 
@@ -145,251 +183,310 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->full[i], kProducers);
-            mbar_init(&bars->empty[i], 1);
-            mbar_init(&bars->sfull[i], 1);
-            mbar_init(&bars->pfull[i], 128);
-            mbar_init(&bars->pempty[i], 1);
+        for (int g = 0; g < kGroups; ++g) {
+            mbar_init(&bars->lfull[g], kProducers);
+            mbar_init(&bars->lempty[g], 1);
         }
+        mbar_init(&bars->sfull, 1);
+        mbar_init(&bars->pfull, 128);
         mbar_init(&bars->done, 1);
-        mbar_init(&bars->qbar, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
-        // the prepared query: one bulk copy into its shared-memory slabs
-        if (ok_tok) {
-            mbar_arrive_expect_tx(&bars->qbar, (uint32_t)kQBytes);
-            bulk_copy_g2s(sQ, p.qf16 + (int64_t)t * kQBytes, (uint32_t)kQBytes, &bars->qbar);
-        } else {
-            mbar_arrive(&bars->qbar);
-        }
     }
-    if (warp == 7) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
 
-    // ---- preamble: row ids (page * 64 + slot) of this CTA's index slots -------
-    for (int k = tid; k < p.split_keys; k += kThreads) {
-        int row = -1;
-        if (ok_tok) {
-            const int s = __ldg(p.indices + (int64_t)t * p.K + slot0 + k);
-            if (s >= seq) {
-                record_error(p.status, DSA_ERR_DEVICE_CHECK);
-            } else if (s >= 0) {
-                const int pg = page_lookup(p.bt, b, s / kPage, p.status);
-                if (pg >= 0) row = pg * kPage + (s % kPage);
+    // ---- preamble 1: row ids (page * 64 + slot) of this CTA's index slots ----
+    // all index loads of a thread first, then all table loads, so the
+    // dependent global reads overlap
+    {
+        constexpr int kPer = (kMaxSplitKeys + kThreads - 1) / kThreads;  // 8
+        int s[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = tid + kThreads * u;
+            s[u] = (ok_tok && k < p.split_keys) ? __ldg(p.indices + (int64_t)t * p.K + slot0 + k) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = tid + kThreads * u;
+            if (k < p.split_keys) {
+                int row = -1;
+                if (s[u] >= seq) {
+                    record_error(p.status, DSA_ERR_DEVICE_CHECK);
+                } else if (s[u] >= 0) {
+                    const int pg = page_lookup(p.bt, b, s[u] / kPage, p.status);
+                    if (pg >= 0) row = pg * kPage + (s[u] % kPage);
+                }
+                sRow[k] = row;
             }
         }
-        sRow[k] = row;
     }
-    if (tid < 2 * 128) sF[tid] = 1.f;
+
+    // ---- preamble 2: the query, bf16 -> f16 after a power-of-two scale 2^-e --
+    // (e = 0 unless max|q| >= 2^15 or < 2^-8; then max|q| * 2^-e lies in
+    // [2^14, 2^15)), written in the 128-byte-swizzled slabs the MMA reads
+    constexpr int kQVec = kMlaHeads * kLatDim / 8 / kThreads;  // 24 vectors of 8 per thread
+    static_assert(kQVec * kThreads * 8 == kMlaHeads * kLatDim, "query split");
+    const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_lat + (int64_t)t * kMlaHeads * kLatDim);
+    float amax = 0.f;
+    if (ok_tok) {
+#pragma unroll 8
+        for (int u = 0; u < kQVec; ++u) {
+            const uint4 r = __ldg(qsrc + tid + kThreads * u);
+            const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[i] << 16)),
+                                         fabsf(__uint_as_float(wv[i] & 0xFFFF0000u))));
+        }
+    }
+    amax = warp_max(amax);
+    if (lane == 0) sF[384 + warp] = amax;
+    __syncthreads();  // also publishes sRow
+    float qmax = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) qmax = fmaxf(qmax, sF[384 + w]);
+    int e = 0;
+    if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
+        int ex;
+        frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
+        e = ex - 15;
+    }
+    if (ok_tok) {
+        const float qmul = ldexpf(1.0f, -e);
+#pragma unroll 8
+        for (int u = 0; u < kQVec; ++u) {
+            const int v = tid + kThreads * u;
+            const uint4 r = __ldg(qsrc + v);
+            const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
+            const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
+                                  __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
+            *reinterpret_cast<uint4*>(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    // valid-slot mask per tile (one ballot per 32 slots)
+    for (int i = warp; i < n_tiles; i += kThreads / 32) {
+        const uint32_t lo = __ballot_sync(0xffffffffu, sRow[i * kTileKeys + lane] >= 0);
+        const uint32_t hi = __ballot_sync(0xffffffffu, sRow[i * kTileKeys + 32 + lane] >= 0);
+        if (lane == 0) sMask[i] = ((uint64_t)hi << 32) | lo;
+    }
+    if (tid < 128) sF[tid] = 1.f;
+    fence_proxy_async_smem();  // the query slabs are read by the tensor cores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    const bool producer = (warp >= 4 && warp < 7);
-    const int e = ok_tok ? __ldg(p.qexp + t) : 0;
-    if (!producer) {
-        // warps 0-3 and 7: valid-slot masks while the producers start gathering
-        const int ctid = (warp == 7) ? 128 + lane : tid;  // 0..159
-        for (int i = ctid; i < n_tiles; i += 160) {
-            uint32_t m = 0;
-            for (int j = 0; j < kTileKeys; ++j) m |= (sRow[i * kTileKeys + j] >= 0 ? 1u : 0u) << j;
-            sMask[i] = m;
-        }
-        asm volatile("bar.sync 2, 160;" ::: "memory");
-    }
     const uint32_t tmem = bars->tmem_base;
     // z in log2 units per unit of the f16 accumulator
     const float zscale = p.sm_scale * p.kv_scale * ldexpf(1.0f, e) * 1.4426950408889634f;
 
-    if (producer) {
+    if (warp >= 4 && warp < kMmaWarp) {
         // ---------------- producers: gather + E4M3 -> f16 ----------------
-        // 32 rows x 36 vectors of 16 bytes = 1152 vectors -> 12 per thread per
-        // tile; two tiles of loads are kept in flight (registers A and B)
-        const int ptid = tid - 128;
-        uint4 rawA[kVecPerProducer], rawB[kVecPerProducer];
-#define DSA_MLA_LOAD(raw_, i_)                                                           \
-    _Pragma("unroll") for (int u = 0; u < kVecPerProducer; ++u) {                        \
-        const int v = ptid + kProducers * u;                                              \
-        const int r = v / 36, c = v % 36;                                                 \
-        const int row = sRow[(i_) * kTileKeys + r];                                       \
-        raw_[u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(                      \
-                                         p.latent_pages + (int64_t)row * kLatDim) + c)    \
-                             : make_uint4(0, 0, 0, 0);                                    \
+        // a tile is 64 rows x 36 chunks of 16 bytes; slab group g < 4 holds
+        // chunks 8g..8g+7 of every row (512 chunks: 6 per thread of warp 4,
+        // 5 per thread of warps 5-6), group 4 chunks 32..35 (256 chunks: 3 per
+        // thread of warps 4-5, 2 per thread of warp 6).  A group is refilled
+        // as soon as it is free, and its next tile is then loaded into the
+        // same registers.
+        const int pt = tid - 128;
+        uint4 raw[kGroups][6];
+#define DSA_MLA_CHUNK(g_, u_, r_, c_)                                          \
+    const int r_ = ((g_) < 4) ? ((ptv >> 3) + 12 * (u_)) : ((ptv >> 2) + 24 * (u_)); \
+    const int c_ = ((g_) < 4) ? (8 * (g_) + (ptv & 7)) : (32 + (ptv & 3));
+#define DSA_MLA_NCHUNK(g_) ((g_) < 4 ? 6 : 3)
+#define DSA_MLA_HAS(g_, u_) (pt + kProducers * (u_) < ((g_) < 4 ? 512 : 256))
+#define DSA_MLA_LOAD(i_, g_)                                                   \
+    _Pragma("unroll") for (int u = 0; u < DSA_MLA_NCHUNK(g_); ++u) {            \
+        if (!DSA_MLA_HAS(g_, u)) continue;                                      \
+        DSA_MLA_CHUNK(g_, u, r, c)                                              \
+        const int row = sRow[(i_) * kTileKeys + r];                             \
+        raw[g_][u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(          \
+                                            p.latent_pages + (int64_t)row * kLatDim) + c) \
+                                : make_uint4(0u, 0u, 0u, 0u);                   \
     }
-#define DSA_MLA_STORE(raw_, st_)                                                         \
-    _Pragma("unroll") for (int u = 0; u < kVecPerProducer; ++u) {                        \
-        const int v = ptid + kProducers * u;                                              \
-        const int r = v / 36, c = v % 36;                                                 \
-        const uint32_t wv[4] = {raw_[u].x, raw_[u].y, raw_[u].z, raw_[u].w};              \
-        uint32_t hv[8];                                                                   \
-        _Pragma("unroll") for (int k = 0; k < 4; ++k) {                                   \
-            __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(                                  \
-                (__nv_fp8x2_storage_t)(wv[k] & 0xFFFF), __NV_E4M3);                       \
-            __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(                                  \
-                (__nv_fp8x2_storage_t)(wv[k] >> 16), __NV_E4M3);                          \
-            hv[2 * k] = *reinterpret_cast<uint32_t*>(&lo);                                \
-            hv[2 * k + 1] = *reinterpret_cast<uint32_t*>(&hi);                            \
-        }                                                                                 \
-        uint8_t* base = sL + (st_) * kLBytes + (c / 4) * kLSlabBytes;                     \
-        *reinterpret_cast<uint4*>(base + sw128(r, (c % 4) * 32)) =                        \
-            make_uint4(hv[0], hv[1], hv[2], hv[3]);                                       \
-        *reinterpret_cast<uint4*>(base + sw128(r, (c % 4) * 32 + 16)) =                   \
-            make_uint4(hv[4], hv[5], hv[6], hv[7]);                                       \
+#define DSA_MLA_STORE(g_)                                                      \
+    _Pragma("unroll") for (int u = 0; u < DSA_MLA_NCHUNK(g_); ++u) {            \
+        if (!DSA_MLA_HAS(g_, u)) continue;                                      \
+        DSA_MLA_CHUNK(g_, u, r, c)                                              \
+        uint32_t h0[4], h1[4];                                                  \
+        e4m3x8_to_f16x8(raw[g_][u].x, raw[g_][u].y, h0);                        \
+        e4m3x8_to_f16x8(raw[g_][u].z, raw[g_][u].w, h1);                        \
+        uint8_t* base = sL + (c >> 2) * kLSlabBytes;                            \
+        *reinterpret_cast<uint4*>(base + sw128(r, (c & 3) * 32)) =              \
+            make_uint4(h0[0], h0[1], h0[2], h0[3]);                             \
+        *reinterpret_cast<uint4*>(base + sw128(r, (c & 3) * 32 + 16)) =         \
+            make_uint4(h1[0], h1[1], h1[2], h1[3]);                             \
     }
-        if (n_tiles > 0) { DSA_MLA_LOAD(rawA, 0) }
-        if (n_tiles > 1) { DSA_MLA_LOAD(rawB, 1) }
-        for (int i = 0; i < n_tiles; i += 2) {
-            if (i >= 2 && !mbar_wait(&bars->empty[0], ((i - 2) >> 1) & 1, abort_flag)) break;
-            DSA_MLA_STORE(rawA, 0)
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->full[0]);
-            if (i + 2 < n_tiles) { DSA_MLA_LOAD(rawA, i + 2) }
-            if (i + 1 >= n_tiles) break;
-            if (i + 1 >= 2 && !mbar_wait(&bars->empty[1], ((i - 1) >> 1) & 1, abort_flag)) break;
-            DSA_MLA_STORE(rawB, 1)
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->full[1]);
-            if (i + 3 < n_tiles) { DSA_MLA_LOAD(rawB, i + 3) }
+        if (n_tiles > 0) {
+            const int ptv = pt;
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) { DSA_MLA_LOAD(0, g) }
         }
+        bool ok = true;
+        for (int i = 0; i < n_tiles && ok; ++i) {
+            // index arithmetic is redone every tile rather than kept live
+            int ptv = pt;
+            asm volatile("" : "+r"(ptv));
+            // group 4 (latent dims 512-575) is freed first: S alone reads it
+#pragma unroll
+            for (int gi = 0; gi < kGroups; ++gi) {
+                const int g = (gi == 0) ? 4 : gi - 1;
+                if (i > 0 && !mbar_wait(&bars->lempty[g], (i - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                DSA_MLA_STORE(g)
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->lfull[g]);
+                if (i + 1 < n_tiles) { DSA_MLA_LOAD(i + 1, g) }
+            }
+        }
+#undef DSA_MLA_CHUNK
+#undef DSA_MLA_NCHUNK
+#undef DSA_MLA_HAS
 #undef DSA_MLA_LOAD
 #undef DSA_MLA_STORE
-    } else if (warp == 7) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one thread) ----------------
+        // descriptors are built once; operand offsets are added in 16-byte
+        // units (the start-address field cannot carry: shared addresses are
+        // below 256 KB)
         if (lane == 0) {
-            const uint32_t qa = smem_u32(sQ), pa = smem_u32(sP), la = smem_u32(sL);
-            auto issue_pv = [&](int i) -> bool {
-                const int st = i & 1;
-                if (!mbar_wait(&bars->pfull[st], (i >> 1) & 1, abort_flag)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const uint64_t ad = smem_desc(
-                            la + st * kLBytes + (2 * mt) * kLSlabBytes + ks * 2048, kLSlabBytes,
-                            1024, kSwizzle128B);
-                        const uint64_t bd =
-                            smem_desc(pa + st * kPBytes + ks * 32, 16, 1024, kSwizzle128B);
-                        mma_f16(tmem + kColO + 96 * mt, ad, bd, kIdescPV,
-                                (i > 0 || ks > 0) ? 1u : 0u);
-                    }
-                mma_commit(&bars->empty[st]);
-                mma_commit(&bars->pempty[st]);
-                return true;
-            };
-            bool ok = mbar_wait(&bars->qbar, 0, abort_flag);
+            const uint64_t qd = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
+            const uint64_t ld = smem_desc(smem_u32(sL), 16, 1024, kSwizzle128B);
+            const uint64_t vd = smem_desc(smem_u32(sL), kLSlabBytes, 1024, kSwizzle128B);
+            const uint64_t pd = smem_desc(smem_u32(sP), 16, 1024, kSwizzle128B);
+            bool ok = true;
             for (int i = 0; i < n_tiles && ok; ++i) {
-                const int st = i & 1;
-                ok = mbar_wait(&bars->full[st], (i >> 1) & 1, abort_flag);
-                if (ok && i >= 2)
-                    ok = mbar_wait(&bars->pfull[st], ((i - 2) >> 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                for (int j = 0; j < kSlabs; ++j)
+                // S = Q . L^T, slab group by slab group as the producers fill them
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad =
-                            smem_desc(qa + j * kQSlabBytes + kk * 32, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(la + st * kLBytes + j * kLSlabBytes + kk * 32,
-                                                      16, 1024, kSwizzle128B);
-                        mma_f16(tmem + kColS + 32 * st, ad, bd, kIdescQK, (j | kk) ? 1u : 0u);
+                for (int g = 0; g < kGroups; ++g) {
+                    if (!mbar_wait(&bars->lfull[g], i & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                mma_commit(&bars->sfull[st]);
-                if (i >= 1) ok = issue_pv(i - 1);
+                    tc_fence_after();
+#pragma unroll
+                    for (int s = 2 * g; s < 2 * g + (g < 4 ? 2 : 1); ++s)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16(tmem + kColS,
+                                    qd + (uint64_t)((s * kQSlabBytes + kk * 32) >> 4),
+                                    ld + (uint64_t)((s * kLSlabBytes + kk * 32) >> 4), kIdescQK,
+                                    (s | kk) ? 1u : 0u);
+                }
+                if (!ok) break;
+                mma_commit(&bars->lempty[4]);
+                mma_commit(&bars->sfull);
+                // O^T += V^T . P^T once the softmax has written P
+                if (!mbar_wait(&bars->pfull, i & 1, abort_flag)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16(tmem + kColO + 96 * c,
+                                vd + (uint64_t)((2 * c * kLSlabBytes + ks * 2048) >> 4),
+                                pd + (uint64_t)((ks * 32) >> 4), kIdescPV,
+                                (i > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&bars->lempty[c]);
+                }
             }
-            if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
             mma_commit(&bars->done);  // also drains whatever is in flight after an abort
         }
         __syncwarp();
     } else {
         // ---------------- softmax (thread = head) ----------------
-        const int h = tid;  // 0..127; rows 96..127 are padding
-        const bool real = h < kQRows;
+        const int h = tid;  // 0..127; rows 96..127 (warp 3) are padding
         float m_ref = -INFINITY, l = 0.f;
         for (int i = 0; i < n_tiles; ++i) {
-            const int st = i & 1;
-            if (!mbar_wait(&bars->sfull[st], (i >> 1) & 1, abort_flag)) break;
+            if (!mbar_wait(&bars->sfull, i & 1, abort_flag)) break;
             tc_fence_after();
-            uint32_t r[32];
-            tmem_ld32(tmem_addr(tmem, 32 * warp, kColS + 32 * st), r);
-            tmem_wait_ld();
-            const uint32_t mask = sMask[i];
-            float z[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                z[j] = ((mask >> j) & 1u) ? __uint_as_float(r[j]) * zscale : -INFINITY;
-            // pairwise trees keep the dependency chains short
-            float mx[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) mx[j] = fmaxf(z[2 * j], z[2 * j + 1]);
-#pragma unroll
-            for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
-            const float mt = mx[0];
+            // S(i) is complete and so is every earlier O^T update; nothing
+            // touches O^T again before this thread arrives on pfull
             float factor = 1.f;
             bool resc = false;
-            if (real && mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog2)) {
-                factor = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
-                m_ref = mt;
-                resc = (i > 0);
+            if (warp < 3) {
+                uint32_t r[64];
+                tmem_ld32(tmem_addr(tmem, 32 * warp, kColS), *reinterpret_cast<uint32_t(*)[32]>(r));
+                tmem_ld32(tmem_addr(tmem, 32 * warp, kColS + 32),
+                          *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+                tmem_wait_ld();
+                const uint64_t mask = sMask[i];
+                if (mask != ~0ull) {
+                    // empty slots score -inf
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (!((mask >> j) & 1u)) r[j] = __float_as_uint(-INFINITY);
+                }
+                // the maximum of the raw accumulators (zscale > 0 keeps the order)
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 64; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(r[j]));
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * zscale;
+                if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog2)) {
+                    factor = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
+                    m_ref = mt;
+                    resc = (i > 0);
+                }
+                // P(i) -> its shared-memory row (the buffer's last reader, the
+                // previous O^T update, has completed).  p = 2^(z - m_ref) with
+                // z = s * zscale; an empty slot gives 2^-inf = 0, and while
+                // m_ref is -inf every slot so far was empty.
+                const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                const bool none = (m_ref == -INFINITY);
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t ph[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int j = 8 * c + 2 * k;
+                        float p0 = ex2_approx(fmaf(__uint_as_float(r[j]), zscale, nm));
+                        float p1 = ex2_approx(fmaf(__uint_as_float(r[j + 1]), zscale, nm));
+                        if (none) p0 = p1 = 0.f;
+                        ps[k] += p0 + p1;
+                        ph[k] = pack_half2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4*>(sP + sw128(h, 16 * c)) =
+                        make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                }
+                l = l * factor + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
             }
-            uint32_t ph[16];
-            float ps[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float p0 = ((mask >> (2 * j)) & 1u) ? exp2f(z[2 * j] - m_ref) : 0.f;
-                const float p1 = ((mask >> (2 * j + 1)) & 1u) ? exp2f(z[2 * j + 1] - m_ref) : 0.f;
-                ps[j] = p0 + p1;
-                ph[j] = pack_half2(p0, p1);
-            }
-#pragma unroll
-            for (int w2 = 8; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                for (int j = 0; j < w2; ++j) ps[j] += ps[j + w2];
-            const float psum = ps[0];
-            l = l * factor + psum;
-            float* fac = sF + 128 * (i & 1);
-            fac[h] = resc ? factor : 1.f;
-            const bool any = softmax_any(resc);
-            // P buffer st was last read by PV(i-2); O^T is complete up to PV(i-1)
-            if (i >= 2 && !mbar_wait(&bars->pempty[st], ((i - 2) >> 1) & 1, abort_flag)) break;
-            if (any) {
-                if (!mbar_wait(&bars->pempty[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) break;
-                tc_fence_after();
-                for (int mtile = 0; mtile < 4; ++mtile)
-                    for (int c = 0; c < 3; ++c) {
-                        const uint32_t a = tmem_addr(tmem, 32 * warp, kColO + 96 * mtile + 32 * c);
+            sF[h] = resc ? factor : 1.f;
+            if (softmax_any(resc)) {
+                // every warp rescales the O^T lanes (latent dims) it may access
+                for (int c = 0; c < 4; ++c)
+                    for (int hg = 0; hg < 3; ++hg) {
+                        const uint32_t a = tmem_addr(tmem, 32 * warp, kColO + 96 * c + 32 * hg);
                         uint32_t o[32];
                         tmem_ld32(a, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            o[j] = __float_as_uint(__uint_as_float(o[j]) * fac[32 * c + j]);
+                            o[j] = __float_as_uint(__uint_as_float(o[j]) * sF[32 * hg + j]);
                         tmem_st32(a, o);
                     }
                 tmem_wait_st();
             }
-            if (real) {
-                uint8_t* row = sP + st * kPBytes;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4*>(row + sw128(h, 16 * c)) =
-                        make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-            }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars->pfull[st]);
+            mbar_arrive(&bars->pfull);
         }
         // ---------------- end of softmax: per-head normaliser ----------------
         const bool ok = mbar_wait(&bars->done, 0, abort_flag);
         tc_fence_after();
         const float scale_out = (p.splits == 1) ? p.kv_scale : 1.f;
         sF[256 + h] = (l > 0.f) ? scale_out / l : 0.f;
-        if (ok && ok_tok && real) {
+        if (ok && ok_tok && h < kQRows) {
             const float lse2 = (l > 0.f) ? m_ref + log2f(l) : -INFINITY;
             if (p.splits == 1) {
                 if (p.lse) p.lse[(int64_t)t * kMlaHeads + h] = lse2 * 0.6931471805599453f;
@@ -397,139 +494,106 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 p.part_lse[((int64_t)t * p.splits + split) * kMlaHeads + h] = lse2;
             }
         }
-        tc_fence_before();
     }
 
     // ---------------- epilogue: O^T / l -> bf16 output or f16 partial ----------
     // warps 0-3 take latent-dim tiles 0-1, warps 4-7 tiles 2-3 (a warp reads
-    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads
-    if (warp < 8) {
-        asm volatile("bar.sync 3, 256;" ::: "memory");
+    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads.  The
+    // [96][512] result is staged in the (now unused) query buffer and leaves
+    // with one bulk copy.
+    {
+        __syncthreads();  // the softmax warps have seen `done` and written 1/l
         tc_fence_after();
-        if (!*abort_flag && ok_tok) {
+        const bool write = !*abort_flag && ok_tok;
+        if (write) {
             const int lq = warp & 3;
             const int mt0 = (warp < 4) ? 0 : 2;
-            for (int c = 0; c < 3; ++c) {
-                float inv[32];
+            for (int mt = mt0; mt < mt0 + 2; ++mt) {
+                const int d = 128 * mt + 32 * lq + lane;
+                uint32_t o[96];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4*>(sF + 256 + 32 * c + j);
-                    inv[j] = v4.x; inv[j + 1] = v4.y; inv[j + 2] = v4.z; inv[j + 3] = v4.w;
-                }
-                for (int mt = mt0; mt < mt0 + 2; ++mt) {
-                    const int d = 128 * mt + 32 * lq + lane;
-                    uint32_t o[32];
-                    tmem_ld32(tmem_addr(tmem, 32 * lq, kColO + 96 * mt + 32 * c), o);
-                    tmem_wait_ld();
-                    if (p.splits == 1) {
-                        __nv_bfloat16* dst = p.out + ((int64_t)t * kMlaHeads + 32 * c) * kVDim + d;
+                for (int hg = 0; hg < 3; ++hg)
+                    tmem_ld32(tmem_addr(tmem, 32 * lq, kColO + 96 * mt + 32 * hg),
+                              *reinterpret_cast<uint32_t(*)[32]>(o + 32 * hg));
+                tmem_wait_ld();
+                if (p.splits == 1) {
+                    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sQ) + d;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            dst[(int64_t)j * kVDim] = __float2bfloat16_rn(__uint_as_float(o[j]) * inv[j]);
-                    } else {
-                        __half* dst = p.part_o +
-                                      (((int64_t)t * p.splits + split) * kMlaHeads + 32 * c) * kVDim + d;
+                    for (int j = 0; j < 96; ++j)
+                        st[j * kVDim] = __float2bfloat16_rn(__uint_as_float(o[j]) * sF[256 + j]);
+                } else {
+                    __half* st = reinterpret_cast<__half*>(sQ) + d;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            dst[(int64_t)j * kVDim] = __float2half_rn(__uint_as_float(o[j]) * inv[j]);
-                    }
+                    for (int j = 0; j < 96; ++j)
+                        st[j * kVDim] = __float2half_rn(__uint_as_float(o[j]) * sF[256 + j]);
                 }
             }
+            fence_proxy_async_smem();  // the bulk copy reads the staged result
+        }
+        __syncthreads();
+        if (write && tid == 0) {
+            void* dst = (p.splits == 1)
+                            ? static_cast<void*>(p.out + (int64_t)t * kMlaHeads * kVDim)
+                            : static_cast<void*>(p.part_o + ((int64_t)t * p.splits + split) *
+                                                                 kMlaHeads * kVDim);
+            bulk_store_s2g(dst, sQ, (uint32_t)kOutBytes);
         }
     }
 
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && tid == 0) record_error(p.status, DSA_ERR_TIMEOUT);
-    if (warp == 7) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Prepare each token's query once: bf16 -> f16 with a power-of-two scale 2^-e
-// (e = 0 unless max|q| >= 2^15 or < 2^-8; then max|q| * 2^-e lies in
-// [2^14, 2^15)), written in the 128-byte-swizzled slab layout the MMA reads,
-// so every CTA of the token loads it with one bulk copy.
+// Merge the split partials of 8 heads of one token: out = kv_scale *
+// sum_s 2^(lse_s - L) o_s with L = log2 sum_s 2^lse_s, in a fixed order over
+// the splits.  Thread = (head, 16 consecutive latent dims).
+constexpr int kCombineHeads = 8;
 __global__ void __launch_bounds__(256)
-sparse_mla_prep_q_kernel(const __nv_bfloat16* __restrict__ q_lat, uint8_t* __restrict__ qf16,
-                         int* __restrict__ qexp) {
-    constexpr int kVec = kMlaHeads * kLatDim / 8 / 256;  // 27 vectors of 8 per thread
-    __shared__ float s_max[8];
-    const int t = blockIdx.x, tid = threadIdx.x;
-    const uint4* src = reinterpret_cast<const uint4*>(q_lat + (int64_t)t * kMlaHeads * kLatDim);
-    uint4 raw[kVec];
-    float amax = 0.f;
-#pragma unroll
-    for (int u = 0; u < kVec; ++u) {
-        raw[u] = __ldg(src + tid + 256 * u);
-        const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[i] << 16)),
-                                     fabsf(__uint_as_float(wv[i] & 0xFFFF0000u))));
-    }
-    amax = warp_max(amax);
-    if ((tid & 31) == 0) s_max[tid >> 5] = amax;
-    __syncthreads();
-    float qmax = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) qmax = fmaxf(qmax, s_max[w]);
-    int e = 0;
-    if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
-        int ex;
-        frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
-        e = ex - 15;
-    }
-    const float qmul = ldexpf(1.0f, -e);
-    uint8_t* dst = qf16 + (int64_t)t * kQBytes;
-#pragma unroll
-    for (int u = 0; u < kVec; ++u) {
-        const int v = tid + 256 * u;
-        const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
-        const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
-                              __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
-        *reinterpret_cast<uint4*>(dst + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    if (tid == 0) qexp[t] = e;
-}
-
-// Merge the split partials: out = sum_s 2^(lse_s - L) o_s with
-// L = log2 sum_s 2^lse_s, in a fixed order over the splits.
-__global__ void __launch_bounds__(128)
 sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __restrict__ part_lse,
                           int splits, float kv_scale, __nv_bfloat16* __restrict__ out,
                           float* __restrict__ lse) {
-    const int t = blockIdx.x / kMlaHeads, h = blockIdx.x % kMlaHeads;
-    __shared__ float w_s[64];
-    __shared__ float s_total;
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int s = 0; s < splits; ++s)
-            M = fmaxf(M, part_lse[((int64_t)t * splits + s) * kMlaHeads + h]);
-        float tot = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float ls = part_lse[((int64_t)t * splits + s) * kMlaHeads + h];
-            const float wgt = (M == -INFINITY) ? 0.f : exp2f(ls - M);
-            w_s[s] = wgt;
-            tot += wgt;
+    constexpr int kGroupsPerToken = kMlaHeads / kCombineHeads;  // 12
+    const int t = blockIdx.x / kGroupsPerToken;
+    const int h = (blockIdx.x % kGroupsPerToken) * kCombineHeads + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int d0 = lane * 16;
+    // split weights: lane s holds split s (splits <= 32)
+    const float ls = (lane < splits) ? part_lse[((int64_t)t * splits + lane) * kMlaHeads + h]
+                                     : -INFINITY;
+    const float M = warp_max(ls);
+    const float wgt = (M == -INFINITY || lane >= splits) ? 0.f : exp2f(ls - M);
+    const float tot = warp_sum(wgt);
+    if (lane == 0 && lse)
+        lse[(int64_t)t * kMlaHeads + h] =
+            (tot > 0.f) ? (M + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, wgt, s);
+        const uint4* src = reinterpret_cast<const uint4*>(
+            part_o + (((int64_t)t * splits + s) * kMlaHeads + h) * kVDim + d0);
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
+            acc[2 * j] += ws * f.x;
+            acc[2 * j + 1] += ws * f.y;
         }
-        s_total = tot;
-        if (lse)
-            lse[(int64_t)t * kMlaHeads + h] =
-                (tot > 0.f) ? (M + log2f(tot)) * 0.6931471805599453f : -INFINITY;
     }
-    __syncthreads();
-    const float inv = (s_total > 0.f) ? kv_scale / s_total : 0.f;
-    for (int d = threadIdx.x; d < kVDim; d += 128) {
-        float acc = 0.f;
-        for (int s = 0; s < splits; ++s)
-            acc += w_s[s] *
-                   __half2float(part_o[(((int64_t)t * splits + s) * kMlaHeads + h) * kVDim + d]);
-        out[((int64_t)t * kMlaHeads + h) * kVDim + d] = __float2bfloat16_rn(acc * inv);
+    const float inv = (tot > 0.f) ? kv_scale / tot : 0.f;
+    uint32_t ob[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+        ob[j] = *reinterpret_cast<uint32_t*>(&b2);
     }
+    uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)t * kMlaHeads + h) * kVDim + d0);
+    dst[0] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    dst[1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
 }
 
 }  // namespace
@@ -548,21 +612,19 @@ int sparse_mla_splits(int total_q, int K) {
     return splits;
 }
 
-// Workspace: prepared queries [T][110592], exponents [T], then for split
-// batches the f16 partial outputs [T, splits, 96, 512] and lse [T, splits, 96].
+// Workspace (split batches only): the f16 partial outputs [T, splits, 96, 512]
+// and their lse [T, splits, 96].
 struct MlaWs {
-    size_t q, qexp, part_o, part_lse, total;
+    size_t part_o, part_lse, total;
 };
 
 MlaWs mla_ws_layout(int total_q, int K) {
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     const int splits = sparse_mla_splits(total_q, K);
     MlaWs w;
-    w.q = 0;
-    w.qexp = up((size_t)total_q * kQBytes);
-    w.part_o = w.qexp + up((size_t)total_q * sizeof(int));
+    w.part_o = 0;
     const size_t po = splits > 1 ? (size_t)total_q * splits * kMlaHeads * kVDim * sizeof(__half) : 0;
-    w.part_lse = w.part_o + up(po);
+    w.part_lse = up(po);
     const size_t pl = splits > 1 ? (size_t)total_q * splits * kMlaHeads * sizeof(float) : 0;
     w.total = w.part_lse + up(pl);
     return w;
@@ -570,9 +632,9 @@ MlaWs mla_ws_layout(int total_q, int K) {
 
 size_t sparse_mla_workspace_bytes(int total_q, int K) { return mla_ws_layout(total_q, K).total; }
 
-// Kernels one sparse-MLA call launches: query preparation, the MMA kernel and,
-// for split batches, the combine.
-int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, K) > 1 ? 3 : 2; }
+// Kernels one sparse-MLA call launches: the MMA kernel and, for split
+// batches, the combine.
+int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, K) > 1 ? 2 : 1; }
 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
@@ -583,8 +645,7 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.bt = bt;
     const MlaWs w = mla_ws_layout(bt.total_q, K);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
-    p.qf16 = wsb + w.q;
-    p.qexp = reinterpret_cast<const int*>(wsb + w.qexp);
+    p.q_lat = reinterpret_cast<const __nv_bfloat16*>(q_lat);
     p.latent_pages = static_cast<const uint8_t*>(latent_pages);
     p.indices = indices;
     p.K = K;
@@ -595,17 +656,15 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.out = reinterpret_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     p.status = status;
-    p.part_o = reinterpret_cast<__half*>(wsb + w.part_o);
-    p.part_lse = reinterpret_cast<float*>(wsb + w.part_lse);
-    sparse_mla_prep_q_kernel<<<bt.total_q, 256, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(q_lat), wsb + w.q, reinterpret_cast<int*>(wsb + w.qexp));
+    p.part_o = p.splits > 1 ? reinterpret_cast<__half*>(wsb + w.part_o) : nullptr;
+    p.part_lse = p.splits > 1 ? reinterpret_cast<float*>(wsb + w.part_lse) : nullptr;
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     sparse_mla_tc_kernel<<<bt.total_q * p.splits, kThreads, kSmemAlloc, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;
-    sparse_mla_combine_kernel<<<bt.total_q * kMlaHeads, 128, 0, stream>>>(
+    sparse_mla_combine_kernel<<<bt.total_q * (kMlaHeads / kCombineHeads), 256, 0, stream>>>(
         p.part_o, p.part_lse, p.splits, kv_scale, p.out, lse);
     return cudaGetLastError();
 }
