@@ -11,11 +11,11 @@ cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const fl
                                 float* scores, int64_t ld, int32_t* status, cudaStream_t stream);
 bool indexer_supported(const BatchArgs& bt);
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
-                        int32_t* out, cudaStream_t stream);
+                        int32_t* out, bool pdl, cudaStream_t stream);
 bool topk_supported(int max_seq);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
-                              uint16_t* out, float* lse, void* ws, int32_t* status,
+                              uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
                               cudaStream_t stream);
 size_t sparse_mla_workspace_bytes(int total_q, int K);
 int sparse_mla_launches(int total_q, int K);
@@ -152,7 +152,7 @@ dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_l
     (void)ws;
     if (batch->total_q == 0) return DSA_OK;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cuda_status(launch_topk(to_args(batch), scores, score_ld, topk, indices,
+    return cuda_status(launch_topk(to_args(batch), scores, score_ld, topk, indices, false,
                                    (cudaStream_t)stream));
 }
 
@@ -175,7 +175,7 @@ dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const v
     g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk),
                          std::memory_order_relaxed);
     return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
-                                         indices, topk, out, lse, ws, dev_status,
+                                         indices, topk, out, lse, ws, dev_status, false,
                                          (cudaStream_t)stream));
 }
 
@@ -213,10 +213,12 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
                          std::memory_order_relaxed);
     cudaError_t e = launch_index_scores(a, q_fp8, q_scale, w, index_pages, (int)key_format,
                                         scores, ld, dev_status, s);
-    if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, s);
+    // the later kernels only read what the kernel before them writes after
+    // their grid-dependency wait, so each may start while its predecessor runs
+    if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, true, s);
     if (e == cudaSuccess)
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
-                              base + off_mla, dev_status, s);
+                              base + off_mla, dev_status, true, s);
     return cuda_status(e);
 }
 

@@ -181,6 +181,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     using C = IdxCfg<kFmt>;
     constexpr bool kMx = C::kMx;
     constexpr int kThreads = C::kThreads;
+    grid_dependents_launch();  // the top-k may start its preamble
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));

@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    grid_dependents_launch();
     const int t = blockIdx.x / p.splits;
     const int split = blockIdx.x % p.splits;
     const int b = request_of(p.bt, t);
@@ -198,34 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         tmem_relinquish();
     }
 
-    // ---- preamble 1: row ids (page * 64 + slot) of this CTA's index slots ----
-    // all index loads of a thread first, then all table loads, so the
-    // dependent global reads overlap
-    {
-        constexpr int kPer = (kMaxSplitKeys + kThreads - 1) / kThreads;  // 8
-        int s[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int k = tid + kThreads * u;
-            s[u] = (ok_tok && k < p.split_keys) ? __ldg(p.indices + (int64_t)t * p.K + slot0 + k) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int k = tid + kThreads * u;
-            if (k < p.split_keys) {
-                int row = -1;
-                if (s[u] >= seq) {
-                    record_error(p.status, DSA_ERR_DEVICE_CHECK);
-                } else if (s[u] >= 0) {
-                    const int pg = page_lookup(p.bt, b, s[u] / kPage, p.status);
-                    if (pg >= 0) row = pg * kPage + (s[u] % kPage);
-                }
-                sRow[k] = row;
-            }
-        }
-    }
-
-    // ---- preamble 2: the query, bf16 -> f16 after a power-of-two scale 2^-e --
+    // ---- preamble 1: the query, bf16 -> f16 after a power-of-two scale 2^-e --
     // (e = 0 unless max|q| >= 2^15 or < 2^-8; then max|q| * 2^-e lies in
     // [2^14, 2^15)), written in the 128-byte-swizzled slabs the MMA reads
     constexpr int kQVec = kMlaHeads * kLatDim / 8 / kThreads;  // 24 vectors of 8 per thread
@@ -245,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     }
     amax = warp_max(amax);
     if (lane == 0) sF[384 + warp] = amax;
-    __syncthreads();  // also publishes sRow
+    __syncthreads();
     float qmax = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) qmax = fmaxf(qmax, sF[384 + w]);
@@ -272,6 +246,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
+    grid_dependency_wait();  // the indices come from the previous kernel
+    // ---- preamble 2: row ids (page * 64 + slot) of this CTA's index slots ----
+    // all index loads of a thread first, then all table loads, so the
+    // dependent global reads overlap
+    {
+        constexpr int kPer = (kMaxSplitKeys + kThreads - 1) / kThreads;  // 8
+        int s[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = tid + kThreads * u;
+            s[u] = (ok_tok && k < p.split_keys) ? __ldg(p.indices + (int64_t)t * p.K + slot0 + k) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int k = tid + kThreads * u;
+            if (k < p.split_keys) {
+                int row = -1;
+                if (s[u] >= seq) {
+                    record_error(p.status, DSA_ERR_DEVICE_CHECK);
+                } else if (s[u] >= 0) {
+                    const int pg = page_lookup(p.bt, b, s[u] / kPage, p.status);
+                    if (pg >= 0) row = pg * kPage + (s[u] % kPage);
+                }
+                sRow[k] = row;
+            }
+        }
+    }
+
+    __syncthreads();
     // valid-slot mask per tile (one ballot per 32 slots)
     for (int i = warp; i < n_tiles; i += kThreads / 32) {
         const uint32_t lo = __ballot_sync(0xffffffffu, sRow[i * kTileKeys + lane] >= 0);
@@ -555,6 +558,7 @@ sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __rest
                           int splits, float kv_scale, __nv_bfloat16* __restrict__ out,
                           float* __restrict__ lse) {
     constexpr int kGroupsPerToken = kMlaHeads / kCombineHeads;  // 12
+    grid_dependency_wait();  // the partials come from the previous kernel
     const int t = blockIdx.x / kGroupsPerToken;
     const int h = (blockIdx.x % kGroupsPerToken) * kCombineHeads + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -638,7 +642,7 @@ int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, 
 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
-                              uint16_t* out, float* lse, void* ws, int32_t* status,
+                              uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
                               cudaStream_t stream) {
     if (bt.total_q == 0) return cudaSuccess;
     MlaParams p;
@@ -661,12 +665,12 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
-    sparse_mla_tc_kernel<<<bt.total_q * p.splits, kThreads, kSmemAlloc, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_kernel(sparse_mla_tc_kernel, dim3(bt.total_q * p.splits), dim3(kThreads),
+                      (size_t)kSmemAlloc, stream, pdl, 1, p);
     if (e != cudaSuccess || p.splits == 1) return e;
-    sparse_mla_combine_kernel<<<bt.total_q * (kMlaHeads / kCombineHeads), 256, 0, stream>>>(
-        p.part_o, p.part_lse, p.splits, kv_scale, p.out, lse);
-    return cudaGetLastError();
+    return launch_kernel(sparse_mla_combine_kernel, dim3(bt.total_q * (kMlaHeads / kCombineHeads)),
+                         dim3(256), 0, stream, true, 1, (const __half*)p.part_o,
+                         (const float*)p.part_lse, p.splits, kv_scale, p.out, lse);
 }
 
 }  // namespace dsa

@@ -236,11 +236,13 @@ topk_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
     const int rank = (int)cluster.block_rank();
     const int t = blockIdx.x / cs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dependents_launch();
     const int b = request_of(bt, t);
     int32_t* o = out + (int64_t)t * K;
     // uniform over the cluster: every CTA of token t takes the same branches
     const bool ok = token_ok(bt, b, t, nullptr);
     const int vis = ok ? visible_of(bt, b, t) : 0;
+    grid_dependency_wait();  // the scores come from the previous kernel
     if (vis <= K) {
         if (rank == 0)
             for (int i = tid; i < K; i += kThreads) o[i] = (i < vis) ? i : -1;
@@ -534,26 +536,252 @@ topk_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
     if (cs > 1) cluster.sync();  // no CTA leaves while others may read its shared memory
 }
 
-template <bool kRes>
-cudaError_t launch(const BatchArgs& bt, const float* scores, int64_t ld, int K, int32_t* out,
-                   int cs, cudaStream_t stream) {
-    const size_t smem = sizeof(TopkSmem<kRes>);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<kRes>,
+// ---------------------------------------------------------------------------
+// Rows of at most 32768 visible positions: one CTA per query token, the whole
+// row resident in shared memory.
+//   A. Load the row once (every load in flight at the same time), store its
+//      order keys and build the histogram of their top 12 bits.
+//   B. Bin b holding the k-th largest key, and rem = how many keys bin b must
+//      still give.
+//   C. Copy the keys of bin b (usually a few hundred) into a candidate list.
+//   D. Two radix levels (10 + 10 bits) over the candidates give tau, the k-th
+//      largest key, and eq_take, how many keys equal to tau are selected.  When
+//      bin b holds more keys than the list, the levels sweep the resident row.
+//   E. Thread i owns positions [32i, 32i + 32): it selects the keys above tau
+//      and, among those equal to tau, the lowest positions still needed (one
+//      block-wide scan of packed counts), and writes them in order.
+// Keys are stored in 16-byte chunks permuted within groups of eight (chunk c
+// at c ^ ((c >> 3) & 7)), so both the strided pass of A/C and the contiguous
+// per-thread reads of E are free of bank conflicts.
+constexpr int kResCand = 4096;
+
+struct ResSmem {
+    alignas(16) uint32_t keys[kResidentMax];
+    uint32_t hist[kBins];
+    uint32_t cand[kResCand];
+    uint32_t warp_tot[kWarps + 1];
+    uint32_t s_digit, s_rem, s_count, pad;
+};
+
+__device__ __forceinline__ int swz_chunk(int c) { return c ^ ((c >> 3) & 7); }
+
+// Block-wide exclusive prefix sum of unsigned values (1024 threads).
+__device__ __forceinline__ uint32_t block_excl_sum_u(uint32_t v, uint32_t* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = warp_tot[lane];
+        uint32_t inc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += u;
+        }
+        warp_tot[lane] = inc - w;
+    }
+    __syncthreads();
+    return incl - v + warp_tot[warp];
+}
+
+// Digit d over nb bins of h with count(> d) < rem <= count(>= d): sets
+// s_digit and s_rem (= rem minus the count above d).  All threads call it.
+__device__ void res_find_digit(ResSmem& S, const uint32_t* h, int nb, uint32_t rem) {
+    const int per = nb / kThreads;  // 4 or 1
+    const int tid = threadIdx.x;
+    uint32_t part = 0;
+    for (int i = 0; i < per; ++i) part += h[nb - 1 - (per * tid + i)];
+    const uint32_t above = block_excl_sum_u(part, S.warp_tot);
+    if (above < rem && rem <= above + part) {
+        uint32_t run = above;
+        for (int i = 0; i < per; ++i) {
+            const int bin = nb - 1 - (per * tid + i);
+            if (run + h[bin] >= rem) {
+                S.s_digit = (uint32_t)bin;
+                S.s_rem = rem - run;
+                break;
+            }
+            run += h[bin];
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
+                     int32_t* __restrict__ out) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    ResSmem& S = *reinterpret_cast<ResSmem*>(smem_raw);
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
+    grid_dependents_launch();
+    const int b = request_of(bt, t);
+    int32_t* o = out + (int64_t)t * K;
+    const bool ok = token_ok(bt, b, t, nullptr);
+    const int vis = ok ? visible_of(bt, b, t) : 0;
+    for (int i = tid; i < kBins; i += kThreads) S.hist[i] = 0;
+    if (tid == 0) S.s_count = 0;
+    grid_dependency_wait();  // the scores come from the previous kernel
+    if (vis <= K) {
+        for (int i = tid; i < K; i += kThreads) o[i] = (i < vis) ? i : -1;
+        return;
+    }
+    __syncthreads();
+    const float* row = scores + (int64_t)t * ld;
+    constexpr int kChunksPerThread = kResidentMax / 4 / kThreads;  // 8
+
+    // ---- A. load, order keys, top-12-bit histogram ------------------------
+    {
+        float4 x[kChunksPerThread];
+#pragma unroll
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int c = tid + kThreads * u;
+            // positions 4c..4c+3 lie below round_up(vis, 4) <= ld
+            x[u] = (4 * c < vis) ? __ldg(reinterpret_cast<const float4*>(row) + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int c = tid + kThreads * u;
+            const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            uint32_t k4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = 4 * c + e < vis;
+                k4[e] = valid ? order_key(xv[e]) : 0u;
+                if (valid) atomicAdd(&S.hist[k4[e] >> 20], 1u);
+            }
+            *reinterpret_cast<uint4*>(&S.keys[4 * swz_chunk(c)]) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+        }
+    }
+    __syncthreads();
+
+    // ---- B. the bin of the k-th largest key --------------------------------
+    res_find_digit(S, S.hist, kBins, (uint32_t)K);
+    const uint32_t bin = S.s_digit;
+    uint32_t rem = S.s_rem;
+    const uint32_t nbin = S.hist[bin];
+    const bool listed = nbin <= (uint32_t)kResCand;
+
+    // ---- C. the keys of that bin ------------------------------------------
+    if (listed) {
+#pragma unroll
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int c = tid + kThreads * u;
+            const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
+            const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+            uint32_t m = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                m |= (4 * c + e < vis && (k4[e] >> 20) == bin) ? (1u << e) : 0u;
+            const int n = __popc(m);
+            int incl = n;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o2);
+                if (lane >= o2) incl += v;
+            }
+            const int wsum = __shfl_sync(0xffffffffu, incl, 31);
+            if (wsum == 0) continue;
+            int base = 0;
+            if (lane == 31) base = (int)atomicAdd(&S.s_count, (uint32_t)wsum);
+            base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (m & (1u << e)) S.cand[base++] = k4[e];
+        }
+    }
+
+    // ---- D. two radix levels below the bin --------------------------------
+    uint32_t prefix = bin << 20;
+    for (int level = 1; level < 3; ++level) {
+        const int shift = (level == 1) ? 10 : 0;
+        const uint32_t pshift = (level == 1) ? 20 : 10;
+        __syncthreads();  // previous readers of hist are done; the list is complete
+        for (int i = tid; i < 1024; i += kThreads) S.hist[i] = 0;
+        __syncthreads();
+        if (listed) {
+            for (int i = tid; i < (int)nbin; i += kThreads) {
+                const uint32_t key = S.cand[i];
+                if ((key >> pshift) == (prefix >> pshift)) atomicAdd(&S.hist[(key >> shift) & 0x3FFu], 1u);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kChunksPerThread; ++u) {
+                const int c = tid + kThreads * u;
+                const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
+                const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * c + e < vis && (k4[e] >> pshift) == (prefix >> pshift))
+                        atomicAdd(&S.hist[(k4[e] >> shift) & 0x3FFu], 1u);
+            }
+        }
+        __syncthreads();
+        res_find_digit(S, S.hist, 1024, rem);
+        prefix |= S.s_digit << shift;
+        rem = S.s_rem;
+    }
+    const uint32_t tau = prefix;
+    const uint32_t eq_take = rem;  // keys equal to tau that are selected (lowest positions)
+
+    // ---- E. ordered output --------------------------------------------------
+    uint32_t mgt = 0, meq = 0;
+#pragma unroll
+    for (int j = 0; j < kChunksPerThread; ++j) {
+        const int c = kChunksPerThread * tid + j;
+        const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
+        const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool valid = 4 * c + e < vis;
+            mgt |= (valid && k4[e] > tau) ? (1u << (4 * j + e)) : 0u;
+            meq |= (valid && k4[e] == tau) ? (1u << (4 * j + e)) : 0u;
+        }
+    }
+    // counts packed as (eq << 16) | gt: per-row totals stay below 2^16 each
+    const uint32_t before = block_excl_sum_u((uint32_t)__popc(mgt) | ((uint32_t)__popc(meq) << 16),
+                                             S.warp_tot);
+    const uint32_t gt_before = before & 0xFFFFu, eq_before = before >> 16;
+    uint32_t take = eq_take > eq_before ? min(eq_take - eq_before, (uint32_t)__popc(meq)) : 0u;
+    uint32_t sel = mgt;
+    for (uint32_t m = meq; take > 0; --take) {
+        sel |= m & (~m + 1u);  // lowest remaining equal position
+        m &= m - 1;
+    }
+    int pos = (int)(gt_before + min(eq_before, eq_take));
+    const int p0 = 32 * tid;
+    while (sel) {
+        const int j = __ffs(sel) - 1;
+        o[pos++] = p0 + j;
+        sel &= sel - 1;
+    }
+}
+
+cudaError_t launch_streaming(const BatchArgs& bt, const float* scores, int64_t ld, int K,
+                             int32_t* out, int cs, bool pdl, cudaStream_t stream) {
+    const size_t smem = sizeof(TopkSmem<false>);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(bt.total_q * cs, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_kernel<kRes>, bt, scores, ld, K, out);
+    return launch_kernel(topk_kernel<false>, dim3(bt.total_q * cs), dim3(kThreads), smem, stream,
+                         pdl, cs, bt, scores, ld, K, out);
+}
+
+cudaError_t launch_resident(const BatchArgs& bt, const float* scores, int64_t ld, int K,
+                            int32_t* out, bool pdl, cudaStream_t stream) {
+    const size_t smem = sizeof(ResSmem);
+    cudaError_t e = cudaFuncSetAttribute(topk_resident_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(topk_resident_kernel, dim3(bt.total_q), dim3(kThreads), smem, stream, pdl,
+                         1, bt, scores, ld, K, out);
 }
 
 }  // namespace
@@ -570,11 +798,11 @@ int topk_cluster_size(int total_q, int max_seq) {
 bool topk_supported(int max_seq) { return max_seq <= kSliceMax * kMaxCluster; }
 
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
-                        int32_t* out, cudaStream_t stream) {
+                        int32_t* out, bool pdl, cudaStream_t stream) {
     if (bt.total_q == 0) return cudaSuccess;
-    if (bt.max_seq <= kResidentMax) return launch<true>(bt, scores, ld, K, out, 1, stream);
-    return launch<false>(bt, scores, ld, K, out, topk_cluster_size(bt.total_q, bt.max_seq),
-                         stream);
+    if (bt.max_seq <= kResidentMax) return launch_resident(bt, scores, ld, K, out, pdl, stream);
+    return launch_streaming(bt, scores, ld, K, out, topk_cluster_size(bt.total_q, bt.max_seq), pdl,
+                            stream);
 }
 
 }  // namespace dsa

@@ -95,3 +95,17 @@ def test_topk_one_million_positions():
     rng = np.random.default_rng(11)
     lens = [1 << 20]
     _run(lens, [1], rng.standard_normal((1, 1 << 20)))
+
+
+@pytest.mark.parametrize("kind", ["equal", "normal", "few_levels"])
+def test_topk_resident_row_limits(kind):
+    """Rows at the resident-path size limit (32768 positions, where the packed
+    counts of equal keys reach 2^15) next to rows at and just above k."""
+    lens, counts = [32768, 2049, 2048, 1], [1, 1, 1, 1]
+    ld = 32768
+    rng = np.random.default_rng(3)
+    if kind == "equal":
+        s = np.full((4, ld), -1.25)
+    else:
+        s = _scores(rng, 4, ld, kind)
+    _run(lens, counts, s)
