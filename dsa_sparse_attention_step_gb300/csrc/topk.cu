@@ -543,24 +543,21 @@ topk_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
 //      order keys and build the histogram of their top 12 bits.
 //   B. Bin b holding the k-th largest key, and rem = how many keys bin b must
 //      still give.
-//   C. Copy the keys of bin b (usually a few hundred) into a candidate list.
-//   D. Two radix levels (10 + 10 bits) over the candidates give tau, the k-th
-//      largest key, and eq_take, how many keys equal to tau are selected.  When
-//      bin b holds more keys than the list, the levels sweep the resident row.
-//   E. Thread i owns positions [32i, 32i + 32): it selects the keys above tau
+//   C. Two radix levels (10 + 10 bits) over the resident keys of bin b give
+//      tau, the k-th largest key, and eq_take, how many keys equal to tau are
+//      selected.
+//   D. Thread i owns positions [32i, 32i + 32): it selects the keys above tau
 //      and, among those equal to tau, the lowest positions still needed (one
 //      block-wide scan of packed counts), and writes them in order.
-// Keys are stored in 16-byte chunks permuted within groups of eight (chunk c
-// at c ^ ((c >> 3) & 7)), so both the strided pass of A/C and the contiguous
-// per-thread reads of E are free of bank conflicts.
-constexpr int kResCand = 4096;
-
+// Every pass stops at the row's visible length.  Keys are stored in 16-byte
+// chunks permuted within groups of eight (chunk c at c ^ ((c >> 3) & 7)), so
+// the strided passes of A/C and the contiguous per-thread reads of D are free
+// of bank conflicts.
 struct ResSmem {
     alignas(16) uint32_t keys[kResidentMax];
     uint32_t hist[kBins];
-    uint32_t cand[kResCand];
     uint32_t warp_tot[kWarps + 1];
-    uint32_t s_digit, s_rem, s_count, pad;
+    uint32_t s_digit, s_rem, pad0, pad1;
 };
 
 __device__ __forceinline__ int swz_chunk(int c) { return c ^ ((c >> 3) & 7); }
@@ -619,14 +616,13 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
     extern __shared__ __align__(16) uint8_t smem_raw[];
     ResSmem& S = *reinterpret_cast<ResSmem*>(smem_raw);
     const int t = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     grid_dependents_launch();
     const int b = request_of(bt, t);
     int32_t* o = out + (int64_t)t * K;
     const bool ok = token_ok(bt, b, t, nullptr);
     const int vis = ok ? visible_of(bt, b, t) : 0;
     for (int i = tid; i < kBins; i += kThreads) S.hist[i] = 0;
-    if (tid == 0) S.s_count = 0;
     grid_dependency_wait();  // the scores come from the previous kernel
     if (vis <= K) {
         for (int i = tid; i < K; i += kThreads) o[i] = (i < vis) ? i : -1;
@@ -635,6 +631,10 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
     __syncthreads();
     const float* row = scores + (int64_t)t * ld;
     constexpr int kChunksPerThread = kResidentMax / 4 / kThreads;  // 8
+    // strided passes: chunk c = tid + 1024u holds positions 4c..4c+3; a warp
+    // stops once its first chunk lies past the row
+    const int nchunk = (vis + 3) / 4;
+    auto warp_live = [&](int u) { return 32 * warp + kThreads * u < nchunk; };
 
     // ---- A. load, order keys, top-12-bit histogram ------------------------
     {
@@ -643,11 +643,12 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
         for (int u = 0; u < kChunksPerThread; ++u) {
             const int c = tid + kThreads * u;
             // positions 4c..4c+3 lie below round_up(vis, 4) <= ld
-            x[u] = (4 * c < vis) ? __ldg(reinterpret_cast<const float4*>(row) + c)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[u] = (c < nchunk) ? __ldg(reinterpret_cast<const float4*>(row) + c)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kChunksPerThread; ++u) {
+            if (!warp_live(u)) break;
             const int c = tid + kThreads * u;
             const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
             uint32_t k4[4];
@@ -664,64 +665,25 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
 
     // ---- B. the bin of the k-th largest key --------------------------------
     res_find_digit(S, S.hist, kBins, (uint32_t)K);
-    const uint32_t bin = S.s_digit;
+    uint32_t prefix = S.s_digit << 20;
     uint32_t rem = S.s_rem;
-    const uint32_t nbin = S.hist[bin];
-    const bool listed = nbin <= (uint32_t)kResCand;
 
-    // ---- C. the keys of that bin ------------------------------------------
-    if (listed) {
-#pragma unroll
-        for (int u = 0; u < kChunksPerThread; ++u) {
-            const int c = tid + kThreads * u;
-            const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
-            const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
-            uint32_t m = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                m |= (4 * c + e < vis && (k4[e] >> 20) == bin) ? (1u << e) : 0u;
-            const int n = __popc(m);
-            int incl = n;
-#pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o2);
-                if (lane >= o2) incl += v;
-            }
-            const int wsum = __shfl_sync(0xffffffffu, incl, 31);
-            if (wsum == 0) continue;
-            int base = 0;
-            if (lane == 31) base = (int)atomicAdd(&S.s_count, (uint32_t)wsum);
-            base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (m & (1u << e)) S.cand[base++] = k4[e];
-        }
-    }
-
-    // ---- D. two radix levels below the bin --------------------------------
-    uint32_t prefix = bin << 20;
+    // ---- C. two radix levels below the bin, over the resident keys --------
     for (int level = 1; level < 3; ++level) {
         const int shift = (level == 1) ? 10 : 0;
         const uint32_t pshift = (level == 1) ? 20 : 10;
-        __syncthreads();  // previous readers of hist are done; the list is complete
         for (int i = tid; i < 1024; i += kThreads) S.hist[i] = 0;
         __syncthreads();
-        if (listed) {
-            for (int i = tid; i < (int)nbin; i += kThreads) {
-                const uint32_t key = S.cand[i];
-                if ((key >> pshift) == (prefix >> pshift)) atomicAdd(&S.hist[(key >> shift) & 0x3FFu], 1u);
-            }
-        } else {
 #pragma unroll
-            for (int u = 0; u < kChunksPerThread; ++u) {
-                const int c = tid + kThreads * u;
-                const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
-                const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            if (!warp_live(u)) break;
+            const int c = tid + kThreads * u;
+            const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
+            const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (4 * c + e < vis && (k4[e] >> pshift) == (prefix >> pshift))
-                        atomicAdd(&S.hist[(k4[e] >> shift) & 0x3FFu], 1u);
-            }
+            for (int e = 0; e < 4; ++e)
+                if ((k4[e] >> pshift) == (prefix >> pshift) && 4 * c + e < vis)
+                    atomicAdd(&S.hist[(k4[e] >> shift) & 0x3FFu], 1u);
         }
         __syncthreads();
         res_find_digit(S, S.hist, 1024, rem);
@@ -731,18 +693,20 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
     const uint32_t tau = prefix;
     const uint32_t eq_take = rem;  // keys equal to tau that are selected (lowest positions)
 
-    // ---- E. ordered output --------------------------------------------------
+    // ---- D. ordered output --------------------------------------------------
     uint32_t mgt = 0, meq = 0;
+    if (32 * 32 * warp < vis) {  // the warp's 1024 positions start inside the row
 #pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-        const int c = kChunksPerThread * tid + j;
-        const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
-        const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
+        for (int j = 0; j < kChunksPerThread; ++j) {
+            const int c = kChunksPerThread * tid + j;
+            const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
+            const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const bool valid = 4 * c + e < vis;
-            mgt |= (valid && k4[e] > tau) ? (1u << (4 * j + e)) : 0u;
-            meq |= (valid && k4[e] == tau) ? (1u << (4 * j + e)) : 0u;
+            for (int e = 0; e < 4; ++e) {
+                const bool valid = 4 * c + e < vis;
+                mgt |= (valid && k4[e] > tau) ? (1u << (4 * j + e)) : 0u;
+                meq |= (valid && k4[e] == tau) ? (1u << (4 * j + e)) : 0u;
+            }
         }
     }
     // counts packed as (eq << 16) | gt: per-row totals stay below 2^16 each
