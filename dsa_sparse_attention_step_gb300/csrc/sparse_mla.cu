@@ -201,63 +201,64 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 
     // ---- preamble 1: the query, bf16 -> f16 after a power-of-two scale 2^-e --
     // (e = 0 unless max|q| >= 2^15 or < 2^-8; then max|q| * 2^-e lies in
-    // [2^14, 2^15)), written in the 128-byte-swizzled slabs the MMA reads
-    constexpr int kQVec = kMlaHeads * kLatDim / 8 / kThreads;  // 24 vectors of 8 per thread
+    // [2^14, 2^15)), written in the 128-byte-swizzled slabs the MMA reads.
+    // One pass converts with e = 0 while finding max|q|; a token that needs
+    // e != 0 is converted again.
+    constexpr int kQVec = kMlaHeads * kLatDim / 8 / kThreads;  // 27 vectors of 8 per thread
     static_assert(kQVec * kThreads * 8 == kMlaHeads * kLatDim, "query split");
     const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_lat + (int64_t)t * kMlaHeads * kLatDim);
-    float amax = 0.f;
-    if (ok_tok) {
-#pragma unroll 8
-        for (int u = 0; u < kQVec; ++u) {
-            const uint4 r = __ldg(qsrc + tid + kThreads * u);
-            const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(wv[i] << 16)),
-                                         fabsf(__uint_as_float(wv[i] & 0xFFFF0000u))));
-        }
-    }
-    amax = warp_max(amax);
-    if (lane == 0) sF[384 + warp] = amax;
-    __syncthreads();
-    float qmax = 0.f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) qmax = fmaxf(qmax, sF[384 + w]);
-    int e = 0;
-    if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
-        int ex;
-        frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
-        e = ex - 15;
-    }
-    if (ok_tok) {
-        const float qmul = ldexpf(1.0f, -e);
-#pragma unroll 8
+    auto convert_q = [&](float qmul) {
+        float amax = 0.f;
+#pragma unroll 9
         for (int u = 0; u < kQVec; ++u) {
             const int v = tid + kThreads * u;
-            const uint4 r = __ldg(qsrc + v);
+            const uint4 r = ok_tok ? __ldg(qsrc + v) : make_uint4(0u, 0u, 0u, 0u);
             const int h = v / (kLatDim / 8), c = v % (kLatDim / 8);
             const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
             uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                o[i] = pack_half2(__uint_as_float(wv[i] << 16) * qmul,
-                                  __uint_as_float(wv[i] & 0xFFFF0000u) * qmul);
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(wv[i] << 16), hi = __uint_as_float(wv[i] & 0xFFFF0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                o[i] = pack_half2(lo * qmul, hi * qmul);
+            }
             *reinterpret_cast<uint4*>(sQ + (c / 8) * kQSlabBytes + sw128(h, (c % 8) * 16)) =
                 make_uint4(o[0], o[1], o[2], o[3]);
         }
+        return amax;
+    };
+    int e = 0;
+    {
+        const float amax = warp_max(convert_q(1.0f));
+        if (lane == 0) sF[384 + warp] = amax;
+        __syncthreads();
+        float qmax = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) qmax = fmaxf(qmax, sF[384 + w]);
+        if (qmax > 0.f && (qmax >= 32768.f || qmax < 0.00390625f)) {
+            int ex;
+            frexpf(qmax, &ex);  // qmax = f * 2^ex, f in [0.5, 1)
+            e = ex - 15;
+            (void)convert_q(ldexpf(1.0f, -e));  // uniform over the CTA
+        }
     }
+
     grid_dependency_wait();  // the indices come from the previous kernel
     // ---- preamble 2: row ids (page * 64 + slot) of this CTA's index slots ----
-    // all index loads of a thread first, then all table loads, so the
-    // dependent global reads overlap
+    // every index load of a thread, then every table load (unconditional, at
+    // a clamped page), so the dependent global reads overlap
     {
         constexpr int kPer = (kMaxSplitKeys + kThreads - 1) / kThreads;  // 8
-        int s[kPer];
+        int s[kPer], pg[kPer];
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = tid + kThreads * u;
             s[u] = (ok_tok && k < p.split_keys) ? __ldg(p.indices + (int64_t)t * p.K + slot0 + k) : -1;
         }
+        const int32_t* table = p.bt.block_table + (int64_t)b * p.bt.max_pages;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            pg[u] = __ldg(table + ((s[u] >= 0 && s[u] < seq) ? s[u] / kPage : 0));
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = tid + kThreads * u;
@@ -266,14 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 if (s[u] >= seq) {
                     record_error(p.status, DSA_ERR_DEVICE_CHECK);
                 } else if (s[u] >= 0) {
-                    const int pg = page_lookup(p.bt, b, s[u] / kPage, p.status);
-                    if (pg >= 0) row = pg * kPage + (s[u] % kPage);
+                    if (pg[u] < 0 || pg[u] >= p.bt.num_pages) record_error(p.status, DSA_ERR_DEVICE_CHECK);
+                    else row = pg[u] * kPage + (s[u] % kPage);
                 }
                 sRow[k] = row;
             }
         }
     }
-
     __syncthreads();
     // valid-slot mask per tile (one ballot per 32 slots)
     for (int i = warp; i < n_tiles; i += kThreads / 32) {
@@ -467,17 +467,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             sF[h] = resc ? factor : 1.f;
             if (softmax_any(resc)) {
                 // every warp rescales the O^T lanes (latent dims) it may access
-                for (int c = 0; c < 4; ++c)
-                    for (int hg = 0; hg < 3; ++hg) {
+                for (int hg = 0; hg < 3; ++hg) {
+                    float fac[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(sF + 32 * hg + j);
+                        fac[j] = v4.x; fac[j + 1] = v4.y; fac[j + 2] = v4.z; fac[j + 3] = v4.w;
+                    }
+                    for (int c = 0; c < 4; ++c) {
                         const uint32_t a = tmem_addr(tmem, 32 * warp, kColO + 96 * c + 32 * hg);
                         uint32_t o[32];
                         tmem_ld32(a, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            o[j] = __float_as_uint(__uint_as_float(o[j]) * sF[32 * hg + j]);
+                            o[j] = __float_as_uint(__uint_as_float(o[j]) * fac[j]);
                         tmem_st32(a, o);
                     }
+                }
                 tmem_wait_st();
             }
             fence_proxy_async_smem();
@@ -519,16 +526,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                     tmem_ld32(tmem_addr(tmem, 32 * lq, kColO + 96 * mt + 32 * hg),
                               *reinterpret_cast<uint32_t(*)[32]>(o + 32 * hg));
                 tmem_wait_ld();
-                if (p.splits == 1) {
-                    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sQ) + d;
+                // the per-head scales go to registers first: a shared load
+                // between the (possibly aliasing) stores would serialise them
 #pragma unroll
-                    for (int j = 0; j < 96; ++j)
-                        st[j * kVDim] = __float2bfloat16_rn(__uint_as_float(o[j]) * sF[256 + j]);
-                } else {
-                    __half* st = reinterpret_cast<__half*>(sQ) + d;
+                for (int hg = 0; hg < 3; ++hg) {
+                    float inv[32];
 #pragma unroll
-                    for (int j = 0; j < 96; ++j)
-                        st[j * kVDim] = __float2half_rn(__uint_as_float(o[j]) * sF[256 + j]);
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(sF + 256 + 32 * hg + j);
+                        inv[j] = v4.x; inv[j + 1] = v4.y; inv[j + 2] = v4.z; inv[j + 3] = v4.w;
+                    }
+                    if (p.splits == 1) {
+                        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sQ) + d;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            st[(32 * hg + j) * kVDim] =
+                                __float2bfloat16_rn(__uint_as_float(o[32 * hg + j]) * inv[j]);
+                    } else {
+                        __half* st = reinterpret_cast<__half*>(sQ) + d;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            st[(32 * hg + j) * kVDim] =
+                                __float2half_rn(__uint_as_float(o[32 * hg + j]) * inv[j]);
+                    }
                 }
             }
             fence_proxy_async_smem();  // the bulk copy reads the staged result

@@ -200,3 +200,29 @@ def test_host_validation_errors():
     with pytest.raises(dsa.DsaError) as e:
         dsa.dsa_topk(gl.batch, S, 128, 1024, idx)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("log2_scale", [16, -12])
+def test_query_exponent_paths(log2_scale):
+    """A query whose largest magnitude is >= 2^15 or < 2^-8 is rescaled by a
+    power of two before it is lifted to f16.  Scaling q_lat by 2^s and the
+    softmax scale by 2^-s leaves the exact result unchanged, so the oracle's
+    output for the scaled inputs must be matched on that path too."""
+    layer = di.make_layer([3000, 700, 2049], [2, 1, 1], di.KEYS_FP8, seed=77)
+    gl = GpuLayer(layer)
+    S_gpu = gl.scores()
+    idx = gl.topk(S_gpu)
+    q_scaled = (layer.q_lat.float() * 2.0 ** log2_scale).to(torch.bfloat16)
+    sm_scale = layer.sm_scale * 2.0 ** -log2_scale
+    out = torch.empty(gl.T, 96, 512, dtype=torch.bfloat16, device="cuda:0")
+    lse = torch.empty(gl.T, 96, dtype=torch.float32, device="cuda:0")
+    nws = dsa.dsa_sparse_mla_workspace_size(gl.batch)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda:0")
+    st = gl.status()
+    dsa.dsa_sparse_mla(gl.batch, q_scaled.to("cuda:0"), gl.g.latent_pages, layer.kv_scale,
+                       sm_scale, idx, dsa.TOPK, out, lse, ws if nws else None, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref_out, ref_lse = oracle.sparse_mla(batch_of(layer), q_scaled, layer.latent_pages,
+                                         layer.kv_scale, sm_scale, idx.cpu().numpy())
+    check_out(out, lse, ref_out, ref_lse, list(range(layer.total_q)))
