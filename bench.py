@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--config", default="c1_batched")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first N requests of the workload (profiling at a "
+                         "smaller scale with the same per-request shape); 0 = all")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bounded CPU-oracle sample for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -254,6 +257,8 @@ def run_ours(args, rank, world, local):
     dsa.load()
 
     lens, q_counts, fmt, seed = config_shape(args.config)
+    if args.requests > 0:
+        lens, q_counts = lens[:args.requests], q_counts[:args.requests]
     T = sum(q_counts)
     L = max(1, args.layers)
     dev = torch.device("cuda", local)

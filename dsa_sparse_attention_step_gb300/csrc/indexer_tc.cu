@@ -15,13 +15,17 @@
 // keys, not the queries, are balanced across SMs.  Per unit:
 //   D[128 keys x N] = K8[128 x 128] . Q8[N x 128]^T,  N = 32 heads x G tokens,
 // tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM, double
-// buffered).  Key pages arrive by TMA (128-byte swizzle) into a 6-stage ring,
-// the query group by TMA into a double buffer.  Eight epilogue warps read the
-// accumulator (thread = key), apply ReLU, the weighted head sum, the key scale
-// and the causal mask, and store fp32 scores.
+// buffered).  Key pages arrive by TMA (128-byte swizzle) into a 6-stage ring
+// (their 64 scale words by bulk copy beside them), the query group by TMA
+// into a double buffer.  The epilogue warps read the accumulator (thread =
+// key), apply ReLU, the weighted head sum, the key scale and the causal mask,
+// and store fp32 scores.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocation and the
-// MMA-issuing thread, warps 2-9 epilogue.  Every wait is bounded.
+// Roles (448 threads): warp 0 producer (the warp looks up pages, lane 0
+// issues the copies), warp 1 TMEM allocation and the MMA-issuing thread, then
+// for FP8 keys twelve epilogue warps (three per TMEM lane quarter, each taking
+// every third token of a query group); for MXFP4 keys four converter warps and
+// eight epilogue warps.  Every wait is bounded.
 #include <cstring>
 #include <mutex>
 
@@ -42,9 +46,10 @@ constexpr int kStages = 6;
 constexpr int kStageBytes = kTile * kIdxDim;   // 16384: E4M3 A operand of one unit
 constexpr int kQBufBytes = 8 * kIdxHeads * kIdxDim;  // 32768: up to 8 tokens x 32 heads
 constexpr int kMaxReq = 4096;
-constexpr int kEpiThreads = 256;               // 8 epilogue warps
 constexpr int kStgSlots = 4;                   // MXFP4: packed-key staging ring
 constexpr int kStgBytes = 2 * kPage * kIdxDim / 2;   // 8192: two pages of packed E2M1
+constexpr int kMetaSlots = kStages + 2;          // scale words of a unit: see the producer
+constexpr int kMetaBytes = 2 * kPage * 4;        // 512: the 64 scale words of two pages
 
 // Per-format layout of the kernel.  FP8 keys go straight from TMA to the MMA;
 // MXFP4 keys are staged packed and expanded to E4M3 by four converter warps,
@@ -55,14 +60,20 @@ struct IdxCfg {
     static constexpr bool kMx = (kFmt == DSA_KEYS_MXFP4);
     static constexpr int kConvWarps = kMx ? 4 : 0;
     static constexpr int kEpiWarp0 = 2 + kConvWarps;
-    static constexpr int kThreads = (kEpiWarp0 + 8) * 32;      // 320 or 448
+    // FP8: 12 epilogue warps, three per TMEM lane quarter, each taking every
+    // third token of a group; MXFP4: 8 warps (registers), every second token
+    static constexpr int kEpiWarps = kMx ? 8 : 12;
+    static constexpr int kEpiThreads = kEpiWarps * 32;
+    static constexpr int kTokSplit = kEpiWarps / 4;            // token stride
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 448 or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
     static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
     static constexpr int kOffReq = kOffW + 2 * 8 * kIdxHeads * 4;
     static constexpr int kOffStg = (kOffReq + (kMaxReq + 1) * 4 + 1023) / 1024 * 1024;
-    static constexpr int kOffBar = kOffStg + (kMx ? kStgSlots * kStgBytes : 0);
+    static constexpr int kOffMeta = kOffStg + (kMx ? kStgSlots * kStgBytes : 0);
+    static constexpr int kOffBar = kOffMeta + kMetaSlots * kMetaBytes;
     static constexpr int kSmemAlloc = kOffBar + 512 + 1024;
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -147,6 +158,19 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const BatchArgs& bt, int 
     } while (c.ngroup == 0 || c.ntile == 0);
 }
 
+// Packed pairs of fp32 (low word = first element) and their fused multiply-add
+// (one instruction for two lanes of the FMA pipe on this GPU).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo_f32x2(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f32x2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // E2M1 magnitude code -> E4M3 code of the same value (0, 0.5, 1, 1.5, 2, 3,
 // 4, 6), as byte lanes of two words for PRMT lookups.
 constexpr uint32_t kE2m1ToE4m3Lo = 0x3C383000u;  // codes 0..3
@@ -190,6 +214,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     float* sW = reinterpret_cast<float*>(sm + C::kOffW);     // [2][8][32]
     int* sReq = reinterpret_cast<int*>(sm + C::kOffReq);      // [B+1]
     uint8_t* sStg = sm + C::kOffStg;                          // MXFP4 staging ring
+    uint8_t* sMeta = sm + C::kOffMeta;                        // scale words per unit
     Bars* bars = reinterpret_cast<Bars*>(sm + C::kOffBar);
     __shared__ int s_warp_sum[kThreads / 32];
 
@@ -205,7 +230,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->tfull[i], 1);
-            mbar_init(&bars->tempty[i], kEpiThreads);
+            mbar_init(&bars->tempty[i], C::kEpiThreads);
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], 1);
         }
@@ -261,52 +286,99 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
 
     if (warp == 0) {
         // ---------------- producer: query groups and key pages ----------------
-        if (lane == 0 && n_units > 0) {
-            Cursor c;
-            cursor_seek(c, bt, sReq, G, u_begin);
-            int gcount = 0, pb = -1, pg = -1;
-            for (int i = 0; i < n_units; ++i) {
-                if (c.b != pb || c.g != pg) {
-                    const int x = gcount & 1;
-                    if (gcount >= 2 &&
-                        !mbar_wait(&bars->qempty[x], ((gcount >> 1) - 1) & 1, abort_flag))
-                        break;
-                    mbar_arrive_expect_tx(&bars->qfull[x], (uint32_t)N * kIdxDim);
-                    tma_load_2d(sQ + x * kQBufBytes, &tm_q, 0, (c.q0 + c.g * G) * kIdxHeads,
-                                &bars->qfull[x]);
-                    ++gcount;
-                    pb = c.b;
-                    pg = c.g;
-                }
-                int pages[2] = {-1, -1};
-                uint32_t bytes = 0;
-                for (int h = 0; h < 2; ++h) {
-                    const int s0 = c.tile * kTile + h * kPage;
-                    if (s0 < c.seq) {
-                        pages[h] = page_lookup(bt, c.b, s0 / kPage, p.status);
-                        if (pages[h] >= 0) bytes += kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim;
+        // The warp looks up the pages of 16 units at a time (lane l: unit
+        // l / 2, page l % 2), so the table reads overlap; lane 0 issues the
+        // copies.
+        bool ok = true;
+        int gcount = 0, pb = -1, pg = -1;
+        for (int i0 = 0; i0 < n_units && ok; i0 += 16) {
+            const int iu = i0 + (lane >> 1);
+            int upage = -1, ub = -1, ug = 0, uq0 = 0;
+            if (iu < n_units) {
+                Cursor c;
+                cursor_seek(c, bt, sReq, G, u_begin + iu);
+                const int s0 = c.tile * kTile + (lane & 1) * kPage;
+                if (s0 < c.seq) upage = page_lookup(bt, c.b, s0 / kPage, p.status);
+                ub = c.b;
+                ug = c.g;
+                uq0 = c.q0;
+            }
+            for (int k = 0; k < 16 && i0 + k < n_units; ++k) {
+                const int i = i0 + k;
+                const int pages[2] = {__shfl_sync(0xffffffffu, upage, 2 * k),
+                                      __shfl_sync(0xffffffffu, upage, 2 * k + 1)};
+                const int cb = __shfl_sync(0xffffffffu, ub, 2 * k);
+                const int cg = __shfl_sync(0xffffffffu, ug, 2 * k);
+                const int cq0 = __shfl_sync(0xffffffffu, uq0, 2 * k);
+                int go = 1;
+                if (lane == 0) {
+                    if (cb != pb || cg != pg) {
+                        const int x = gcount & 1;
+                        if (gcount >= 2 &&
+                            !mbar_wait(&bars->qempty[x], ((gcount >> 1) - 1) & 1, abort_flag))
+                            go = 0;
+                        if (go) {
+                            mbar_arrive_expect_tx(&bars->qfull[x], (uint32_t)N * kIdxDim);
+                            tma_load_2d(sQ + x * kQBufBytes, &tm_q, 0, (cq0 + cg * G) * kIdxHeads,
+                                        &bars->qfull[x]);
+                            ++gcount;
+                            pb = cb;
+                            pg = cg;
+                        }
+                    }
+                    uint32_t bytes = 0;
+                    for (int h = 0; h < 2; ++h)
+                        if (pages[h] >= 0)
+                            bytes += (kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim) + kPage * 4;
+                    // the 64 scale words of each page land in meta slot i % 8,
+                    // completing on the same barrier as the keys.  Slot reuse
+                    // is safe: unit i is issued after the MMA of unit i - 6,
+                    // which waited for the epilogue of unit i - 8.
+                    uint8_t* meta = sMeta + (i % kMetaSlots) * kMetaBytes;
+                    if (go && !kMx) {
+                        const int st = i % kStages, kq = i / kStages;
+                        if (kq >= 1 && !mbar_wait(&bars->empty[st], (kq - 1) & 1, abort_flag)) go = 0;
+                        if (go) {
+                            mbar_arrive_expect_tx(&bars->full[st], bytes);
+                            for (int h = 0; h < 2; ++h)
+                                if (pages[h] >= 0) {
+                                    tma_load_2d(sStage + st * kStageBytes + h * (kPage * kIdxDim),
+                                                &tm_keys, 0, pages[h] * (kFp8PageBytes / kIdxDim),
+                                                &bars->full[st]);
+                                    bulk_copy_g2s(meta + h * kPage * 4,
+                                                  p.pages + (int64_t)pages[h] * kFp8PageBytes +
+                                                      kPage * kIdxDim,
+                                                  (uint32_t)(kPage * 4), &bars->full[st]);
+                                }
+                        }
+                    } else if (go) {
+                        // packed E2M1 bytes of the two pages into a staging
+                        // slot; the wait for the MMA of unit i - 6 frees meta
+                        // slot i % 8 (as for FP8 keys)
+                        const int ss = i % kStgSlots, kq = i / kStgSlots;
+                        if (kq >= 1 && !mbar_wait(&bars->sempty[ss], (kq - 1) & 1, abort_flag)) go = 0;
+                        if (go && i >= kStages &&
+                            !mbar_wait(&bars->empty[i % kStages], ((i / kStages) - 1) & 1, abort_flag))
+                            go = 0;
+                        if (go) {
+                            mbar_arrive_expect_tx(&bars->sfull[ss], bytes);
+                            for (int h = 0; h < 2; ++h)
+                                if (pages[h] >= 0) {
+                                    bulk_copy_g2s(sStg + ss * kStgBytes + h * (kPage * kIdxDim / 2),
+                                                  p.pages + (int64_t)pages[h] * kMxPageBytes,
+                                                  (uint32_t)(kPage * kIdxDim / 2), &bars->sfull[ss]);
+                                    bulk_copy_g2s(meta + h * kPage * 4,
+                                                  p.pages + (int64_t)pages[h] * kMxPageBytes +
+                                                      kPage * kIdxDim / 2,
+                                                  (uint32_t)(kPage * 4), &bars->sfull[ss]);
+                                }
+                        }
                     }
                 }
-                if (!kMx) {
-                    const int st = i % kStages, k = i / kStages;
-                    if (k >= 1 && !mbar_wait(&bars->empty[st], (k - 1) & 1, abort_flag)) break;
-                    mbar_arrive_expect_tx(&bars->full[st], bytes);
-                    for (int h = 0; h < 2; ++h)
-                        if (pages[h] >= 0)
-                            tma_load_2d(sStage + st * kStageBytes + h * (kPage * kIdxDim), &tm_keys,
-                                        0, pages[h] * (kFp8PageBytes / kIdxDim), &bars->full[st]);
-                } else {
-                    // packed E2M1 bytes of the two pages into a staging slot
-                    const int ss = i % kStgSlots, k = i / kStgSlots;
-                    if (k >= 1 && !mbar_wait(&bars->sempty[ss], (k - 1) & 1, abort_flag)) break;
-                    mbar_arrive_expect_tx(&bars->sfull[ss], bytes);
-                    for (int h = 0; h < 2; ++h)
-                        if (pages[h] >= 0)
-                            bulk_copy_g2s(sStg + ss * kStgBytes + h * (kPage * kIdxDim / 2),
-                                          p.pages + (int64_t)pages[h] * kMxPageBytes,
-                                          (uint32_t)(kPage * kIdxDim / 2), &bars->sfull[ss]);
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
                 }
-                cursor_next(c, bt, G);
             }
         }
         __syncwarp();
@@ -381,9 +453,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         }
     } else {
         // ---------------- epilogue (thread = key) ----------------
-        const int etid = tid - 32 * C::kEpiWarp0;     // 0..255
+        const int etid = tid - 32 * C::kEpiWarp0;
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter..+31
-        const int half = (warp - C::kEpiWarp0) >> 2;  // token parity handled by this warp
+        const int half = (warp - C::kEpiWarp0) >> 2;  // first token of this warp (stride kTokSplit)
+        constexpr int kTS = C::kTokSplit;
         if (n_units > 0) {
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
@@ -393,12 +466,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
                 if (c.b != pb || c.g != pg) {
                     float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
-                    for (int e = etid; e < gr * kIdxHeads; e += kEpiThreads) {
+                    for (int e = etid; e < gr * kIdxHeads; e += C::kEpiThreads) {
                         const int64_t t = c.q0 + gtok0 + e / kIdxHeads;
                         const int h = e % kIdxHeads;
                         wdst[e] = __ldg(p.w + t * kIdxHeads + h) * __ldg(p.qscale + t * kIdxHeads + h);
                     }
-                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                    asm volatile("bar.sync 2, %0;" ::"n"(C::kEpiThreads) : "memory");
                     ++gcount;
                     pb = c.b;
                     pg = c.g;
@@ -406,69 +479,97 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 const float* wq = sW + ((gcount - 1) & 1) * (8 * kIdxHeads);
                 const int s = c.tile * kTile + quarter * 32 + lane;
                 const bool in_seq = s < c.seq;
-                float kscale = 0.f;                   // FP8: per-key scale
-                float bsc[4] = {0.f, 0.f, 0.f, 0.f};  // MXFP4: block scales 2^(e-127)
+                // page validity from the table (independent of the MMA wait)
                 bool page_ok = false;
                 if (in_seq) {
                     const int pg2 = __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + s / kPage);
-                    if (pg2 >= 0 && pg2 < bt.num_pages) {
-                        page_ok = true;
-                        if (!kMx) {
-                            kscale = __ldg(reinterpret_cast<const float*>(
-                                               p.pages + (int64_t)pg2 * kFp8PageBytes +
-                                               kPage * kIdxDim) + (s % kPage));
-                        } else {
-                            const uint32_t e4 = __ldg(reinterpret_cast<const uint32_t*>(
-                                p.pages + (int64_t)pg2 * kMxPageBytes + kPage * kIdxDim / 2) +
-                                (s % kPage));
-#pragma unroll
-                            for (int bb = 0; bb < 4; ++bb) {
-                                const int ev = (e4 >> (8 * bb)) & 0xFF;
-                                bsc[bb] = (ev == 0xFF) ? __int_as_float(0x7fffffff)
-                                                       : ldexpf(1.0f, ev - 127);
-                            }
-                        }
-                    }
+                    page_ok = pg2 >= 0 && pg2 < bt.num_pages;
                 }
                 const int acc = i & 1;
                 if (!mbar_wait(&bars->tfull[acc], (i >> 1) & 1, abort_flag)) break;
                 tc_fence_after();
-                for (int j = half; j < gr; j += 2) {
-                    uint32_t v[32];
-                    float x[32];
-                    if (!kMx) {
-                        tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v);
-                        tmem_wait_ld();
+                // the unit's scale words arrived with its keys (before tfull)
+                const uint32_t sw = reinterpret_cast<const uint32_t*>(
+                    sMeta + (i % kMetaSlots) * kMetaBytes)[quarter * 32 + lane];
+                float kscale = 0.f;                   // FP8: per-key scale
+                float bsc[4] = {0.f, 0.f, 0.f, 0.f};  // MXFP4: block scales 2^(e-127)
+                if (!kMx) {
+                    kscale = __uint_as_float(sw);
+                } else {
 #pragma unroll
-                        for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(v[h]);
-                    } else {
+                    for (int bb = 0; bb < 4; ++bb) {
+                        const int ev = (sw >> (8 * bb)) & 0xFF;
+                        bsc[bb] = (ev == 0xFF) ? __int_as_float(0x7fffffff) : ldexpf(1.0f, ev - 127);
+                    }
+                }
+                if (!kMx) {
+                    // the TMEM loads of two of this thread's tokens, then one wait
+                  for (int jp = 0; jp < 2; ++jp) {
+                    if (half + 2 * kTS * jp >= gr) break;
+                    uint32_t v[2][32];
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = half + 2 * kTS * jp + kTS * jj;
+                        if (j < gr) tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v[jj]);
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = half + 2 * kTS * jp + kTS * jj;
+                        if (j >= gr) break;
+                        const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
+                        // two independent packed (f32x2) partial sums
+                        uint64_t a01 = 0ull, a23 = 0ull;
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 ww = w4[h4];
+                            a01 = fma_f32x2(pack_f32x2(ww.x, ww.y),
+                                            pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 0]), 0.f),
+                                                       fmaxf(__uint_as_float(v[jj][4 * h4 + 1]), 0.f)),
+                                            a01);
+                            a23 = fma_f32x2(pack_f32x2(ww.z, ww.w),
+                                            pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 2]), 0.f),
+                                                       fmaxf(__uint_as_float(v[jj][4 * h4 + 3]), 0.f)),
+                                            a23);
+                        }
+                        const float sc = ((lo_f32x2(a01) + hi_f32x2(a01)) +
+                                          (lo_f32x2(a23) + hi_f32x2(a23))) * kscale;
+                        if (in_seq) {
+                            const int vis = c.seq - c.nb + gtok0 + j + 1;
+                            p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
+                                (s < vis && page_ok) ? sc : -INFINITY;
+                        }
+                    }
+                  }
+                } else {
+                    for (int j = half; j < gr; j += kTS) {
+                        float x[32];
 #pragma unroll
                         for (int h = 0; h < 32; ++h) x[h] = 0.f;
 #pragma unroll
                         for (int bb = 0; bb < 4; ++bb) {
+                            uint32_t v[32];
                             tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * 4 * N + bb * N + 32 * j), v);
                             tmem_wait_ld();
 #pragma unroll
                             for (int h = 0; h < 32; ++h) x[h] = fmaf(bsc[bb], __uint_as_float(v[h]), x[h]);
                         }
-                    }
-                    const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
-                    // four independent partial sums keep the FMA pipe busy
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                        const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
+                        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-                    for (int h4 = 0; h4 < 8; ++h4) {
-                        const float4 ww = w4[h4];
-                        s0 = fmaf(ww.x, fmaxf(x[4 * h4 + 0], 0.f), s0);
-                        s1 = fmaf(ww.y, fmaxf(x[4 * h4 + 1], 0.f), s1);
-                        s2 = fmaf(ww.z, fmaxf(x[4 * h4 + 2], 0.f), s2);
-                        s3 = fmaf(ww.w, fmaxf(x[4 * h4 + 3], 0.f), s3);
-                    }
-                    float sc = (s0 + s1) + (s2 + s3);
-                    if (!kMx) sc *= kscale;
-                    if (in_seq) {
-                        const int vis = c.seq - c.nb + gtok0 + j + 1;
-                        p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
-                            (s < vis && page_ok) ? sc : -INFINITY;
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 ww = w4[h4];
+                            s0 = fmaf(ww.x, fmaxf(x[4 * h4 + 0], 0.f), s0);
+                            s1 = fmaf(ww.y, fmaxf(x[4 * h4 + 1], 0.f), s1);
+                            s2 = fmaf(ww.z, fmaxf(x[4 * h4 + 2], 0.f), s2);
+                            s3 = fmaf(ww.w, fmaxf(x[4 * h4 + 3], 0.f), s3);
+                        }
+                        const float sc = (s0 + s1) + (s2 + s3);
+                        if (in_seq) {
+                            const int vis = c.seq - c.nb + gtok0 + j + 1;
+                            p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
+                                (s < vis && page_ok) ? sc : -INFINITY;
+                        }
                     }
                 }
                 tc_fence_before();

@@ -299,50 +299,72 @@ topk_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
     if (sampled_all >= (uint32_t)vis) {
         need_s = (uint32_t)K;  // every position sampled: the exact threshold bin
     } else {
-        const double f = (double)sampled_all / (double)vis;
-        need_s = (uint32_t)fmin((double)sampled_all, ceil(1.25 * K * f) + 16.0);
+        // ceil(1.25 K sampled / vis) + 16 in exact integer arithmetic (the
+        // FP64 units of this GPU are far too slow for per-thread use)
+        const uint64_t num = 5ull * (uint64_t)K * sampled_all;
+        const uint64_t den = 4ull * (uint64_t)vis;
+        const uint64_t want = (num + den - 1) / den + 16ull;
+        need_s = (want < (uint64_t)sampled_all) ? (uint32_t)want : sampled_all;
     }
     find_digit(S, th, kBins, need_s);
     const uint32_t key_lo = S.s_digit << 20;
 
     // ---- 2. candidates: every key in a bin >= b_lo -------------------------
-    sweep<kRes>(row, kRes ? S.keys : nullptr, lo, hi,
-                [&](const int (&i)[kVec], const uint4 (&kv)[kVec]) {
-        uint32_t mask = 0;  // bit 4u+e: element e of vector u is a candidate
+    // A float compare against the smallest float of bin b_lo (order keys are
+    // monotone in the float value); order keys are formed for the candidates
+    // only, and a thread's write loop visits only its vectors that hold one.
+    {
+        const float thr = (key_lo == 0u) ? -INFINITY
+                        : __uint_as_float((key_lo & 0x80000000u) ? (key_lo & 0x7FFFFFFFu) : ~key_lo);
+        for (int base0 = lo; base0 < hi; base0 += 4 * kVec * kThreads) {
+            float4 x[kVec];
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) {
-            const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+            for (int u = 0; u < kVec; ++u) {
+                const int i0 = base0 + u * 4 * kThreads + 4 * tid;
+                x[u] = (i0 < hi) ? __ldg(reinterpret_cast<const float4*>(row + i0))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            uint32_t mask = 0;  // bit 4u+e: element e of vector u is a candidate
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                mask |= (i[u] + e < hi && k4[e] >= key_lo) ? (1u << (4 * u + e)) : 0u;
-        }
-        const int n = __popc(mask);
-        int incl = n;
+            for (int u = 0; u < kVec; ++u) {
+                const int i0 = base0 + u * 4 * kThreads + 4 * tid;
+                const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o2);
-            if (lane >= o2) incl += v;
-        }
-        const int wsum = __shfl_sync(0xffffffffu, incl, 31);
-        if (wsum == 0) return;
-        int base = 0;
-        if (lane == 31) base = (int)atomicAdd(&S.s_count, (uint32_t)wsum);
-        base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+                for (int e = 0; e < 4; ++e)
+                    mask |= (i0 + e < hi && xv[e] >= thr) ? (1u << (4 * u + e)) : 0u;
+            }
+            const int n = __popc(mask);
+            int incl = n;
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) {
-            const uint32_t k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o2);
+                if (lane >= o2) incl += v;
+            }
+            const int wsum = __shfl_sync(0xffffffffu, incl, 31);
+            if (wsum == 0) continue;
+            int base = 0;
+            if (lane == 31) base = (int)atomicAdd(&S.s_count, (uint32_t)wsum);
+            base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+            if (mask == 0u) continue;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (mask & (1u << (4 * u + e))) {
-                    if (base < kCand) {
-                        S.cand_key[base] = k4[e];
-                        S.cand_pos[base] = i[u] + e;
+            for (int u = 0; u < kVec; ++u) {
+                const uint32_t mu = (mask >> (4 * u)) & 0xFu;
+                if (mu == 0u) continue;
+                const int i0 = base0 + u * 4 * kThreads + 4 * tid;
+                const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (mu & (1u << e)) {
+                        if (base < kCand) {
+                            S.cand_key[base] = order_key(xv[e]);
+                            S.cand_pos[base] = i0 + e;
+                        }
+                        ++base;
                     }
-                    ++base;
                 }
             }
         }
-    });
+    }
     __syncthreads();
     const uint32_t ncand_raw = S.s_count;
     S.xchg[0] = ncand_raw;
