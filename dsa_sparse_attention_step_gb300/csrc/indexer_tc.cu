@@ -14,8 +14,8 @@
 // A persistent grid splits the unit list into equal contiguous ranges, so the
 // keys, not the queries, are balanced across SMs.  Per unit:
 //   D[128 keys x N] = K8[128 x 128] . Q8[N x 128]^T,  N = 32 heads x G tokens,
-// tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM, double
-// buffered).  Key pages arrive by TMA (128-byte swizzle) into a 6-stage ring
+// tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM, two or
+// three buffers).  Key pages arrive by TMA (128-byte swizzle) into an 8-stage ring
 // (their 64 scale words by bulk copy beside them), the query group by TMA
 // into a double buffer.  The epilogue warps read the accumulator (thread =
 // key), apply ReLU, the weighted head sum, the key scale and the causal mask,
@@ -42,13 +42,12 @@ using namespace sm100;
 namespace {
 
 constexpr int kTile = 128;                     // keys per unit
-constexpr int kStages = 6;
+constexpr int kMaxStages = 8;                  // key-tile ring: 8 stages (FP8), 6 (MXFP4)
 constexpr int kStageBytes = kTile * kIdxDim;   // 16384: E4M3 A operand of one unit
 constexpr int kQBufBytes = 8 * kIdxHeads * kIdxDim;  // 32768: up to 8 tokens x 32 heads
 constexpr int kMaxReq = 4096;
 constexpr int kStgSlots = 4;                   // MXFP4: packed-key staging ring
 constexpr int kStgBytes = 2 * kPage * kIdxDim / 2;   // 8192: two pages of packed E2M1
-constexpr int kMetaSlots = kStages + 2;          // scale words of a unit: see the producer
 constexpr int kMetaBytes = 2 * kPage * 4;        // 512: the 64 scale words of two pages
 
 // Per-format layout of the kernel.  FP8 keys go straight from TMA to the MMA;
@@ -67,6 +66,9 @@ struct IdxCfg {
     static constexpr int kTokSplit = kEpiWarps / 4;            // token stride
     static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 448 or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
+    // enough key bytes in flight per SM to cover the memory latency at full load
+    static constexpr int kStages = kMx ? 6 : 8;
+    static constexpr int kMetaSlots = kStages + 3;             // scale words of a unit
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
     static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
@@ -79,10 +81,10 @@ struct IdxCfg {
 };
 
 struct Bars {
-    uint64_t full[kStages];   // TMA / converters -> MMA: key tile ready
-    uint64_t empty[kStages];  // MMA -> TMA / converters: stage free (commit)
-    uint64_t tfull[2];        // MMA -> epilogue: accumulator ready (commit)
-    uint64_t tempty[2];       // epilogue -> MMA: accumulator drained (256 arrivals)
+    uint64_t full[kMaxStages];   // TMA / converters -> MMA: key tile ready
+    uint64_t empty[kMaxStages];  // MMA -> TMA / converters: stage free (commit)
+    uint64_t tfull[3];        // MMA -> epilogue: accumulator ready (commit)
+    uint64_t tempty[3];       // epilogue -> MMA: accumulator drained (epilogue arrivals)
     uint64_t qfull[2];        // TMA -> MMA: query group landed
     uint64_t qempty[2];       // MMA -> TMA: query buffer free (commit)
     uint64_t sfull[kStgSlots];   // MXFP4: packed keys landed (bulk copy)
@@ -221,18 +223,24 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const BatchArgs& bt = p.bt;
     const int G = p.G, N = p.N;
+    // TMEM accumulators: columns per unit, and three buffers when they fit in
+    // the 512 columns (the MMA then runs two units ahead of the epilogue)
+    const int acc_cols = kMx ? 4 * N : N;
+    const int nacc = (3 * acc_cols <= 512) ? 3 : 2;
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&bars->full[i], kMx ? 128 : 1);
             mbar_init(&bars->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->tfull[i], 1);
-            mbar_init(&bars->tempty[i], C::kEpiThreads);
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], 1);
+        }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&bars->tfull[i], 1);
+            mbar_init(&bars->tempty[i], C::kEpiThreads);
         }
         for (int i = 0; i < kStgSlots; ++i) {
             mbar_init(&bars->sfull[i], 1);
@@ -286,30 +294,35 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
 
     if (warp == 0) {
         // ---------------- producer: query groups and key pages ----------------
-        // The warp looks up the pages of 16 units at a time (lane l: unit
-        // l / 2, page l % 2), so the table reads overlap; lane 0 issues the
+        // Every lane follows the unit cursor.  Page ids come from two windows
+        // of 32 consecutive table entries (lane l holds one), each loaded with
+        // one coalesced read one window ahead of its use; lane 0 issues the
         // copies.
         bool ok = true;
         int gcount = 0, pb = -1, pg = -1;
+        Cursor c;
+        if (n_units > 0) cursor_seek(c, bt, sReq, G, u_begin);
+        int wb = -1, wlp0 = 0, wcur = -1, wnext = -1;
+        auto lookup = [&](int lp) {
+            return (lp * kPage < c.seq) ? page_lookup(bt, c.b, lp, p.status) : -1;
+        };
         for (int i0 = 0; i0 < n_units && ok; i0 += 16) {
-            const int iu = i0 + (lane >> 1);
-            int upage = -1, ub = -1, ug = 0, uq0 = 0;
-            if (iu < n_units) {
-                Cursor c;
-                cursor_seek(c, bt, sReq, G, u_begin + iu);
-                const int s0 = c.tile * kTile + (lane & 1) * kPage;
-                if (s0 < c.seq) upage = page_lookup(bt, c.b, s0 / kPage, p.status);
-                ub = c.b;
-                ug = c.g;
-                uq0 = c.q0;
-            }
             for (int k = 0; k < 16 && i0 + k < n_units; ++k) {
                 const int i = i0 + k;
-                const int pages[2] = {__shfl_sync(0xffffffffu, upage, 2 * k),
-                                      __shfl_sync(0xffffffffu, upage, 2 * k + 1)};
-                const int cb = __shfl_sync(0xffffffffu, ub, 2 * k);
-                const int cg = __shfl_sync(0xffffffffu, ug, 2 * k);
-                const int cq0 = __shfl_sync(0xffffffffu, uq0, 2 * k);
+                const int lp = c.tile * 2;
+                if (c.b != wb || lp < wlp0 || lp >= wlp0 + 64) {
+                    wb = c.b;
+                    wlp0 = lp;
+                    wcur = lookup(lp + lane);
+                    wnext = lookup(lp + 32 + lane);
+                } else if (lp >= wlp0 + 32) {
+                    wlp0 += 32;
+                    wcur = wnext;
+                    wnext = lookup(wlp0 + 32 + lane);
+                }
+                const int pages[2] = {__shfl_sync(0xffffffffu, wcur, lp - wlp0),
+                                      __shfl_sync(0xffffffffu, wcur, lp - wlp0 + 1)};
+                const int cb = c.b, cg = c.g, cq0 = c.q0;
                 int go = 1;
                 if (lane == 0) {
                     if (cb != pb || cg != pg) {
@@ -330,13 +343,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     for (int h = 0; h < 2; ++h)
                         if (pages[h] >= 0)
                             bytes += (kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim) + kPage * 4;
-                    // the 64 scale words of each page land in meta slot i % 8,
-                    // completing on the same barrier as the keys.  Slot reuse
-                    // is safe: unit i is issued after the MMA of unit i - 6,
-                    // which waited for the epilogue of unit i - 8.
-                    uint8_t* meta = sMeta + (i % kMetaSlots) * kMetaBytes;
+                    // the 64 scale words of each page land in meta slot
+                    // i % (S + 3) (S = key stages), completing on the same
+                    // barrier as the keys.  Slot reuse is safe: unit i is
+                    // issued after the MMA of unit i - S, which waited for the
+                    // epilogue of unit i - S - 3 (or - 2).
+                    uint8_t* meta = sMeta + (i % C::kMetaSlots) * kMetaBytes;
                     if (go && !kMx) {
-                        const int st = i % kStages, kq = i / kStages;
+                        const int st = i % C::kStages, kq = i / C::kStages;
                         if (kq >= 1 && !mbar_wait(&bars->empty[st], (kq - 1) & 1, abort_flag)) go = 0;
                         if (go) {
                             mbar_arrive_expect_tx(&bars->full[st], bytes);
@@ -353,12 +367,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         }
                     } else if (go) {
                         // packed E2M1 bytes of the two pages into a staging
-                        // slot; the wait for the MMA of unit i - 6 frees meta
-                        // slot i % 8 (as for FP8 keys)
+                        // slot; the wait for the MMA of unit i - S frees meta
+                        // slot i % (S + 3) (as for FP8 keys)
                         const int ss = i % kStgSlots, kq = i / kStgSlots;
                         if (kq >= 1 && !mbar_wait(&bars->sempty[ss], (kq - 1) & 1, abort_flag)) go = 0;
-                        if (go && i >= kStages &&
-                            !mbar_wait(&bars->empty[i % kStages], ((i / kStages) - 1) & 1, abort_flag))
+                        if (go && i >= C::kStages &&
+                            !mbar_wait(&bars->empty[i % C::kStages], ((i / C::kStages) - 1) & 1, abort_flag))
                             go = 0;
                         if (go) {
                             mbar_arrive_expect_tx(&bars->sfull[ss], bytes);
@@ -379,6 +393,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     ok = false;
                     break;
                 }
+                cursor_next(c, bt, G);
             }
         }
         __syncwarp();
@@ -399,10 +414,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     pb = c.b;
                     pg = c.g;
                 }
-                const int st = i % kStages;
-                const int acc = i & 1;
-                if (ok) ok = mbar_wait(&bars->full[st], (i / kStages) & 1, abort_flag);
-                if (ok && i >= 2) ok = mbar_wait(&bars->tempty[acc], ((i >> 1) - 1) & 1, abort_flag);
+                const int st = i % C::kStages;
+                const int acc = i % nacc;
+                if (ok) ok = mbar_wait(&bars->full[st], (i / C::kStages) & 1, abort_flag);
+                if (ok && i >= nacc) ok = mbar_wait(&bars->tempty[acc], ((i / nacc) - 1) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t qa = sq + ((gcount - 1) & 1) * kQBufBytes;
@@ -412,9 +427,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                                   kSwizzle128B);
                     const uint64_t bd = smem_desc(qa + kk * 32, 16, 1024, kSwizzle128B);
                     if (kMx)  // one accumulator per 32-element block
-                        mma_f8f6f4(tmem + acc * 4 * N + kk * N, ad, bd, idesc, 0u);
+                        mma_f8f6f4(tmem + acc * acc_cols + kk * N, ad, bd, idesc, 0u);
                     else
-                        mma_f8f6f4(tmem + acc * N, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                        mma_f8f6f4(tmem + acc * acc_cols, ad, bd, idesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars->empty[st]);
                 mma_commit(&bars->tfull[acc]);
@@ -431,9 +446,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         // ---------------- MXFP4 converters: E2M1 -> E4M3 A-operand tiles ----------
         const int ctid = tid - 64;  // 0..127
         for (int i = 0; i < n_units; ++i) {
-            const int ss = i % kStgSlots, st = i % kStages;
+            const int ss = i % kStgSlots, st = i % C::kStages;
             if (!mbar_wait(&bars->sfull[ss], (i / kStgSlots) & 1, abort_flag)) break;
-            if (i >= kStages && !mbar_wait(&bars->empty[st], ((i / kStages) - 1) & 1, abort_flag))
+            if (i >= C::kStages && !mbar_wait(&bars->empty[st], ((i / C::kStages) - 1) & 1, abort_flag))
                 break;
             const uint8_t* src = sStg + ss * kStgBytes;
             uint8_t* dst = sStage + st * kStageBytes;
@@ -485,12 +500,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     const int pg2 = __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + s / kPage);
                     page_ok = pg2 >= 0 && pg2 < bt.num_pages;
                 }
-                const int acc = i & 1;
-                if (!mbar_wait(&bars->tfull[acc], (i >> 1) & 1, abort_flag)) break;
+                const int acc = i % nacc;
+                if (!mbar_wait(&bars->tfull[acc], (i / nacc) & 1, abort_flag)) break;
                 tc_fence_after();
                 // the unit's scale words arrived with its keys (before tfull)
                 const uint32_t sw = reinterpret_cast<const uint32_t*>(
-                    sMeta + (i % kMetaSlots) * kMetaBytes)[quarter * 32 + lane];
+                    sMeta + (i % C::kMetaSlots) * kMetaBytes)[quarter * 32 + lane];
                 float kscale = 0.f;                   // FP8: per-key scale
                 float bsc[4] = {0.f, 0.f, 0.f, 0.f};  // MXFP4: block scales 2^(e-127)
                 if (!kMx) {
@@ -510,7 +525,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
                         const int j = half + 2 * kTS * jp + kTS * jj;
-                        if (j < gr) tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * N + 32 * j), v[jj]);
+                        if (j < gr) tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * j), v[jj]);
                     }
                     tmem_wait_ld();
 #pragma unroll
@@ -549,7 +564,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
 #pragma unroll
                         for (int bb = 0; bb < 4; ++bb) {
                             uint32_t v[32];
-                            tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * 4 * N + bb * N + 32 * j), v);
+                            tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + bb * N + 32 * j), v);
                             tmem_wait_ld();
 #pragma unroll
                             for (int h = 0; h < 32; ++h) x[h] = fmaf(bsc[bb], __uint_as_float(v[h]), x[h]);
