@@ -154,7 +154,7 @@ struct MlaParams {
     float sm_scale;
     __nv_bfloat16* out;    // final output (splits == 1)
     float* lse;            // final lse (splits == 1), nullable
-    __half* part_o;        // [T, splits, 96, 512] normalised partial outputs (splits > 1)
+    __half* part_o;        // [T, splits, 512, 96] normalised partial outputs (splits > 1)
     float* part_lse;       // [T, splits, 96] partial lse, log2 domain (splits > 1)
     int32_t* status;
 };
@@ -508,16 +508,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 
     // ---------------- epilogue: O^T / l -> bf16 output or f16 partial ----------
     // warps 0-3 take latent-dim tiles 0-1, warps 4-7 tiles 2-3 (a warp reads
-    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads.  The
-    // [96][512] result is staged in the (now unused) query buffer and leaves
-    // with one bulk copy.
+    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads.  A
+    // final result ([96][512] bf16) is staged in the (now unused) query buffer
+    // and leaves with one bulk copy; a split partial is stored dim-major
+    // ([512][96] f16: a thread's 96 heads are 192 contiguous bytes) straight
+    // from registers, and the combine transposes it.
     {
         __syncthreads();  // the softmax warps have seen `done` and written 1/l
         tc_fence_after();
         const bool write = !*abort_flag && ok_tok;
+        const int lq = warp & 3;
+        const int mt0 = (warp < 4) ? 0 : 2;
         if (write) {
-            const int lq = warp & 3;
-            const int mt0 = (warp < 4) ? 0 : 2;
             for (int mt = mt0; mt < mt0 + 2; ++mt) {
                 const int d = 128 * mt + 32 * lq + lane;
                 uint32_t o[96];
@@ -528,38 +530,42 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 tmem_wait_ld();
                 // the per-head scales go to registers first: a shared load
                 // between the (possibly aliasing) stores would serialise them
+                if (p.splits == 1) {
+                    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sQ) + d;
 #pragma unroll
-                for (int hg = 0; hg < 3; ++hg) {
-                    float inv[32];
+                    for (int hg = 0; hg < 3; ++hg) {
+                        float inv[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 v4 = *reinterpret_cast<const float4*>(sF + 256 + 32 * hg + j);
-                        inv[j] = v4.x; inv[j + 1] = v4.y; inv[j + 2] = v4.z; inv[j + 3] = v4.w;
-                    }
-                    if (p.splits == 1) {
-                        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sQ) + d;
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4*>(sF + 256 + 32 * hg + j);
+                            inv[j] = v4.x; inv[j + 1] = v4.y; inv[j + 2] = v4.z; inv[j + 3] = v4.w;
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             st[(32 * hg + j) * kVDim] =
                                 __float2bfloat16_rn(__uint_as_float(o[32 * hg + j]) * inv[j]);
-                    } else {
-                        __half* st = reinterpret_cast<__half*>(sQ) + d;
+                    }
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        p.part_o + (((int64_t)t * p.splits + split) * kVDim + d) * kMlaHeads);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            st[(32 * hg + j) * kVDim] =
-                                __float2half_rn(__uint_as_float(o[32 * hg + j]) * inv[j]);
+                    for (int q = 0; q < 12; ++q) {  // heads 8q .. 8q+7
+                        const float4 ia = *reinterpret_cast<const float4*>(sF + 256 + 8 * q);
+                        const float4 ib = *reinterpret_cast<const float4*>(sF + 256 + 8 * q + 4);
+                        const float* ov = reinterpret_cast<const float*>(o + 8 * q);
+                        dst[q] = make_uint4(pack_half2(ov[0] * ia.x, ov[1] * ia.y),
+                                            pack_half2(ov[2] * ia.z, ov[3] * ia.w),
+                                            pack_half2(ov[4] * ib.x, ov[5] * ib.y),
+                                            pack_half2(ov[6] * ib.z, ov[7] * ib.w));
                     }
                 }
             }
-            fence_proxy_async_smem();  // the bulk copy reads the staged result
+            if (p.splits == 1) fence_proxy_async_smem();  // the bulk copy reads the staged result
         }
-        __syncthreads();
-        if (write && tid == 0) {
-            void* dst = (p.splits == 1)
-                            ? static_cast<void*>(p.out + (int64_t)t * kMlaHeads * kVDim)
-                            : static_cast<void*>(p.part_o + ((int64_t)t * p.splits + split) *
-                                                                 kMlaHeads * kVDim);
-            bulk_store_s2g(dst, sQ, (uint32_t)kOutBytes);
+        if (p.splits == 1) {
+            __syncthreads();
+            if (write && tid == 0)
+                bulk_store_s2g(p.out + (int64_t)t * kMlaHeads * kVDim, sQ, (uint32_t)kOutBytes);
         }
     }
 
@@ -569,55 +575,73 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Merge the split partials of 8 heads of one token: out = kv_scale *
-// sum_s 2^(lse_s - L) o_s with L = log2 sum_s 2^lse_s, in a fixed order over
-// the splits.  Thread = (head, 16 consecutive latent dims).
-constexpr int kCombineHeads = 8;
-__global__ void __launch_bounds__(256)
+// Merge the split partials of one token over 32 latent dims: out = kv_scale *
+// sum_s 2^(lse_s - L) o_s with L = log2 sum_s 2^lse_s per head, in a fixed
+// order over the splits.  The partials are dim-major ([512][96] f16 per
+// split); thread = (latent dim, 8 heads): one 16-byte vector per split, all
+// of them in flight at once.
+constexpr int kCombineDims = 32;
+constexpr int kMaxSplits = 16;
+constexpr int kCombineThreads = kCombineDims * (kMlaHeads / 8);  // 384
+__global__ void __launch_bounds__(kCombineThreads)
 sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __restrict__ part_lse,
                           int splits, float kv_scale, __nv_bfloat16* __restrict__ out,
                           float* __restrict__ lse) {
-    constexpr int kGroupsPerToken = kMlaHeads / kCombineHeads;  // 12
+    constexpr int kBlocksPerToken = kVDim / kCombineDims;  // 16
+    __shared__ float s_w[kMaxSplits][kMlaHeads];
+    __shared__ float s_inv[kMlaHeads];
     grid_dependency_wait();  // the partials come from the previous kernel
-    const int t = blockIdx.x / kGroupsPerToken;
-    const int h = (blockIdx.x % kGroupsPerToken) * kCombineHeads + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int d0 = lane * 16;
-    // split weights: lane s holds split s (splits <= 32)
-    const float ls = (lane < splits) ? part_lse[((int64_t)t * splits + lane) * kMlaHeads + h]
-                                     : -INFINITY;
-    const float M = warp_max(ls);
-    const float wgt = (M == -INFINITY || lane >= splits) ? 0.f : exp2f(ls - M);
-    const float tot = warp_sum(wgt);
-    if (lane == 0 && lse)
-        lse[(int64_t)t * kMlaHeads + h] =
-            (tot > 0.f) ? (M + log2f(tot)) * 0.6931471805599453f : -INFINITY;
-    float acc[16];
+    const int t = blockIdx.x / kBlocksPerToken;
+    const int dblk = blockIdx.x % kBlocksPerToken;
+    const int tid = threadIdx.x;
+    const int d = dblk * kCombineDims + (tid & (kCombineDims - 1));
+    const int h0 = 8 * (tid / kCombineDims);  // 0, 8, ..., 88
+    uint4 v[kMaxSplits];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float ws = __shfl_sync(0xffffffffu, wgt, s);
-        const uint4* src = reinterpret_cast<const uint4*>(
-            part_o + (((int64_t)t * splits + s) * kMlaHeads + h) * kVDim + d0);
-        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    for (int s = 0; s < kMaxSplits; ++s)
+        v[s] = (s < splits) ? __ldg(reinterpret_cast<const uint4*>(
+                                  part_o + (((int64_t)t * splits + s) * kVDim + d) * kMlaHeads + h0))
+                            : make_uint4(0u, 0u, 0u, 0u);
+    if (tid < kMlaHeads) {
+        const int h = tid;
+        float ls[kMaxSplits];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
-            acc[2 * j] += ws * f.x;
-            acc[2 * j + 1] += ws * f.y;
+        for (int s = 0; s < kMaxSplits; ++s)
+            ls[s] = (s < splits) ? part_lse[((int64_t)t * splits + s) * kMlaHeads + h] : -INFINITY;
+        float M = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ls[s]);
+        float tot = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) {
+            if (s >= splits) break;
+            const float wgt = (M == -INFINITY) ? 0.f : exp2f(ls[s] - M);
+            s_w[s][h] = wgt;
+            tot += wgt;
+        }
+        s_inv[h] = (tot > 0.f) ? kv_scale / tot : 0.f;
+        if (dblk == 0 && lse)
+            lse[(int64_t)t * kMlaHeads + h] =
+                (tot > 0.f) ? (M + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+        if (s >= splits) break;
+        const uint32_t wv[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[k]));
+            acc[2 * k] = fmaf(s_w[s][h0 + 2 * k], f.x, acc[2 * k]);
+            acc[2 * k + 1] = fmaf(s_w[s][h0 + 2 * k + 1], f.y, acc[2 * k + 1]);
         }
     }
-    const float inv = (tot > 0.f) ? kv_scale / tot : 0.f;
-    uint32_t ob[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
-        ob[j] = *reinterpret_cast<uint32_t*>(&b2);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)t * kMlaHeads + h) * kVDim + d0);
-    dst[0] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-    dst[1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+    for (int j = 0; j < 8; ++j)
+        out[((int64_t)t * kMlaHeads + h0 + j) * kVDim + d] = __float2bfloat16_rn(acc[j] * s_inv[h0 + j]);
 }
 
 }  // namespace
@@ -627,7 +651,7 @@ sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __rest
 // request's result is bit-identical across batches within one step.
 int sparse_mla_splits(int total_q, int K) {
     int splits;
-    if (total_q <= 9) splits = 16;
+    if (total_q <= 9) splits = kMaxSplits;
     else if (total_q <= 19) splits = 8;
     else if (total_q <= 38) splits = 4;
     else if (total_q <= 76) splits = 2;
@@ -636,7 +660,7 @@ int sparse_mla_splits(int total_q, int K) {
     return splits;
 }
 
-// Workspace (split batches only): the f16 partial outputs [T, splits, 96, 512]
+// Workspace (split batches only): the f16 partial outputs [T, splits, 512, 96]
 // and their lse [T, splits, 96].
 struct MlaWs {
     size_t part_o, part_lse, total;
@@ -688,8 +712,8 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     e = launch_kernel(sparse_mla_tc_kernel, dim3(bt.total_q * p.splits), dim3(kThreads),
                       (size_t)kSmemAlloc, stream, pdl, 1, p);
     if (e != cudaSuccess || p.splits == 1) return e;
-    return launch_kernel(sparse_mla_combine_kernel, dim3(bt.total_q * (kMlaHeads / kCombineHeads)),
-                         dim3(256), 0, stream, true, 1, (const __half*)p.part_o,
+    return launch_kernel(sparse_mla_combine_kernel, dim3(bt.total_q * (kVDim / kCombineDims)),
+                         dim3(kCombineThreads), 0, stream, true, 1, (const __half*)p.part_o,
                          (const float*)p.part_lse, p.splits, kv_scale, p.out, lse);
 }
 
