@@ -256,6 +256,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         tmem_alloc(&bars->tmem_base, 512);
         tmem_relinquish();
     }
+    // Everything below reads the caller's inputs: wait for the previous grid
+    // of the stream (the launch may overlap its tail; the setup above does
+    // not touch global memory).
+    grid_dependency_wait();
     // ---- unit table: exclusive prefix of per-request unit counts ----
     int carry = 0;
     for (int b0 = 0; b0 < bt.num_requests; b0 += kThreads) {
@@ -660,8 +664,10 @@ cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscal
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    indexer_tc_kernel<kFmt><<<sms, C::kThreads, C::kSmemAlloc, stream>>>(tm_keys, tm_q, p);
-    return cudaGetLastError();
+    // programmatic dependent launch is safe after any predecessor: the kernel
+    // reads no global memory before its grid-dependency wait
+    return launch_kernel(indexer_tc_kernel<kFmt>, dim3(sms), dim3(C::kThreads),
+                         (size_t)C::kSmemAlloc, stream, true, 1, tm_keys, tm_q, p);
 }
 
 }  // namespace

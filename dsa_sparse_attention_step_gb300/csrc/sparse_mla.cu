@@ -590,6 +590,7 @@ sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __rest
     constexpr int kBlocksPerToken = kVDim / kCombineDims;  // 16
     __shared__ float s_w[kMaxSplits][kMlaHeads];
     __shared__ float s_inv[kMlaHeads];
+    grid_dependents_launch();  // the next step's first kernel may start its setup
     grid_dependency_wait();  // the partials come from the previous kernel
     const int t = blockIdx.x / kBlocksPerToken;
     const int dblk = blockIdx.x % kBlocksPerToken;

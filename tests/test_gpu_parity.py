@@ -1,8 +1,8 @@
 """GPU parity of every C-ABI entry point against the CPU oracle, on seeded
 inputs that span several tiles and ragged tails, plus the edge cases: a
 single token, page and tile boundaries, contexts at and around 2048,
-multi-token causal rows, MXFP4 keys, page placement, batch invariance,
-determinism and device-side range checks."""
+multi-token causal rows, query groups of up to 9 tokens, MXFP4 keys, page
+placement, batch invariance, determinism and device-side range checks."""
 import zlib
 
 import numpy as np
@@ -25,6 +25,9 @@ CASES = {
     "multi_token": ([5000, 2300, 40], [5, 3, 2], di.KEYS_FP8),
     "ragged_batch": ([9000, 3001, 130, 7777], [1, 2, 1, 4], di.KEYS_FP8),
     "mxfp4": ([2047, 6000, 300], [1, 3, 1], di.KEYS_MXFP4),
+    # query groups of 6, 7 and 8 tokens (two TMEM accumulators, N >= 192) and
+    # a request split into a group of 8 and a group of 1
+    "wide_groups": ([3000, 2600, 1200, 5000], [6, 7, 8, 9], di.KEYS_FP8),
 }
 
 
