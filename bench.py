@@ -277,8 +277,17 @@ def run_ours(args, rank, world, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    # prefill-append: a step first writes the new tokens' keys and latents into
+    # the paged caches, then runs the step over them
+    append = args.config == "c4_prefill_append"
+    payloads = [di.append_payload(lay, seed + 31 * l) for l, lay in enumerate(layers)] if append else None
+
     def step(i, s=None):
         lay, b = layers[i % L], batches[i % L]
+        if append:
+            keys, lat = payloads[i % L]
+            dsa.dsa_append_cache(b, keys, lat, lay.kv_scale, lay.index_pages, lay.latent_pages, fmt,
+                                 status, stream=s)
         dsa.dsa_decode(b, lay.q8, lay.qscale, lay.w, lay.index_pages, fmt, lay.q_lat,
                        lay.latent_pages, lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx,
                        ws, status, stream=s)
@@ -389,24 +398,45 @@ def run_ours(args, rank, world, local):
               "sparse_mla": wl.mla_bytes(lens, q_counts)}
     dominant = max(kern, key=kern.get)
     hbm, bf16, src = peaks()
-    achieved = kbytes[dominant] / kern[dominant] / 1e9
-    traffic = recorded_traffic(dominant, args.config)
-    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
-                "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                "peak_source": src + " (burst copy)",
-                "algorithmic_bytes_per_launch": kbytes[dominant],
-                "avg_launch_us": kern[dominant] * 1e6,
-                "kernels_us": {k: v * 1e6 for k, v in kern.items()}}
+    if args.config == "c4_prefill_append":
+        # the prefill-append indexer is a dense causal FP8 GEMM: its roofline is
+        # the FP8 tensor peak (the measured bf16 GEMM rate x the nominal 2x of
+        # FP8 over bf16), for the indexer kernel alone
+        dominant = "indexer"
+        flops = wl.indexer_flops(lens, q_counts)
+        fp8_peak = 2.0 * bf16
+        achieved = flops / kern["indexer"] / 1e12
+        roofline = {"bound": "tensor", "kernel": "indexer", "achieved": achieved,
+                    "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                    "traffic": recorded_traffic("indexer", args.config),
+                    "peak_source": src + " (bf16 GEMM burst x 2 for FP8)",
+                    "algorithmic_flops_per_launch": flops,
+                    "avg_launch_us": kern["indexer"] * 1e6,
+                    "kernels_us": {k: v * 1e6 for k, v in kern.items()}}
+    else:
+        achieved = kbytes[dominant] / kern[dominant] / 1e9
+        traffic = recorded_traffic(dominant, args.config)
+        roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
+                    "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                    "peak_source": src + " (burst copy)",
+                    "algorithmic_bytes_per_launch": kbytes[dominant],
+                    "avg_launch_us": kern[dominant] * 1e6,
+                    "kernels_us": {k: v * 1e6 for k, v in kern.items()}}
 
     # ---- end to end through the public API with host buffers --------------
     e2e = None
     if rank == 0:
         pin = lambda t: t.cpu().pin_memory()
         hq = [(pin(l.q8), pin(l.qscale), pin(l.w), pin(l.q_lat)) for l in layers]
+        if append:  # the new tokens' keys and latents come from the host too
+            hq = [h + (pin(pl[0]), pin(pl[1])) for h, pl in zip(hq, payloads)]
         hmeta = [(pin(l.q_offsets), pin(l.seq_lens), pin(l.block_table)) for l in layers]
         two = [layers[0], layers[0]]  # two device slots, alternated step by step
         dq = [(torch.empty_like(l.q8), torch.empty_like(l.qscale), torch.empty_like(l.w),
                torch.empty_like(l.q_lat)) for l in two]
+        if append:
+            dq = [d + (torch.empty_like(payloads[0][0]), torch.empty_like(payloads[0][1]))
+                  for d in dq]
         dmeta = [(torch.empty_like(l.q_offsets), torch.empty_like(l.seq_lens),
                   torch.empty_like(l.block_table)) for l in two]
         dbatch = [dsa.Batch(m[0], m[1], m[2], layers[0].num_pages, lens, q_counts)
@@ -422,7 +452,10 @@ def run_ours(args, rank, world, local):
             lay = layers[j]
             for d, h in zip(dq[slot] + dmeta[slot], hq[j] + hmeta[j]):
                 d.copy_(h, non_blocking=True)
-            q8, qs, w, ql = dq[slot]
+            q8, qs, w, ql = dq[slot][:4]
+            if append:
+                dsa.dsa_append_cache(dbatch[slot], dq[slot][4], dq[slot][5], lay.kv_scale,
+                                     lay.index_pages, lay.latent_pages, fmt, status, stream=stream)
             # the block table copied in belongs to layer j's pools
             dsa.dsa_decode(dbatch[slot], q8, qs, w, lay.index_pages, fmt, ql, lay.latent_pages,
                            lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx, ws, status,
@@ -445,8 +478,9 @@ def run_ours(args, rank, world, local):
         te = a.elapsed_time(b) / 1000.0
         e2e = {"value": T * n_e2e / te, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "note": "per step: pinned H2D of queries and metadata, dsa_decode, D2H of "
-                       "output and indices; caches resident"}
+               "note": "per step: pinned H2D of queries and metadata" +
+                       (" and the new tokens' keys and latents, dsa_append_cache" if append else "") +
+                       ", dsa_decode, D2H of output and indices; caches resident"}
 
     if rank == 0:
         step_b = wl.step_bytes(lens, q_counts, fmt)
@@ -461,6 +495,8 @@ def run_ours(args, rank, world, local):
                            "layers_rotated": L, "cache_bytes_rotated": cache_bytes,
                            "l2": "inputs larger than L2: %d layer copies, %.2f GB of caches "
                                  "rotated" % (L, cache_bytes / 1e9),
+                           "step": "dsa_append_cache + dsa_decode" if args.config == "c4_prefill_append"
+                                   else "dsa_decode",
                            "parallelism": "replicas" if world > 1 else "single"},
                 "step_hbm_gbs": step_b / (elapsed / args.steps) / 1e9,
                 "step_bytes": step_b,

@@ -522,7 +522,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     }
                 }
                 if (!kMx) {
-                    // the TMEM loads of two of this thread's tokens, then one wait
+                    // the TMEM loads of two of this thread's tokens (half + 3k),
+                    // then one wait
                   for (int jp = 0; jp < 2; ++jp) {
                     if (half + 2 * kTS * jp >= gr) break;
                     uint32_t v[2][32];
@@ -537,22 +538,26 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         const int j = half + 2 * kTS * jp + kTS * jj;
                         if (j >= gr) break;
                         const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
-                        // two independent packed (f32x2) partial sums
-                        uint64_t a01 = 0ull, a23 = 0ull;
+                        // four independent packed (f32x2) partial sums
+                        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                         for (int h4 = 0; h4 < 8; ++h4) {
                             const float4 ww = w4[h4];
-                            a01 = fma_f32x2(pack_f32x2(ww.x, ww.y),
-                                            pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 0]), 0.f),
-                                                       fmaxf(__uint_as_float(v[jj][4 * h4 + 1]), 0.f)),
-                                            a01);
-                            a23 = fma_f32x2(pack_f32x2(ww.z, ww.w),
-                                            pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 2]), 0.f),
-                                                       fmaxf(__uint_as_float(v[jj][4 * h4 + 3]), 0.f)),
-                                            a23);
+                            acc2[(2 * h4) & 3] = fma_f32x2(
+                                pack_f32x2(ww.x, ww.y),
+                                pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 0]), 0.f),
+                                           fmaxf(__uint_as_float(v[jj][4 * h4 + 1]), 0.f)),
+                                acc2[(2 * h4) & 3]);
+                            acc2[(2 * h4 + 1) & 3] = fma_f32x2(
+                                pack_f32x2(ww.z, ww.w),
+                                pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 2]), 0.f),
+                                           fmaxf(__uint_as_float(v[jj][4 * h4 + 3]), 0.f)),
+                                acc2[(2 * h4 + 1) & 3]);
                         }
-                        const float sc = ((lo_f32x2(a01) + hi_f32x2(a01)) +
-                                          (lo_f32x2(a23) + hi_f32x2(a23))) * kscale;
+                        const float sc = (((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
+                                           (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
+                                          ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
+                                           (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
                         if (in_seq) {
                             const int vis = c.seq - c.nb + gtok0 + j + 1;
                             p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
