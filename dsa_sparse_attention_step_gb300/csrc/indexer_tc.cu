@@ -72,7 +72,7 @@ struct IdxCfg {
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
     static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
-    static constexpr int kOffReq = kOffW + 2 * 8 * kIdxHeads * 4;
+    static constexpr int kOffReq = kOffW + 3 * 8 * kIdxHeads * 4;   // w x q_scale: [3][8][32]
     static constexpr int kOffStg = (kOffReq + (kMaxReq + 1) * 4 + 1023) / 1024 * 1024;
     static constexpr int kOffMeta = kOffStg + (kMx ? kStgSlots * kStgBytes : 0);
     static constexpr int kOffBar = kOffMeta + kMetaSlots * kMetaBytes;
@@ -213,7 +213,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                              ~static_cast<uintptr_t>(1023));
     uint8_t* sStage = sm + C::kOffStage;
     uint8_t* sQ = sm + C::kOffQ;
-    float* sW = reinterpret_cast<float*>(sm + C::kOffW);     // [2][8][32]
+    float* sW = reinterpret_cast<float*>(sm + C::kOffW);     // [3][8][32]
     int* sReq = reinterpret_cast<int*>(sm + C::kOffReq);      // [B+1]
     uint8_t* sStg = sm + C::kOffStg;                          // MXFP4 staging ring
     uint8_t* sMeta = sm + C::kOffMeta;                        // scale words per unit
@@ -240,7 +240,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         }
         for (int i = 0; i < 3; ++i) {
             mbar_init(&bars->tfull[i], 1);
-            mbar_init(&bars->tempty[i], C::kEpiThreads);
+            // FP8: the min(G, 3) warp groups that take items of a unit arrive
+            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : 128 * min(G, 3));
         }
         for (int i = 0; i < kStgSlots; ++i) {
             mbar_init(&bars->sfull[i], 1);
@@ -474,7 +475,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         // ---------------- epilogue (thread = key) ----------------
         const int etid = tid - 32 * C::kEpiWarp0;
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter..+31
-        const int half = (warp - C::kEpiWarp0) >> 2;  // first token of this warp (stride kTokSplit)
+        const int half = (warp - C::kEpiWarp0) >> 2;  // warp group (FP8: 0..2, MXFP4: token parity)
         constexpr int kTS = C::kTokSplit;
         if (n_units > 0) {
             Cursor c;
@@ -483,19 +484,42 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             for (int i = 0; i < n_units; ++i) {
                 const int gtok0 = c.g * G;                    // first token of the group
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
+                // FP8: the (unit, token) items k = i * G + j go round-robin to
+                // the three warp groups (group k % 3), so with one or two
+                // tokens per unit different groups drain different
+                // accumulators at the same time.  j0 = this group's first token.
+                const int j0 = kMx ? half : (half - (i * G) % 3 + 3) % 3;
+                if (!kMx && j0 >= G) {  // no item of this unit (only when G < 3)
+                    cursor_next(c, bt, G);
+                    continue;
+                }
                 if (c.b != pb || c.g != pg) {
-                    float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
-                    for (int e = etid; e < gr * kIdxHeads; e += C::kEpiThreads) {
-                        const int64_t t = c.q0 + gtok0 + e / kIdxHeads;
-                        const int h = e % kIdxHeads;
-                        wdst[e] = __ldg(p.w + t * kIdxHeads + h) * __ldg(p.qscale + t * kIdxHeads + h);
+                    if (kMx) {
+                        float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
+                        for (int e = etid; e < gr * kIdxHeads; e += C::kEpiThreads) {
+                            const int64_t t = c.q0 + gtok0 + e / kIdxHeads;
+                            const int h = e % kIdxHeads;
+                            wdst[e] = __ldg(p.w + t * kIdxHeads + h) * __ldg(p.qscale + t * kIdxHeads + h);
+                        }
+                        asm volatile("bar.sync 2, %0;" ::"n"(C::kEpiThreads) : "memory");
+                    } else {
+                        // each warp group keeps its own copy (barrier 3 + group
+                        // over its 128 threads, which follow the same units)
+                        float* wdst = sW + half * (8 * kIdxHeads);
+                        asm volatile("bar.sync %0, 128;" ::"r"(3 + half) : "memory");
+                        for (int e = etid - 128 * half; e < gr * kIdxHeads; e += 128) {
+                            const int64_t t = c.q0 + gtok0 + e / kIdxHeads;
+                            const int h = e % kIdxHeads;
+                            wdst[e] = __ldg(p.w + t * kIdxHeads + h) * __ldg(p.qscale + t * kIdxHeads + h);
+                        }
+                        asm volatile("bar.sync %0, 128;" ::"r"(3 + half) : "memory");
                     }
-                    asm volatile("bar.sync 2, %0;" ::"n"(C::kEpiThreads) : "memory");
                     ++gcount;
                     pb = c.b;
                     pg = c.g;
                 }
-                const float* wq = sW + ((gcount - 1) & 1) * (8 * kIdxHeads);
+                const float* wq = kMx ? sW + ((gcount - 1) & 1) * (8 * kIdxHeads)
+                                      : sW + half * (8 * kIdxHeads);
                 const int s = c.tile * kTile + quarter * 32 + lane;
                 const bool in_seq = s < c.seq;
                 // page validity from the table (independent of the MMA wait)
@@ -525,17 +549,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     // the TMEM loads of two of this thread's tokens (half + 3k),
                     // then one wait
                   for (int jp = 0; jp < 2; ++jp) {
-                    if (half + 2 * kTS * jp >= gr) break;
+                    if (j0 + 2 * kTS * jp >= gr) break;
                     uint32_t v[2][32];
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
-                        const int j = half + 2 * kTS * jp + kTS * jj;
+                        const int j = j0 + 2 * kTS * jp + kTS * jj;
                         if (j < gr) tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * j), v[jj]);
                     }
                     tmem_wait_ld();
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
-                        const int j = half + 2 * kTS * jp + kTS * jj;
+                        const int j = j0 + 2 * kTS * jp + kTS * jj;
                         if (j >= gr) break;
                         const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
                         // four independent packed (f32x2) partial sums
