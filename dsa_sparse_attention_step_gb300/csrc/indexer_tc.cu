@@ -21,11 +21,15 @@
 // key), apply ReLU, the weighted head sum, the key scale and the causal mask,
 // and store fp32 scores.
 //
-// Roles (448 threads): warp 0 producer (the warp looks up pages, lane 0
-// issues the copies), warp 1 TMEM allocation and the MMA-issuing thread, then
-// for FP8 keys twelve epilogue warps (three per TMEM lane quarter, each taking
-// every third token of a query group); for MXFP4 keys four converter warps and
-// eight epilogue warps.  Every wait is bounded.
+// Roles: producer warps (each looks up pages and one lane issues the copies),
+// then MMA warps (the first allocates TMEM; lane 0 issues MMAs), then for FP8
+// keys twelve epilogue warps (three per TMEM lane quarter, each taking every
+// third token of a query group) -- 512 threads; for MXFP4 keys four converter
+// warps and eight epilogue warps -- 448 threads.  With FP8 keys there are two
+// producer and two MMA warps, each pair taking alternate units: one thread
+// spends about a thousand cycles of instruction latency on a unit's copies
+// (or on its waits, MMAs and commits), more than the unit's share of the
+// memory bandwidth allows.  Every wait is bounded.
 #include <cstring>
 #include <mutex>
 
@@ -54,17 +58,24 @@ constexpr int kMetaBytes = 2 * kPage * 4;        // 512: the 64 scale words of t
 // MXFP4 keys are staged packed and expanded to E4M3 by four converter warps,
 // and each 32-element block gets its own accumulator (its E8M0 scale is
 // applied in the epilogue), which limits a query group to 2 tokens.
-template <int kFmt>
+// kDual (FP8 keys, query groups of one or two tokens, where the epilogue
+// has time to spare): two producer and two MMA warps taking alternate units.
+template <int kFmt, bool kDual>
 struct IdxCfg {
     static constexpr bool kMx = (kFmt == DSA_KEYS_MXFP4);
+    static_assert(!(kMx && kDual), "MXFP4 keys use one producer and one MMA warp");
+    static constexpr int kProdWarps = kDual ? 2 : 1;
+    static constexpr int kMmaWarp = kProdWarps;    // allocates TMEM
+    static constexpr int kMmaWarps = kDual ? 2 : 1;  // MMA-issuing threads (alternate units)
+    static constexpr int kConvWarp0 = kMmaWarp + kMmaWarps;
     static constexpr int kConvWarps = kMx ? 4 : 0;
-    static constexpr int kEpiWarp0 = 2 + kConvWarps;
+    static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
     // FP8: 12 epilogue warps, three per TMEM lane quarter, each taking every
     // third token of a group; MXFP4: 8 warps (registers), every second token
     static constexpr int kEpiWarps = kMx ? 8 : 12;
     static constexpr int kEpiThreads = kEpiWarps * 32;
     static constexpr int kTokSplit = kEpiWarps / 4;            // token stride
-    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 448 or 448
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 512 (kDual) or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
     // enough key bytes in flight per SM to cover the memory latency at full load
     static constexpr int kStages = kMx ? 6 : 8;
@@ -200,11 +211,11 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w) {
     return r;
 }
 
-template <int kFmt>
-__global__ void __launch_bounds__(IdxCfg<kFmt>::kThreads, 1)
+template <int kFmt, bool kDual>
+__global__ void __launch_bounds__(IdxCfg<kFmt, kDual>::kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                   const __grid_constant__ CUtensorMap tm_q, const IdxParams p) {
-    using C = IdxCfg<kFmt>;
+    using C = IdxCfg<kFmt, kDual>;
     constexpr bool kMx = C::kMx;
     constexpr int kThreads = C::kThreads;
     grid_dependents_launch();  // the top-k may start its preamble
@@ -236,7 +247,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->qfull[i], 1);
-            mbar_init(&bars->qempty[i], 1);
+            mbar_init(&bars->qempty[i], C::kMmaWarps);  // one commit per MMA thread
         }
         for (int i = 0; i < 3; ++i) {
             mbar_init(&bars->tfull[i], 1);
@@ -247,13 +258,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             mbar_init(&bars->sfull[i], 1);
             mbar_init(&bars->sempty[i], 128);
         }
-        mbar_init(&bars->done, 1);
+        mbar_init(&bars->done, C::kMmaWarps);
         bars->abort_flag = 0;
         fence_mbar_init();
         if (!kMx) tma_prefetch_desc(&tm_keys);
         tma_prefetch_desc(&tm_q);
     }
-    if (warp == 1) {
+    if (warp == C::kMmaWarp) {
         tmem_alloc(&bars->tmem_base, 512);
         tmem_relinquish();
     }
@@ -297,64 +308,78 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     const int u_end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
     const int n_units = u_end - u_begin;
 
-    if (warp == 0) {
-        // ---------------- producer: query groups and key pages ----------------
-        // Every lane follows the unit cursor.  Page ids come from two windows
-        // of 32 consecutive table entries (lane l holds one), each loaded with
-        // one coalesced read one window ahead of its use; lane 0 issues the
-        // copies.
+    if (warp < C::kProdWarps) {
+        // ---------------- producers: query groups and key pages ----------------
+        // Every producer warp follows the unit cursor; warp pw issues the keys
+        // of units i = pw (mod kProdWarps) and warp 0 also the query groups.
+        // Page ids come from two windows of 32 consecutive table entries (lane
+        // l holds one), each loaded with one coalesced read one window ahead
+        // of its use and range-checked only when it becomes current, so that
+        // the read's latency never stalls the copies; lane 0 issues the copies.
+        // Stage and meta-slot reuse does not depend on which warp issues a
+        // unit: unit i waits for the MMA of unit i - S (S = key stages), which
+        // itself waited for unit i - S's keys, and that MMA waited for the
+        // epilogue of unit i - S - 3 (or - 2), so meta slot i % (S + 3) is free.
+        const int pw = warp;
         bool ok = true;
         int gcount = 0, pb = -1, pg = -1;
         Cursor c;
         if (n_units > 0) cursor_seek(c, bt, sReq, G, u_begin);
         int wb = -1, wlp0 = 0, wcur = -1, wnext = -1;
-        auto lookup = [&](int lp) {
-            return (lp * kPage < c.seq) ? page_lookup(bt, c.b, lp, p.status) : -1;
+        auto fetch = [&](int lp) {  // raw table entry, -1 past the sequence
+            return (lp * kPage < c.seq) ? __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + lp) : -1;
         };
-        for (int i0 = 0; i0 < n_units && ok; i0 += 16) {
-            for (int k = 0; k < 16 && i0 + k < n_units; ++k) {
-                const int i = i0 + k;
+        auto check = [&](int raw, int lp) {  // -1 (and the status set) for a bad page id
+            if (lp * kPage < c.seq && (raw < 0 || raw >= bt.num_pages)) {
+                record_error(p.status, DSA_ERR_DEVICE_CHECK);
+                return -1;
+            }
+            return raw;
+        };
+        for (int i = 0; i < n_units && ok; ++i) {
+            const int cb = c.b, cg = c.g, cq0 = c.q0;
+            const bool mine = C::kProdWarps == 1 || i % C::kProdWarps == pw;
+            const bool qnew = pw == 0 && (cb != pb || cg != pg);  // warp-uniform
+            int go = 1;
+            if (qnew) {
+                if (lane == 0) {
+                    const int x = gcount & 1;
+                    if (gcount >= 2 &&
+                        !mbar_wait(&bars->qempty[x], ((gcount >> 1) - 1) & 1, abort_flag))
+                        go = 0;
+                    if (go) {
+                        mbar_arrive_expect_tx(&bars->qfull[x], (uint32_t)N * kIdxDim);
+                        tma_load_2d(sQ + x * kQBufBytes, &tm_q, 0, (cq0 + cg * G) * kIdxHeads,
+                                    &bars->qfull[x]);
+                    }
+                }
+                ++gcount;
+                pb = cb;
+                pg = cg;
+            }
+            if (mine) {
                 const int lp = c.tile * 2;
                 if (c.b != wb || lp < wlp0 || lp >= wlp0 + 64) {
                     wb = c.b;
                     wlp0 = lp;
-                    wcur = lookup(lp + lane);
-                    wnext = lookup(lp + 32 + lane);
+                    wnext = fetch(lp + 32 + lane);
+                    wcur = check(fetch(lp + lane), lp + lane);
                 } else if (lp >= wlp0 + 32) {
                     wlp0 += 32;
-                    wcur = wnext;
-                    wnext = lookup(wlp0 + 32 + lane);
+                    wcur = check(wnext, wlp0 + lane);
+                    wnext = fetch(wlp0 + 32 + lane);
                 }
                 const int pages[2] = {__shfl_sync(0xffffffffu, wcur, lp - wlp0),
                                       __shfl_sync(0xffffffffu, wcur, lp - wlp0 + 1)};
-                const int cb = c.b, cg = c.g, cq0 = c.q0;
-                int go = 1;
-                if (lane == 0) {
-                    if (cb != pb || cg != pg) {
-                        const int x = gcount & 1;
-                        if (gcount >= 2 &&
-                            !mbar_wait(&bars->qempty[x], ((gcount >> 1) - 1) & 1, abort_flag))
-                            go = 0;
-                        if (go) {
-                            mbar_arrive_expect_tx(&bars->qfull[x], (uint32_t)N * kIdxDim);
-                            tma_load_2d(sQ + x * kQBufBytes, &tm_q, 0, (cq0 + cg * G) * kIdxHeads,
-                                        &bars->qfull[x]);
-                            ++gcount;
-                            pb = cb;
-                            pg = cg;
-                        }
-                    }
+                if (lane == 0 && go) {
                     uint32_t bytes = 0;
                     for (int h = 0; h < 2; ++h)
                         if (pages[h] >= 0)
                             bytes += (kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim) + kPage * 4;
                     // the 64 scale words of each page land in meta slot
-                    // i % (S + 3) (S = key stages), completing on the same
-                    // barrier as the keys.  Slot reuse is safe: unit i is
-                    // issued after the MMA of unit i - S, which waited for the
-                    // epilogue of unit i - S - 3 (or - 2).
+                    // i % (S + 3), completing on the same barrier as the keys
                     uint8_t* meta = sMeta + (i % C::kMetaSlots) * kMetaBytes;
-                    if (go && !kMx) {
+                    if (!kMx) {
                         const int st = i % C::kStages, kq = i / C::kStages;
                         if (kq >= 1 && !mbar_wait(&bars->empty[st], (kq - 1) & 1, abort_flag)) go = 0;
                         if (go) {
@@ -370,7 +395,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                                   (uint32_t)(kPage * 4), &bars->full[st]);
                                 }
                         }
-                    } else if (go) {
+                    } else {
                         // packed E2M1 bytes of the two pages into a staging
                         // slot; the wait for the MMA of unit i - S frees meta
                         // slot i % (S + 3) (as for FP8 keys)
@@ -394,21 +419,34 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         }
                     }
                 }
+            }
+            if (mine || qnew) {
                 if (!__shfl_sync(0xffffffffu, go, 0)) {
                     ok = false;
                     break;
                 }
-                cursor_next(c, bt, G);
             }
+            cursor_next(c, bt, G);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp < C::kMmaWarp + C::kMmaWarps) {
         // ---------------- MMA issue ----------------
+        // FP8 keys: two issuing threads (lane 0 of two warps) take alternate
+        // units, since one thread's waits, MMAs and commits of a unit take
+        // longer than the unit's keys take to arrive.  Both follow every
+        // query-group change: each releases the old query buffer with its own
+        // commit (the buffer's barrier counts both) and waits for the new one.
+        // Each unit's stage, accumulator and scale slot belong to that unit
+        // alone, so the two threads' MMAs never share an operand they write.
+        const int mw = warp - C::kMmaWarp;
         if (lane == 0 && n_units > 0) {
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
             const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 128, N, false, false);
-            const uint32_t sa = smem_u32(sStage), sq = smem_u32(sQ);
+            // descriptors of stage 0 and query buffer 0; a byte offset o moves
+            // the start-address field (16-byte units, 14 bits) by o >> 4
+            const uint64_t a0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
+            const uint64_t b0 = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
             int gcount = 0, pb = -1, pg = -1;
             bool ok = true;
             for (int i = 0; i < n_units && ok; ++i) {
@@ -419,25 +457,26 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     pb = c.b;
                     pg = c.g;
                 }
-                const int st = i % C::kStages;
-                const int acc = i % nacc;
-                if (ok) ok = mbar_wait(&bars->full[st], (i / C::kStages) & 1, abort_flag);
-                if (ok && i >= nacc) ok = mbar_wait(&bars->tempty[acc], ((i / nacc) - 1) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t qa = sq + ((gcount - 1) & 1) * kQBufBytes;
+                if (ok && (C::kMmaWarps == 1 || i % C::kMmaWarps == mw)) {
+                    const int st = i % C::kStages;
+                    const int acc = i % nacc;
+                    ok = mbar_wait(&bars->full[st], (i / C::kStages) & 1, abort_flag);
+                    if (ok && i >= nacc) ok = mbar_wait(&bars->tempty[acc], ((i / nacc) - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t ad = a0 + (uint64_t)((st * kStageBytes) >> 4);
+                    const uint64_t bd = b0 + (uint64_t)((((gcount - 1) & 1) * kQBufBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = smem_desc(sa + st * kStageBytes + kk * 32, 16, 1024,
-                                                  kSwizzle128B);
-                    const uint64_t bd = smem_desc(qa + kk * 32, 16, 1024, kSwizzle128B);
-                    if (kMx)  // one accumulator per 32-element block
-                        mma_f8f6f4(tmem + acc * acc_cols + kk * N, ad, bd, idesc, 0u);
-                    else
-                        mma_f8f6f4(tmem + acc * acc_cols, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (kMx)  // one accumulator per 32-element block
+                            mma_f8f6f4(tmem + acc * acc_cols + kk * N, ad + 2 * kk, bd + 2 * kk, idesc, 0u);
+                        else
+                            mma_f8f6f4(tmem + acc * acc_cols, ad + 2 * kk, bd + 2 * kk, idesc,
+                                       kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars->empty[st]);
+                    mma_commit(&bars->tfull[acc]);
                 }
-                mma_commit(&bars->empty[st]);
-                mma_commit(&bars->tfull[acc]);
                 cursor_next(c, bt, G);
             }
         }
@@ -449,7 +488,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         __syncwarp();
     } else if (warp < C::kEpiWarp0) {
         // ---------------- MXFP4 converters: E2M1 -> E4M3 A-operand tiles ----------
-        const int ctid = tid - 64;  // 0..127
+        const int ctid = tid - 32 * C::kConvWarp0;  // 0..127
         for (int i = 0; i < n_units; ++i) {
             const int ss = i % kStgSlots, st = i % C::kStages;
             if (!mbar_wait(&bars->sfull[ss], (i / kStgSlots) & 1, abort_flag)) break;
@@ -629,7 +668,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && tid == 0) record_error(p.status, DSA_ERR_TIMEOUT);
-    if (warp == 1) tmem_dealloc(tmem, 512);
+    if (warp == C::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -663,11 +702,11 @@ bool encode_rows128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t b
 }
 
 
-template <int kFmt>
+template <int kFmt, bool kDual>
 cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscale, const float* w,
                       const void* pages, float* scores, int64_t ld, int32_t* status,
                       cudaStream_t stream) {
-    using C = IdxCfg<kFmt>;
+    using C = IdxCfg<kFmt, kDual>;
     IdxParams p;
     p.bt = bt;
     p.qscale = qscale;
@@ -686,7 +725,7 @@ cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscal
         return cudaErrorInvalidValue;
     if (!encode_rows128(&tm_q, q8, (uint64_t)bt.total_q * kIdxHeads, (uint32_t)p.N))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<kFmt>,
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<kFmt, kDual>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -695,7 +734,7 @@ cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscal
         return e;
     // programmatic dependent launch is safe after any predecessor: the kernel
     // reads no global memory before its grid-dependency wait
-    return launch_kernel(indexer_tc_kernel<kFmt>, dim3(sms), dim3(C::kThreads),
+    return launch_kernel(indexer_tc_kernel<kFmt, kDual>, dim3(sms), dim3(C::kThreads),
                          (size_t)C::kSmemAlloc, stream, true, 1, tm_keys, tm_q, p);
 }
 
@@ -708,8 +747,12 @@ cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const fl
                                 float* scores, int64_t ld, int32_t* status,
                                 cudaStream_t stream) {
     if (key_format == DSA_KEYS_MXFP4)
-        return launch_tc<DSA_KEYS_MXFP4>(bt, q8, qscale, w, pages, scores, ld, status, stream);
-    return launch_tc<DSA_KEYS_FP8_E4M3>(bt, q8, qscale, w, pages, scores, ld, status, stream);
+        return launch_tc<DSA_KEYS_MXFP4, false>(bt, q8, qscale, w, pages, scores, ld, status, stream);
+    // groups of one or two tokens: the copies and MMAs of a unit, not its
+    // epilogue, bound the rate, so two threads issue each
+    if (bt.max_q <= 2)
+        return launch_tc<DSA_KEYS_FP8_E4M3, true>(bt, q8, qscale, w, pages, scores, ld, status, stream);
+    return launch_tc<DSA_KEYS_FP8_E4M3, false>(bt, q8, qscale, w, pages, scores, ld, status, stream);
 }
 
 }  // namespace dsa
