@@ -385,8 +385,11 @@ def run_ours(args, rank, world, local):
         lambda i: dsa.dsa_index_scores(batches[i], layers[i].q8, layers[i].qscale, layers[i].w,
                                        layers[i].index_pages, fmt, scores, ld, status,
                                        stream=stream), reps)
+    topk_ws = torch.empty(max(16, dsa.dsa_topk_workspace_size(batches[0])), dtype=torch.uint8,
+                          device=dev)
     kern["topk"] = time_graph(
-        lambda i: dsa.dsa_topk(batches[i], scores, ld, dsa.TOPK, idx, None, stream=stream), reps)
+        lambda i: dsa.dsa_topk(batches[i], scores, ld, dsa.TOPK, idx, topk_ws, stream=stream),
+        reps)
     mla_ws = torch.empty(max(16, dsa.dsa_sparse_mla_workspace_size(batches[0])),
                          dtype=torch.uint8, device=dev)
     kern["sparse_mla"] = time_graph(

@@ -11,7 +11,9 @@ cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const fl
                                 float* scores, int64_t ld, int32_t* status, cudaStream_t stream);
 bool indexer_supported(const BatchArgs& bt);
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
-                        int32_t* out, bool pdl, cudaStream_t stream);
+                        int32_t* out, void* ws, bool pdl, cudaStream_t stream);
+size_t topk_workspace_bytes(int total_q, int max_seq);
+int topk_launches(int total_q, int max_seq);
 bool topk_supported(int max_seq);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
@@ -134,9 +136,8 @@ dsa_status dsa_index_scores(const dsa_batch* batch, const uint8_t* q_fp8, const 
 }
 
 size_t dsa_topk_workspace_size(const dsa_batch* batch, int32_t topk) {
-    (void)batch;
-    (void)topk;
-    return 0;
+    if (check_batch(batch) != DSA_OK || topk != kTopK) return 0;
+    return topk_workspace_bytes(batch->total_q, batch->max_seq_len);
 }
 
 dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_ld, int32_t topk,
@@ -148,11 +149,12 @@ dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_l
     if (!aligned16(scores) || !aligned16(indices) || score_ld < batch->max_seq_len ||
         (score_ld % 4) != 0)
         return DSA_ERR_INVALID_ARG;
-    if (ws_bytes < dsa_topk_workspace_size(batch, topk)) return DSA_ERR_WORKSPACE;
-    (void)ws;
+    const size_t need = dsa_topk_workspace_size(batch, topk);
+    if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return DSA_ERR_WORKSPACE;
     if (batch->total_q == 0) return DSA_OK;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return cuda_status(launch_topk(to_args(batch), scores, score_ld, topk, indices, false,
+    g_launches.fetch_add((uint64_t)topk_launches(batch->total_q, batch->max_seq_len),
+                         std::memory_order_relaxed);
+    return cuda_status(launch_topk(to_args(batch), scores, score_ld, topk, indices, ws, false,
                                    (cudaStream_t)stream));
 }
 
@@ -209,13 +211,14 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
     uint8_t* base = static_cast<uint8_t*>(ws);
     const size_t off_topk = align_up((size_t)batch->total_q * ld * sizeof(float), 256);
     const size_t off_mla = off_topk + align_up(dsa_topk_workspace_size(batch, topk), 256);
-    g_launches.fetch_add(2 + (uint64_t)sparse_mla_launches(batch->total_q, topk),
+    g_launches.fetch_add(1 + (uint64_t)topk_launches(batch->total_q, batch->max_seq_len) +
+                             (uint64_t)sparse_mla_launches(batch->total_q, topk),
                          std::memory_order_relaxed);
     cudaError_t e = launch_index_scores(a, q_fp8, q_scale, w, index_pages, (int)key_format,
                                         scores, ld, dev_status, s);
     // the later kernels only read what the kernel before them writes after
     // their grid-dependency wait, so each may start while its predecessor runs
-    if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, true, s);
+    if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, base + off_topk, true, s);
     if (e == cudaSuccess)
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
                               base + off_mla, dev_status, true, s);

@@ -750,6 +750,384 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Split-row top-k, for a few query tokens over long rows: P CTAs per row, each
+// owning a contiguous slice (a multiple of 4 positions), so that every SM
+// works on the few rows.  Four kernels, each one pass over its slice (the rows
+// stay in L2 between them):
+//   L1   histogram of key bits 31..20 -> the bin d1 holding the k-th largest
+//   L2   keys above d1 counted; histogram of bits 19..8 of the keys in d1 -> d2
+//   L3   keys of d1 above d2 counted; histogram of bits 7..0 of the keys whose
+//        top 24 bits are (d1, d2) -> tau, and how many keys equal to tau are
+//        taken (the lowest positions); every CTA stores the suffix sums of its
+//        own level-3 histogram
+//   OUT  every CTA adds up the counts of the CTAs before it (keys above tau,
+//        keys equal to tau: two suffix-sum entries and two counts each) and
+//        writes its selected positions in order at its offset
+// Each level's row histogram is accumulated in the workspace with atomics (the
+// accumulators are cleared by a memset before L1), and the last CTA of the row
+// to finish its atomics (counter incremented after a memory fence) resolves the
+// digit; no CTA ever waits for another.
+constexpr int kSplitThreads = 512;
+constexpr int kSplitWarps = kSplitThreads / 32;
+constexpr int kSplitVec = 4;                    // float4 loads in flight per thread
+constexpr int kSplitMinSlice = 2048;            // positions per CTA, at least
+constexpr int kSplitMaxRows = 8;
+constexpr int kSplitMinSeq = kResidentMax + 1;  // shorter rows: resident kernel
+// accumulators per row (cleared): h1[4096], h2[4096], h3[256], done[4]
+constexpr int kAccH1 = 0, kAccH2 = 4096, kAccH3 = 8192, kAccDone = 8448, kAccWords = 8456;
+// per-row words after all rows' accumulators: state[8], cnt[P][2], suf[P][257]
+__host__ __device__ constexpr size_t split_row_words(int P) { return 8 + (size_t)P * 259; }
+
+struct SplitArgs {
+    BatchArgs bt;
+    const float* scores;
+    int64_t ld;
+    int K;
+    int32_t* out;
+    uint32_t* ws;
+    int P;  // CTAs per row
+};
+
+struct SplitRow {
+    int vis, lo, hi;
+    uint32_t* acc;   // cleared accumulators of the row
+    uint32_t* st;    // state[8]: d1, rem1, d2, rem2, tau, rem3
+    uint32_t* cnt;   // [P][2]: keys above d1; keys of d1 above (d1, d2)
+    uint32_t* suf;   // [P][257]: suffix sums of each CTA's level-3 histogram
+};
+
+__device__ __forceinline__ SplitRow split_row(const SplitArgs& a, int t, int c) {
+    SplitRow g;
+    const int b = request_of(a.bt, t);
+    g.vis = token_ok(a.bt, b, t, nullptr) ? visible_of(a.bt, b, t) : 0;
+    const int per = ((g.vis + a.P - 1) / a.P + 3) & ~3;
+    g.lo = min(g.vis, c * per);
+    g.hi = min(g.vis, g.lo + per);
+    g.acc = a.ws + (size_t)t * kAccWords;
+    uint32_t* rest = a.ws + (size_t)a.bt.total_q * kAccWords + (size_t)t * split_row_words(a.P);
+    g.st = rest;
+    g.cnt = rest + 8;
+    g.suf = g.cnt + 2 * a.P;
+    return g;
+}
+
+// f(pos, key, valid) over the slice, kSplitVec 16-byte loads in flight per
+// thread (positions past hi are read inside the row's padding and masked).
+template <typename F>
+__device__ __forceinline__ void split_pass(const float* row, int lo, int hi, F&& f) {
+    for (int base = lo; base < hi; base += 4 * kSplitVec * kSplitThreads) {
+        float4 x[kSplitVec];
+#pragma unroll
+        for (int u = 0; u < kSplitVec; ++u) {
+            const int i0 = base + 4 * (u * kSplitThreads + (int)threadIdx.x);
+            x[u] = (i0 < hi) ? __ldg(reinterpret_cast<const float4*>(row + i0))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kSplitVec; ++u) {
+            const int i0 = base + 4 * (u * kSplitThreads + (int)threadIdx.x);
+            f(i0 + 0, order_key(x[u].x), i0 + 0 < hi);
+            f(i0 + 1, order_key(x[u].y), i0 + 1 < hi);
+            f(i0 + 2, order_key(x[u].z), i0 + 2 < hi);
+            f(i0 + 3, order_key(x[u].w), i0 + 3 < hi);
+        }
+    }
+}
+
+// Block-wide exclusive sum over kSplitThreads threads; *total gets the sum.
+__device__ __forceinline__ uint32_t split_excl_sum(uint32_t v, uint32_t* warp_tot, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = (lane < kSplitWarps) ? warp_tot[lane] : 0u;
+        uint32_t inc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += u;
+        }
+        if (lane < kSplitWarps) warp_tot[lane] = inc - w;
+        if (lane == 31) warp_tot[kSplitWarps] = inc;
+    }
+    __syncthreads();
+    const uint32_t r = incl - v + warp_tot[warp];
+    *total = warp_tot[kSplitWarps];
+    __syncthreads();
+    return r;
+}
+
+// Flush this CTA's histogram into the row's accumulator, then report whether
+// this CTA is the row's last to do so (its atomics, and every other CTA's, are
+// then visible to it).
+__device__ __forceinline__ bool split_flush_last(const uint32_t* hist, int nb, uint32_t* acc_h,
+                                                 uint32_t* done, int P, int* s_last) {
+    for (int i = threadIdx.x; i < nb; i += kSplitThreads)
+        if (hist[i]) atomicAdd(&acc_h[i], hist[i]);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_last = (atomicAdd(done, 1u) == (uint32_t)(P - 1)) ? 1 : 0;
+    __syncthreads();
+    if (*s_last) __threadfence();
+    return *s_last != 0;
+}
+
+// Digit d over the nb = kPer * kSplitThreads (or fewer) bins of the row
+// histogram h (read once from L2) with count(> d) < rem <= count(>= d); writes
+// d and rem - count(> d) to s_out.
+template <int kPer>
+__device__ __forceinline__ void split_find(const uint32_t* h, int nb, uint32_t rem,
+                                           uint32_t* warp_tot, uint32_t* s_out) {
+    const int tid = threadIdx.x;
+    uint32_t v[kPer], part = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int r = kPer * tid + i;  // descending rank of the bin
+        v[i] = (r < nb) ? __ldcg(h + nb - 1 - r) : 0u;
+        part += v[i];
+    }
+    uint32_t tot;
+    const uint32_t above = split_excl_sum(part, warp_tot, &tot);
+    if (above < rem && rem <= above + part) {
+        uint32_t run = above;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (run < rem && run + v[i] >= rem) {
+                s_out[0] = (uint32_t)(nb - 1 - (kPer * tid + i));
+                s_out[1] = rem - run;
+            }
+            run += v[i];
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t split_block_sum(uint32_t v, uint32_t* warp_tot) {
+    uint32_t tot;
+    split_excl_sum(v, warp_tot, &tot);
+    return tot;
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_l1(SplitArgs a) {
+    __shared__ uint32_t hist[4096];
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    __shared__ uint32_t s_out[2];
+    __shared__ int s_last;
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    grid_dependency_wait();  // the scores come from the previous kernel
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) return;  // the same for every CTA of the row
+    for (int i = threadIdx.x; i < 4096; i += kSplitThreads) hist[i] = 0;
+    __syncthreads();
+    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
+        if (v) atomicAdd(&hist[key >> 20], 1u);
+    });
+    __syncthreads();
+    if (!split_flush_last(hist, 4096, g.acc + kAccH1, g.acc + kAccDone + 0, a.P, &s_last)) return;
+    split_find<4096 / kSplitThreads>(g.acc + kAccH1, 4096, (uint32_t)a.K, warp_tot, s_out);
+    if (threadIdx.x == 0) {
+        g.st[0] = s_out[0];
+        g.st[1] = s_out[1];
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_l2(SplitArgs a) {
+    __shared__ uint32_t hist[4096];
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    __shared__ uint32_t s_out[2];
+    __shared__ int s_last;
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    grid_dependency_wait();
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) return;
+    const uint32_t d1 = __ldcg(g.st + 0), rem1 = __ldcg(g.st + 1);
+    for (int i = threadIdx.x; i < 4096; i += kSplitThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t gt = 0;
+    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
+        const uint32_t b1 = key >> 20;
+        gt += (v && b1 > d1) ? 1u : 0u;
+        if (v && b1 == d1) atomicAdd(&hist[(key >> 8) & 0xFFFu], 1u);
+    });
+    gt = split_block_sum(gt, warp_tot);
+    if (threadIdx.x == 0) g.cnt[2 * c + 0] = gt;
+    __syncthreads();
+    if (!split_flush_last(hist, 4096, g.acc + kAccH2, g.acc + kAccDone + 1, a.P, &s_last)) return;
+    split_find<4096 / kSplitThreads>(g.acc + kAccH2, 4096, rem1, warp_tot, s_out);
+    if (threadIdx.x == 0) {
+        g.st[2] = s_out[0];
+        g.st[3] = s_out[1];
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_l3(SplitArgs a) {
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    __shared__ uint32_t s_out[2];
+    __shared__ int s_last;
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    grid_dependency_wait();
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) return;
+    const uint32_t d1 = __ldcg(g.st + 0), d2 = __ldcg(g.st + 2), rem2 = __ldcg(g.st + 3);
+    const uint32_t p24 = (d1 << 12) | d2;
+    for (int i = threadIdx.x; i < 256; i += kSplitThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t gt = 0;
+    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
+        const uint32_t k24 = key >> 8;
+        gt += (v && (key >> 20) == d1 && k24 > p24) ? 1u : 0u;
+        if (v && k24 == p24) atomicAdd(&hist[key & 0xFFu], 1u);
+    });
+    gt = split_block_sum(gt, warp_tot);
+    if (threadIdx.x == 0) g.cnt[2 * c + 1] = gt;
+    {   // suf[b] = keys of this slice in level-3 bins >= b (suf[256] = 0):
+        // thread i < 256 takes bin 255 - i of a scan in descending bin order
+        const int i = threadIdx.x;
+        const uint32_t hv = (i < 256) ? hist[255 - i] : 0u;
+        uint32_t tot;
+        const uint32_t ex = split_excl_sum(hv, warp_tot, &tot);
+        if (i < 256) g.suf[257 * c + 255 - i] = ex + hv;
+        if (i == 0) g.suf[257 * c + 256] = 0u;
+    }
+    if (!split_flush_last(hist, 256, g.acc + kAccH3, g.acc + kAccDone + 2, a.P, &s_last)) return;
+    split_find<1>(g.acc + kAccH3, 256, rem2, warp_tot, s_out);
+    if (threadIdx.x == 0) {
+        g.st[4] = (p24 << 8) | s_out[0];
+        g.st[5] = s_out[1];
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_out(SplitArgs a) {
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    int32_t* o = a.out + (int64_t)t * a.K;
+    grid_dependency_wait();
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) {  // every visible position, then -1
+        const int chunk = (a.K + a.P - 1) / a.P;
+        for (int i = c * chunk + (int)threadIdx.x; i < min(a.K, (c + 1) * chunk); i += kSplitThreads)
+            o[i] = (i < g.vis) ? i : -1;
+        return;
+    }
+    // thread i owns 16 consecutive positions of each 8192-position chunk; the
+    // first chunk's loads are issued before the counts are read
+    const float* row = a.scores + (size_t)t * a.ld;
+    float4 x[4];
+    auto load = [&](int base) {
+        const int p0 = base + 16 * (int)threadIdx.x;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            x[u] = (p0 + 4 * u < g.hi) ? __ldg(reinterpret_cast<const float4*>(row + p0 + 4 * u))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load(g.lo);
+    const uint32_t tau = __ldcg(g.st + 4), rem3 = __ldcg(g.st + 5);
+    const uint32_t d3 = tau & 0xFFu;
+    // keys above tau and keys equal to tau of slice cc
+    auto counts = [&](int cc, uint32_t* gt, uint32_t* eq) {
+        const uint32_t s0 = __ldcg(g.suf + 257 * cc + d3), s1 = __ldcg(g.suf + 257 * cc + d3 + 1);
+        *gt = __ldcg(g.cnt + 2 * cc) + __ldcg(g.cnt + 2 * cc + 1) + s1;
+        *eq = s0 - s1;
+    };
+    uint32_t gb = 0, eb = 0;
+    for (int cc = threadIdx.x; cc < c; cc += kSplitThreads) {
+        uint32_t gv, ev;
+        counts(cc, &gv, &ev);
+        gb += gv;
+        eb += ev;
+    }
+    const uint32_t gt_before = split_block_sum(gb, warp_tot);
+    const uint32_t eq_before = split_block_sum(eb, warp_tot);
+    uint32_t my_gt, my_eq;
+    counts(c, &my_gt, &my_eq);
+    const uint32_t my_take = rem3 > eq_before ? min(my_eq, rem3 - eq_before) : 0u;
+    const uint32_t base_out = gt_before + min(eq_before, rem3);
+    uint32_t gt_run = 0, eq_run = 0;
+    for (int base = g.lo; base < g.hi; base += 16 * kSplitThreads) {
+        const int p0 = base + 16 * (int)threadIdx.x;
+        if (base != g.lo) load(base);
+        uint32_t gm = 0, em = 0;  // bit j: position p0 + j is above / equal to tau
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * u + e;
+                if (p0 + j < g.hi) {
+                    const uint32_t key = order_key(xv[e]);
+                    gm |= (key > tau) ? (1u << j) : 0u;
+                    em |= (key == tau) ? (1u << j) : 0u;
+                }
+            }
+        }
+        uint32_t tot;
+        const uint32_t pre = split_excl_sum(((uint32_t)__popc(em) << 16) | (uint32_t)__popc(gm),
+                                            warp_tot, &tot);
+        uint32_t eq_seen = eq_run + (pre >> 16);
+        uint32_t pos = base_out + gt_run + (pre & 0xFFFFu) + min(eq_seen, my_take);
+        for (uint32_t m = gm | em; m; m &= m - 1) {
+            const int j = __ffs(m) - 1;
+            // (pos < K always holds: the per-CTA counts add up to K exactly)
+            if (gm & (1u << j)) {
+                if (pos < (uint32_t)a.K) o[pos] = p0 + j;
+                ++pos;
+            } else {
+                if (eq_seen < my_take) {
+                    if (pos < (uint32_t)a.K) o[pos] = p0 + j;
+                    ++pos;
+                }
+                ++eq_seen;
+            }
+        }
+        gt_run += tot & 0xFFFFu;
+        eq_run += tot >> 16;
+    }
+}
+
+// CTAs per row of the split path.
+int split_ctas(int total_q, int max_seq) {
+    const int by_sm = 152 / (total_q > 0 ? total_q : 1);
+    const int by_len = (max_seq + kSplitMinSlice - 1) / kSplitMinSlice;
+    const int p = by_sm < by_len ? by_sm : by_len;
+    return p > 0 ? p : 1;
+}
+
+bool use_split(int total_q, int max_seq) {
+    return total_q <= kSplitMaxRows && max_seq >= kSplitMinSeq;
+}
+
+cudaError_t launch_split(const BatchArgs& bt, const float* scores, int64_t ld, int K,
+                         int32_t* out, void* ws, bool pdl, cudaStream_t stream) {
+    SplitArgs a;
+    a.bt = bt;
+    a.scores = scores;
+    a.ld = ld;
+    a.K = K;
+    a.out = out;
+    a.ws = static_cast<uint32_t*>(ws);
+    a.P = split_ctas(bt.total_q, bt.max_seq);
+    const dim3 grid((unsigned)(bt.total_q * a.P));
+    cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)bt.total_q * kAccWords * sizeof(uint32_t), stream);
+    (void)pdl;  // the first kernel follows the memset
+    if (e == cudaSuccess) e = launch_kernel(topk_split_l1, grid, dim3(kSplitThreads), 0, stream, false, 1, a);
+    if (e == cudaSuccess) e = launch_kernel(topk_split_l2, grid, dim3(kSplitThreads), 0, stream, true, 1, a);
+    if (e == cudaSuccess) e = launch_kernel(topk_split_l3, grid, dim3(kSplitThreads), 0, stream, true, 1, a);
+    if (e == cudaSuccess) e = launch_kernel(topk_split_out, grid, dim3(kSplitThreads), 0, stream, true, 1, a);
+    return e;
+}
+
 cudaError_t launch_streaming(const BatchArgs& bt, const float* scores, int64_t ld, int K,
                              int32_t* out, int cs, bool pdl, cudaStream_t stream) {
     const size_t smem = sizeof(TopkSmem<false>);
@@ -783,9 +1161,19 @@ int topk_cluster_size(int total_q, int max_seq) {
 
 bool topk_supported(int max_seq) { return max_seq <= kSliceMax * kMaxCluster; }
 
+// Device scratch of the top-k: the split path's histograms and counts.
+size_t topk_workspace_bytes(int total_q, int max_seq) {
+    if (!use_split(total_q, max_seq)) return 0;
+    return ((size_t)total_q * kAccWords +
+            (size_t)total_q * split_row_words(split_ctas(total_q, max_seq))) * sizeof(uint32_t);
+}
+
+int topk_launches(int total_q, int max_seq) { return use_split(total_q, max_seq) ? 4 : 1; }
+
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
-                        int32_t* out, bool pdl, cudaStream_t stream) {
+                        int32_t* out, void* ws, bool pdl, cudaStream_t stream) {
     if (bt.total_q == 0) return cudaSuccess;
+    if (use_split(bt.total_q, bt.max_seq)) return launch_split(bt, scores, ld, K, out, ws, pdl, stream);
     if (bt.max_seq <= kResidentMax) return launch_resident(bt, scores, ld, K, out, pdl, stream);
     return launch_streaming(bt, scores, ld, K, out, topk_cluster_size(bt.total_q, bt.max_seq), pdl,
                             stream);

@@ -140,8 +140,13 @@ dsa_status dsa_index_scores(const dsa_batch* batch, const uint8_t* q_fp8,
  * order; when visible(t) <= topk all visible positions are written and the rest
  * is -1.  Scores must not be NaN.  -0.0 and +0.0 are equal.
  *   indices  [T, topk] int32 output (logical positions)
- *   ws       device scratch of at least dsa_topk_workspace_size() bytes (may be
- *            NULL when that size is 0)                                        */
+ *   ws       device scratch of at least dsa_topk_workspace_size() bytes,
+ *            16-byte aligned (may be NULL when that size is 0).  The size is
+ *            nonzero for batches of at most 8 query tokens with max_seq_len
+ *            above 32768: their rows are split over the whole GPU and the
+ *            scratch holds the row histograms and per-slice counts (it is
+ *            cleared by the call; its contents need not be kept between
+ *            calls).  Returns DSA_ERR_WORKSPACE when it is missing or short. */
 size_t dsa_topk_workspace_size(const dsa_batch* batch, int32_t topk);
 dsa_status dsa_topk(const dsa_batch* batch, const float* scores, int64_t score_ld,
                     int32_t topk, int32_t* indices, void* ws, size_t ws_bytes,

@@ -1,7 +1,9 @@
 """dsa_topk on crafted score matrices (independent of the indexer), bit-exact
 against the oracle's selection on the same fp32 scores: heavy ties, signed
-zeros, negative scores, rows of every length class, batch sizes that select
-different cluster sizes, and inputs that force the streaming fallback."""
+zeros, negative scores, rows of every length class, and batches that take
+each path: rows kept in shared memory (up to 32768 positions), rows split over
+the whole GPU (at most 8 query tokens), and one cluster per row (more tokens),
+including inputs that force the cluster path's exact fallback."""
 import numpy as np
 import pytest
 import torch
@@ -36,7 +38,9 @@ def _run(seq_lens, q_counts, scores):
     ld = scores.shape[1]
     S = torch.from_numpy(scores.astype(np.float32)).cuda()
     idx = torch.full((b.total_q, dsa.TOPK), -7, dtype=torch.int32, device="cuda:0")
-    dsa.dsa_topk(b, S, ld, dsa.TOPK, idx)
+    nws = dsa.dsa_topk_workspace_size(b)
+    ws = torch.full((max(nws, 16),), 0xA5, dtype=torch.uint8, device="cuda:0")  # not zero
+    dsa.dsa_topk(b, S, ld, dsa.TOPK, idx, ws if nws else None)
     torch.cuda.synchronize()
     want = oracle.topk(scores.astype(np.float32).astype(np.float64),
                        _visible(seq_lens, q_counts), dsa.TOPK)
@@ -60,8 +64,9 @@ def _scores(rng, T, ld, kind):
 
 
 @pytest.mark.parametrize("kind", ["normal", "few_levels", "signed_zero", "offset"])
-@pytest.mark.parametrize("shape", [([30000, 2049, 4096], [1, 1, 2]),     # few tokens: clusters
-                                   ([131072], [1]),                      # one long row
+@pytest.mark.parametrize("shape", [([30000, 2049, 4096], [1, 1, 2]),     # resident rows
+                                   ([131072], [1]),                      # one long row: split
+                                   ([40000] * 5, [2] * 5),               # 10 tokens: clusters
                                    ([9000] * 40, [2] * 40)])             # 80 tokens: one CTA each
 def test_topk_crafted(kind, shape):
     lens, counts = shape
@@ -71,24 +76,26 @@ def test_topk_crafted(kind, shape):
     _run(lens, counts, _scores(rng, T, ld, kind))
 
 
-def test_topk_all_equal_long_rows_use_streaming_selection():
-    # the threshold bin holds far more keys than the candidate buffers
-    lens, counts = [70000, 300000], [1, 1]
+@pytest.mark.parametrize("counts", [[1, 1], [5, 5]])
+def test_topk_all_equal_long_rows(counts):
+    # split rows (2 tokens): every key equals tau; cluster rows (10 tokens): the
+    # threshold bin holds far more keys than the candidate buffers
+    lens = [70000, 300000]
     ld = ((max(lens) + 127) // 128) * 128
-    _run(lens, counts, np.full((2, ld), 2.5))
+    _run(lens, counts, np.full((sum(counts), ld), 2.5))
 
 
 def test_topk_sample_misses_the_top():
     """The large scores sit exactly in the sampled chunks (every 16th run of 32
     positions), so the sampled threshold is far too high: the candidate pass
     finds fewer than k keys and the exact fallback must take over."""
-    lens = [131072, 200000]
+    lens, counts = [131072, 200000], [5, 5]  # 10 tokens: one cluster per row
     ld = ((max(lens) + 127) // 128) * 128
     rng = np.random.default_rng(5)
-    s = rng.standard_normal((2, ld))
+    s = rng.standard_normal((10, ld))
     pos = np.arange(ld)
     s[:, (pos // 32) % 16 == 0] += 100.0
-    _run(lens, [1, 1], s)
+    _run(lens, counts, s)
 
 
 def test_topk_one_million_positions():
@@ -108,4 +115,27 @@ def test_topk_resident_row_limits(kind):
         s = np.full((4, ld), -1.25)
     else:
         s = _scores(rng, 4, ld, kind)
+    _run(lens, counts, s)
+
+
+@pytest.mark.parametrize("kind", ["normal", "few_levels", "signed_zero", "offset"])
+def test_topk_split_rows(kind):
+    """At most 8 query tokens with a row above 32768 positions: every row is
+    split over the GPU.  Rows at and below k (all visible positions, then -1),
+    ragged slice ends, and multi-token requests (causal visibility) in one
+    batch; the workspace starts filled with garbage."""
+    lens, counts = [33000, 1000, 70001, 2049, 500000], [1, 1, 3, 1, 2]
+    rng = np.random.default_rng(21)
+    ld = ((max(lens) + 127) // 128) * 128
+    _run(lens, counts, _scores(rng, sum(counts), ld, kind))
+
+
+def test_topk_split_ties_at_the_threshold():
+    """Many keys equal to tau spread over every slice: the lowest positions are
+    taken across slice boundaries."""
+    lens, counts = [262144], [1]
+    rng = np.random.default_rng(8)
+    s = rng.standard_normal((1, lens[0]))
+    s[0, rng.random(lens[0]) < 0.05] = 1.5  # ~13,000 copies of one value
+    s[0, :100] = 9.0
     _run(lens, counts, s)
