@@ -756,7 +756,11 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
 // works on the few rows.  Four kernels, each one pass over its slice (the rows
 // stay in L2 between them):
 //   L1   histogram of key bits 31..20 -> the bin d1 holding the k-th largest
-//   L2   keys above d1 counted; histogram of bits 19..8 of the keys in d1 -> d2
+//   L2   keys above d1 counted; histogram of bits 19..8 of the keys in d1 -> d2;
+//        the keys in d1 are also appended to a list of up to 4096 (low 20 key
+//        bits, slice).  When the list holds all of them, the last CTA resolves
+//        tau and the per-slice counts from it in shared memory, and the L3
+//        kernel writes the output instead (OUT then returns at once).
 //   L3   keys of d1 above d2 counted; histogram of bits 7..0 of the keys whose
 //        top 24 bits are (d1, d2) -> tau, and how many keys equal to tau are
 //        taken (the lowest positions); every CTA stores the suffix sums of its
@@ -774,10 +778,15 @@ constexpr int kSplitVec = 4;                    // float4 loads in flight per th
 constexpr int kSplitMinSlice = 2048;            // positions per CTA, at least
 constexpr int kSplitMaxRows = 8;
 constexpr int kSplitMinSeq = kResidentMax + 1;  // shorter rows: resident kernel
-// accumulators per row (cleared): h1[4096], h2[4096], h3[256], done[4]
-constexpr int kAccH1 = 0, kAccH2 = 4096, kAccH3 = 8192, kAccDone = 8448, kAccWords = 8456;
-// per-row words after all rows' accumulators: state[8], cnt[P][2], suf[P][257]
-__host__ __device__ constexpr size_t split_row_words(int P) { return 8 + (size_t)P * 259; }
+// accumulators per row (cleared): h1[4096], h2[4096], h3[256], done[3], list length
+constexpr int kAccH1 = 0, kAccH2 = 4096, kAccH3 = 8192, kAccDone = 8448, kAccCand = 8451,
+              kAccWords = 8456;
+constexpr int kSplitCand = 4096;  // candidate list of the threshold bin
+// per-row words after all rows' accumulators: state[8], cnt[P][2], suf[P][257],
+// cand[kSplitCand]
+__host__ __device__ constexpr size_t split_row_words(int P) {
+    return 8 + (size_t)P * 259 + kSplitCand;
+}
 
 struct SplitArgs {
     BatchArgs bt;
@@ -795,6 +804,8 @@ struct SplitRow {
     uint32_t* st;    // state[8]: d1, rem1, d2, rem2, tau, rem3
     uint32_t* cnt;   // [P][2]: keys above d1; keys of d1 above (d1, d2)
     uint32_t* suf;   // [P][257]: suffix sums of each CTA's level-3 histogram
+    uint32_t* cand;  // [kSplitCand]: (key bits 19..0) << 12 | slice, keys in d1
+    int per;         // positions per slice
 };
 
 __device__ __forceinline__ SplitRow split_row(const SplitArgs& a, int t, int c) {
@@ -809,6 +820,8 @@ __device__ __forceinline__ SplitRow split_row(const SplitArgs& a, int t, int c) 
     g.st = rest;
     g.cnt = rest + 8;
     g.suf = g.cnt + 2 * a.P;
+    g.cand = g.suf + 257 * a.P;
+    g.per = per;
     return g;
 }
 
@@ -882,7 +895,7 @@ __device__ __forceinline__ bool split_flush_last(const uint32_t* hist, int nb, u
 // Digit d over the nb = kPer * kSplitThreads (or fewer) bins of the row
 // histogram h (read once from L2) with count(> d) < rem <= count(>= d); writes
 // d and rem - count(> d) to s_out.
-template <int kPer>
+template <int kPer, bool kGlobal = true>
 __device__ __forceinline__ void split_find(const uint32_t* h, int nb, uint32_t rem,
                                            uint32_t* warp_tot, uint32_t* s_out) {
     const int tid = threadIdx.x;
@@ -890,7 +903,7 @@ __device__ __forceinline__ void split_find(const uint32_t* h, int nb, uint32_t r
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int r = kPer * tid + i;  // descending rank of the bin
-        v[i] = (r < nb) ? __ldcg(h + nb - 1 - r) : 0u;
+        v[i] = (r < nb) ? (kGlobal ? __ldcg(h + nb - 1 - r) : h[nb - 1 - r]) : 0u;
         part += v[i];
     }
     uint32_t tot;
@@ -915,112 +928,12 @@ __device__ __forceinline__ uint32_t split_block_sum(uint32_t v, uint32_t* warp_t
     return tot;
 }
 
-__global__ void __launch_bounds__(kSplitThreads) topk_split_l1(SplitArgs a) {
-    __shared__ uint32_t hist[4096];
-    __shared__ uint32_t warp_tot[kSplitWarps + 1];
-    __shared__ uint32_t s_out[2];
-    __shared__ int s_last;
-    grid_dependents_launch();
-    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
-    grid_dependency_wait();  // the scores come from the previous kernel
-    const SplitRow g = split_row(a, t, c);
-    if (g.vis <= a.K) return;  // the same for every CTA of the row
-    for (int i = threadIdx.x; i < 4096; i += kSplitThreads) hist[i] = 0;
-    __syncthreads();
-    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
-        if (v) atomicAdd(&hist[key >> 20], 1u);
-    });
-    __syncthreads();
-    if (!split_flush_last(hist, 4096, g.acc + kAccH1, g.acc + kAccDone + 0, a.P, &s_last)) return;
-    split_find<4096 / kSplitThreads>(g.acc + kAccH1, 4096, (uint32_t)a.K, warp_tot, s_out);
-    if (threadIdx.x == 0) {
-        g.st[0] = s_out[0];
-        g.st[1] = s_out[1];
-    }
-}
-
-__global__ void __launch_bounds__(kSplitThreads) topk_split_l2(SplitArgs a) {
-    __shared__ uint32_t hist[4096];
-    __shared__ uint32_t warp_tot[kSplitWarps + 1];
-    __shared__ uint32_t s_out[2];
-    __shared__ int s_last;
-    grid_dependents_launch();
-    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
-    grid_dependency_wait();
-    const SplitRow g = split_row(a, t, c);
-    if (g.vis <= a.K) return;
-    const uint32_t d1 = __ldcg(g.st + 0), rem1 = __ldcg(g.st + 1);
-    for (int i = threadIdx.x; i < 4096; i += kSplitThreads) hist[i] = 0;
-    __syncthreads();
-    uint32_t gt = 0;
-    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
-        const uint32_t b1 = key >> 20;
-        gt += (v && b1 > d1) ? 1u : 0u;
-        if (v && b1 == d1) atomicAdd(&hist[(key >> 8) & 0xFFFu], 1u);
-    });
-    gt = split_block_sum(gt, warp_tot);
-    if (threadIdx.x == 0) g.cnt[2 * c + 0] = gt;
-    __syncthreads();
-    if (!split_flush_last(hist, 4096, g.acc + kAccH2, g.acc + kAccDone + 1, a.P, &s_last)) return;
-    split_find<4096 / kSplitThreads>(g.acc + kAccH2, 4096, rem1, warp_tot, s_out);
-    if (threadIdx.x == 0) {
-        g.st[2] = s_out[0];
-        g.st[3] = s_out[1];
-    }
-}
-
-__global__ void __launch_bounds__(kSplitThreads) topk_split_l3(SplitArgs a) {
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t warp_tot[kSplitWarps + 1];
-    __shared__ uint32_t s_out[2];
-    __shared__ int s_last;
-    grid_dependents_launch();
-    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
-    grid_dependency_wait();
-    const SplitRow g = split_row(a, t, c);
-    if (g.vis <= a.K) return;
-    const uint32_t d1 = __ldcg(g.st + 0), d2 = __ldcg(g.st + 2), rem2 = __ldcg(g.st + 3);
-    const uint32_t p24 = (d1 << 12) | d2;
-    for (int i = threadIdx.x; i < 256; i += kSplitThreads) hist[i] = 0;
-    __syncthreads();
-    uint32_t gt = 0;
-    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
-        const uint32_t k24 = key >> 8;
-        gt += (v && (key >> 20) == d1 && k24 > p24) ? 1u : 0u;
-        if (v && k24 == p24) atomicAdd(&hist[key & 0xFFu], 1u);
-    });
-    gt = split_block_sum(gt, warp_tot);
-    if (threadIdx.x == 0) g.cnt[2 * c + 1] = gt;
-    {   // suf[b] = keys of this slice in level-3 bins >= b (suf[256] = 0):
-        // thread i < 256 takes bin 255 - i of a scan in descending bin order
-        const int i = threadIdx.x;
-        const uint32_t hv = (i < 256) ? hist[255 - i] : 0u;
-        uint32_t tot;
-        const uint32_t ex = split_excl_sum(hv, warp_tot, &tot);
-        if (i < 256) g.suf[257 * c + 255 - i] = ex + hv;
-        if (i == 0) g.suf[257 * c + 256] = 0u;
-    }
-    if (!split_flush_last(hist, 256, g.acc + kAccH3, g.acc + kAccDone + 2, a.P, &s_last)) return;
-    split_find<1>(g.acc + kAccH3, 256, rem2, warp_tot, s_out);
-    if (threadIdx.x == 0) {
-        g.st[4] = (p24 << 8) | s_out[0];
-        g.st[5] = s_out[1];
-    }
-}
-
-__global__ void __launch_bounds__(kSplitThreads) topk_split_out(SplitArgs a) {
-    __shared__ uint32_t warp_tot[kSplitWarps + 1];
-    grid_dependents_launch();
-    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+// The ordered output of slice c of row t: every CTA adds up the counts of the
+// CTAs before it (keys above tau and keys equal to tau) and writes its
+// selected positions in ascending order at its offset.
+__device__ __forceinline__ void split_output(const SplitArgs& a, const SplitRow& g, int t, int c,
+                                             uint32_t* warp_tot) {
     int32_t* o = a.out + (int64_t)t * a.K;
-    grid_dependency_wait();
-    const SplitRow g = split_row(a, t, c);
-    if (g.vis <= a.K) {  // every visible position, then -1
-        const int chunk = (a.K + a.P - 1) / a.P;
-        for (int i = c * chunk + (int)threadIdx.x; i < min(a.K, (c + 1) * chunk); i += kSplitThreads)
-            o[i] = (i < g.vis) ? i : -1;
-        return;
-    }
     // thread i owns 16 consecutive positions of each 8192-position chunk; the
     // first chunk's loads are issued before the counts are read
     const float* row = a.scores + (size_t)t * a.ld;
@@ -1094,6 +1007,174 @@ __global__ void __launch_bounds__(kSplitThreads) topk_split_out(SplitArgs a) {
         gt_run += tot & 0xFFFFu;
         eq_run += tot >> 16;
     }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_l1(SplitArgs a) {
+    __shared__ uint32_t hist[4096];
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    __shared__ uint32_t s_out[2];
+    __shared__ int s_last;
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    grid_dependency_wait();  // the scores come from the previous kernel
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) return;  // the same for every CTA of the row
+    for (int i = threadIdx.x; i < 4096; i += kSplitThreads) hist[i] = 0;
+    __syncthreads();
+    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
+        if (v) atomicAdd(&hist[key >> 20], 1u);
+    });
+    __syncthreads();
+    if (!split_flush_last(hist, 4096, g.acc + kAccH1, g.acc + kAccDone + 0, a.P, &s_last)) return;
+    split_find<4096 / kSplitThreads>(g.acc + kAccH1, 4096, (uint32_t)a.K, warp_tot, s_out);
+    if (threadIdx.x == 0) {
+        g.st[0] = s_out[0];
+        g.st[1] = s_out[1];
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_l2(SplitArgs a) {
+    __shared__ uint32_t hist[4096];
+    __shared__ uint32_t hsm[1024];
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    __shared__ uint32_t s_out[2];
+    __shared__ int s_last;
+    __shared__ volatile int s_full;
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    grid_dependency_wait();
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) return;
+    const uint32_t d1 = __ldcg(g.st + 0), rem1 = __ldcg(g.st + 1);
+    for (int i = threadIdx.x; i < 4096; i += kSplitThreads) hist[i] = 0;
+    if (threadIdx.x == 0) s_full = 0;
+    __syncthreads();
+    uint32_t gt = 0;
+    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int pos, uint32_t key, bool v) {
+        const uint32_t b1 = key >> 20;
+        gt += (v && b1 > d1) ? 1u : 0u;
+        if (v && b1 == d1) {  // rare: the keys of the threshold bin
+            atomicAdd(&hist[(key >> 8) & 0xFFFu], 1u);
+            // append to the list; once a CTA sees it full it stops appending
+            if (!s_full) {
+                const uint32_t slot = atomicAdd(g.acc + kAccCand, 1u);
+                if (slot < (uint32_t)kSplitCand) g.cand[slot] = ((key & 0xFFFFFu) << 12) | (uint32_t)c;
+                else s_full = 1;
+            }
+        }
+    });
+    gt = split_block_sum(gt, warp_tot);
+    if (threadIdx.x == 0) g.cnt[2 * c + 0] = gt;
+    __syncthreads();
+    if (!split_flush_last(hist, 4096, g.acc + kAccH2, g.acc + kAccDone + 1, a.P, &s_last)) return;
+    const uint32_t ncand = __ldcg(g.acc + kAccCand);
+    if (ncand > (uint32_t)kSplitCand) {  // the list overflowed: level 3 resolves tau
+        split_find<4096 / kSplitThreads>(g.acc + kAccH2, 4096, rem1, warp_tot, s_out);
+        if (threadIdx.x == 0) {
+            g.st[2] = s_out[0];
+            g.st[3] = s_out[1];
+            g.st[6] = 0u;
+        }
+        return;
+    }
+    // tau from the list: bits 19..10, then 9..0 of the keys in d1
+    uint32_t* cl = hist;  // the list (this CTA's histogram is flushed)
+    for (int i = threadIdx.x; i < (int)ncand; i += kSplitThreads) cl[i] = __ldcg(g.cand + i);
+    for (int i = threadIdx.x; i < 1024; i += kSplitThreads) hsm[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < (int)ncand; i += kSplitThreads) atomicAdd(&hsm[cl[i] >> 22], 1u);
+    __syncthreads();
+    split_find<1024 / kSplitThreads, false>(hsm, 1024, rem1, warp_tot, s_out);
+    const uint32_t da = s_out[0], rema = s_out[1];
+    for (int i = threadIdx.x; i < 1024; i += kSplitThreads) hsm[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < (int)ncand; i += kSplitThreads)
+        if ((cl[i] >> 22) == da) atomicAdd(&hsm[(cl[i] >> 12) & 0x3FFu], 1u);
+    __syncthreads();
+    split_find<1024 / kSplitThreads, false>(hsm, 1024, rema, warp_tot, s_out);
+    const uint32_t tau20 = (da << 10) | s_out[0], rem3 = s_out[1];
+    const uint32_t tau = (d1 << 20) | tau20;
+    // per slice: keys of d1 above tau (hsm[0, P)) and keys equal to tau
+    // (hsm[512, 512 + P)), written where the output kernel reads them
+    for (int i = threadIdx.x; i < 1024; i += kSplitThreads) hsm[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < (int)ncand; i += kSplitThreads) {
+        const uint32_t k20 = cl[i] >> 12, sl = cl[i] & 0xFFFu;
+        if (k20 > tau20) atomicAdd(&hsm[sl], 1u);
+        else if (k20 == tau20) atomicAdd(&hsm[512 + sl], 1u);
+    }
+    __syncthreads();
+    const uint32_t d3 = tau & 0xFFu;
+    for (int cc = threadIdx.x; cc < a.P; cc += kSplitThreads) {
+        g.cnt[2 * cc + 1] = hsm[cc];
+        g.suf[257 * cc + d3] = hsm[512 + cc];
+        g.suf[257 * cc + d3 + 1] = 0u;
+    }
+    if (threadIdx.x == 0) {
+        g.st[4] = tau;
+        g.st[5] = rem3;
+        g.st[6] = 1u;
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_l3(SplitArgs a) {
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    __shared__ uint32_t s_out[2];
+    __shared__ int s_last;
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    grid_dependency_wait();
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) return;
+    if (__ldcg(g.st + 6)) {  // tau resolved from the list: write the output
+        split_output(a, g, t, c, warp_tot);
+        return;
+    }
+    const uint32_t d1 = __ldcg(g.st + 0), d2 = __ldcg(g.st + 2), rem2 = __ldcg(g.st + 3);
+    const uint32_t p24 = (d1 << 12) | d2;
+    for (int i = threadIdx.x; i < 256; i += kSplitThreads) hist[i] = 0;
+    __syncthreads();
+    uint32_t gt = 0;
+    split_pass(a.scores + (size_t)t * a.ld, g.lo, g.hi, [&](int, uint32_t key, bool v) {
+        const uint32_t k24 = key >> 8;
+        gt += (v && (key >> 20) == d1 && k24 > p24) ? 1u : 0u;
+        if (v && k24 == p24) atomicAdd(&hist[key & 0xFFu], 1u);
+    });
+    gt = split_block_sum(gt, warp_tot);
+    if (threadIdx.x == 0) g.cnt[2 * c + 1] = gt;
+    {   // suf[b] = keys of this slice in level-3 bins >= b (suf[256] = 0):
+        // thread i < 256 takes bin 255 - i of a scan in descending bin order
+        const int i = threadIdx.x;
+        const uint32_t hv = (i < 256) ? hist[255 - i] : 0u;
+        uint32_t tot;
+        const uint32_t ex = split_excl_sum(hv, warp_tot, &tot);
+        if (i < 256) g.suf[257 * c + 255 - i] = ex + hv;
+        if (i == 0) g.suf[257 * c + 256] = 0u;
+    }
+    if (!split_flush_last(hist, 256, g.acc + kAccH3, g.acc + kAccDone + 2, a.P, &s_last)) return;
+    split_find<1>(g.acc + kAccH3, 256, rem2, warp_tot, s_out);
+    if (threadIdx.x == 0) {
+        g.st[4] = (p24 << 8) | s_out[0];
+        g.st[5] = s_out[1];
+    }
+}
+
+__global__ void __launch_bounds__(kSplitThreads) topk_split_out(SplitArgs a) {
+    __shared__ uint32_t warp_tot[kSplitWarps + 1];
+    grid_dependents_launch();
+    const int t = blockIdx.x / a.P, c = blockIdx.x % a.P;
+    int32_t* o = a.out + (int64_t)t * a.K;
+    grid_dependency_wait();
+    const SplitRow g = split_row(a, t, c);
+    if (g.vis <= a.K) {  // every visible position, then -1
+        const int chunk = (a.K + a.P - 1) / a.P;
+        for (int i = c * chunk + (int)threadIdx.x; i < min(a.K, (c + 1) * chunk); i += kSplitThreads)
+            o[i] = (i < g.vis) ? i : -1;
+        return;
+    }
+    if (__ldcg(g.st + 6)) return;  // written by the level-3 kernel
+    split_output(a, g, t, c, warp_tot);
 }
 
 // CTAs per row of the split path.

@@ -139,3 +139,14 @@ def test_topk_split_ties_at_the_threshold():
     s[0, rng.random(lens[0]) < 0.05] = 1.5  # ~13,000 copies of one value
     s[0, :100] = 9.0
     _run(lens, counts, s)
+
+
+def test_topk_split_ties_within_the_list():
+    """3,000 copies of 2.5 spread over the slices of a 262,144-position row:
+    the threshold bin (about 3,800 keys) fits the candidate list, so tau and
+    the lowest 428-or-so equal positions come from the list itself."""
+    lens, counts = [262144], [1]
+    rng = np.random.default_rng(13)
+    s = rng.standard_normal((1, lens[0]))
+    s[0, rng.choice(lens[0], 3000, replace=False)] = 2.5
+    _run(lens, counts, s)
