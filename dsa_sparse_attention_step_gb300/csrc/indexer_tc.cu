@@ -79,7 +79,9 @@ struct IdxCfg {
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
     // enough key bytes in flight per SM to cover the memory latency at full load
     static constexpr int kStages = kMx ? 6 : 8;
-    static constexpr int kMetaSlots = kStages + 3;             // scale words of a unit
+    // scale words of a unit: a slot is free again S + 3 units later (S + 6 with
+    // two MMA threads, whose accumulators repeat every sixth unit)
+    static constexpr int kMetaSlots = kStages + (kDual ? 6 : 3);
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
     static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
@@ -94,8 +96,8 @@ struct IdxCfg {
 struct Bars {
     uint64_t full[kMaxStages];   // TMA / converters -> MMA: key tile ready
     uint64_t empty[kMaxStages];  // MMA -> TMA / converters: stage free (commit)
-    uint64_t tfull[3];        // MMA -> epilogue: accumulator ready (commit)
-    uint64_t tempty[3];       // epilogue -> MMA: accumulator drained (epilogue arrivals)
+    uint64_t tfull[6];        // MMA -> epilogue: accumulator ready (commit)
+    uint64_t tempty[6];       // epilogue -> MMA: accumulator drained (epilogue arrivals)
     uint64_t qfull[2];        // TMA -> MMA: query group landed
     uint64_t qempty[2];       // MMA -> TMA: query buffer free (commit)
     uint64_t sfull[kStgSlots];   // MXFP4: packed keys landed (bulk copy)
@@ -105,6 +107,8 @@ struct Bars {
     int abort_flag;
     int total_units;
 };
+
+static_assert(sizeof(Bars) <= 512, "barrier block of the shared-memory layout");
 
 struct IdxParams {
     BatchArgs bt;
@@ -235,9 +239,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     const BatchArgs& bt = p.bt;
     const int G = p.G, N = p.N;
     // TMEM accumulators: columns per unit, and three buffers when they fit in
-    // the 512 columns (the MMA then runs two units ahead of the epilogue)
+    // the 512 columns (the MMA then runs two units ahead of the epilogue).
+    // With two MMA threads (kDual, N <= 64) each thread owns three of six
+    // buffers and cycles through them in its own unit order: unit i uses
+    // buffer 3 (i % 2) + (i / 2) % 3 for the (i / 6)-th time.  Were the
+    // buffers shared, the thread at unit i could reach its wait for the
+    // epilogue of unit i - 3 while that of unit i - 6 (issued by the same
+    // thread, same buffer) is still running, and the parity wait would take
+    // the older, unfinished phase for the awaited one.
     const int acc_cols = kMx ? 4 * N : N;
-    const int nacc = (3 * acc_cols <= 512) ? 3 : 2;
+    const int nacc = kDual ? 6 : ((3 * acc_cols <= 512) ? 3 : 2);
+    auto acc_of = [&](int i) { return kDual ? 3 * (i & 1) + (i >> 1) % 3 : i % nacc; };
+    auto use_of = [&](int i) { return kDual ? (i >> 1) / 3 : i / nacc; };
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
@@ -249,7 +262,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             mbar_init(&bars->qfull[i], 1);
             mbar_init(&bars->qempty[i], C::kMmaWarps);  // one commit per MMA thread
         }
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < 6; ++i) {
             mbar_init(&bars->tfull[i], 1);
             // FP8: the min(G, 3) warp groups that take items of a unit arrive
             mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : 128 * min(G, 3));
@@ -316,10 +329,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         // l holds one), each loaded with one coalesced read one window ahead
         // of its use and range-checked only when it becomes current, so that
         // the read's latency never stalls the copies; lane 0 issues the copies.
-        // Stage and meta-slot reuse does not depend on which warp issues a
-        // unit: unit i waits for the MMA of unit i - S (S = key stages), which
-        // itself waited for unit i - S's keys, and that MMA waited for the
-        // epilogue of unit i - S - 3 (or - 2), so meta slot i % (S + 3) is free.
+        // Stage and meta-slot reuse: unit i waits for the MMA of unit i - S
+        // (S = key stages, a multiple of 2, so the same producer and MMA
+        // thread), which itself waited for unit i - S's keys and for the
+        // epilogue of the unit before it on its accumulator: i - S - 3 (or
+        // - 2) with one MMA thread, i - S - 6 with two; meta slot i % (S + 3)
+        // (S + 6) is therefore free.
         const int pw = warp;
         bool ok = true;
         int gcount = 0, pb = -1, pg = -1;
@@ -459,9 +474,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 }
                 if (ok && (C::kMmaWarps == 1 || i % C::kMmaWarps == mw)) {
                     const int st = i % C::kStages;
-                    const int acc = i % nacc;
+                    const int acc = acc_of(i), use = use_of(i);
                     ok = mbar_wait(&bars->full[st], (i / C::kStages) & 1, abort_flag);
-                    if (ok && i >= nacc) ok = mbar_wait(&bars->tempty[acc], ((i / nacc) - 1) & 1, abort_flag);
+                    if (ok && use >= 1) ok = mbar_wait(&bars->tempty[acc], (use - 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t ad = a0 + (uint64_t)((st * kStageBytes) >> 4);
@@ -567,8 +582,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     const int pg2 = __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + s / kPage);
                     page_ok = pg2 >= 0 && pg2 < bt.num_pages;
                 }
-                const int acc = i % nacc;
-                if (!mbar_wait(&bars->tfull[acc], (i / nacc) & 1, abort_flag)) break;
+                const int acc = acc_of(i);
+                if (!mbar_wait(&bars->tfull[acc], use_of(i) & 1, abort_flag)) break;
                 tc_fence_after();
                 // the unit's scale words arrived with its keys (before tfull)
                 const uint32_t sw = reinterpret_cast<const uint32_t*>(
