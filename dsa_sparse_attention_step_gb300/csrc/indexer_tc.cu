@@ -15,7 +15,7 @@
 // keys, not the queries, are balanced across SMs.  Per unit:
 //   D[128 keys x N] = K8[128 x 128] . Q8[N x 128]^T,  N = 32 heads x G tokens,
 // tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM, two or
-// three buffers).  Key pages arrive by TMA (128-byte swizzle) into an 8-stage ring
+// three buffers, or three per MMA thread when two threads issue).  Key pages arrive by TMA (128-byte swizzle) into an 8-stage ring
 // (their 64 scale words by bulk copy beside them), the query group by TMA
 // into a double buffer.  The epilogue warps read the accumulator (thread =
 // key), apply ReLU, the weighted head sum, the key scale and the causal mask,

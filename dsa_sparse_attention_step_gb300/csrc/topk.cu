@@ -9,9 +9,13 @@
 // position order.  Scores are mapped to order-preserving uint32 keys (-0
 // folded onto +0); tau denotes the k-th largest key.
 //
-// One thread-block cluster of `cs` CTAs per query token (cs = 1 for rows that
-// fit in shared memory, which are then kept resident there); CTA r owns a
-// contiguous, 32-aligned slice of the positions.
+// Three paths, by batch shape:
+//   - rows of at most 32,768 positions: one CTA per query token with the row
+//     resident in shared memory (topk_resident_kernel, below);
+//   - at most 8 query tokens over longer rows: every row split over the whole
+//     GPU by radix levels (topk_split_*, below);
+//   - otherwise one thread-block cluster of `cs` CTAs per query token, as
+//     follows.  CTA r owns a contiguous, 32-aligned slice of the positions.
 //   1. Threshold estimate.  A histogram over the top 12 key bits of a sample
 //      (every 16th 32-position chunk of the slice; every position when the row
 //      is resident) is summed over the cluster through distributed shared
