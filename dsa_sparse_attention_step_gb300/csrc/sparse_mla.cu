@@ -508,11 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 
     // ---------------- epilogue: O^T / l -> bf16 output or f16 partial ----------
     // warps 0-3 take latent-dim tiles 0-1, warps 4-7 tiles 2-3 (a warp reads
-    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads.  A
-    // final result ([96][512] bf16) is staged in the (now unused) query buffer
-    // and leaves with one bulk copy; a split partial is stored dim-major
-    // ([512][96] f16: a thread's 96 heads are 192 contiguous bytes) straight
-    // from registers, and the combine transposes it.
+    // TMEM lanes 32*(warp%4)..+31); thread = one latent dim, 96 heads.  The
+    // result is staged in the (now unused) query buffer and leaves with one
+    // bulk copy: a final result as [96][512] bf16, a split partial dim-major
+    // as [512][96] f16, row d's twelve 16-byte chunks (heads 8q..8q+7) stored
+    // at chunk (q + d) mod 12 so that a warp's stores of 32 rows spread over
+    // the banks; the combine reads them there.  (Stored from registers, the
+    // 192-byte-strided pieces cost a transaction each: about 3 us per CTA.)
     {
         __syncthreads();  // the softmax warps have seen `done` and written 1/l
         tc_fence_after();
@@ -546,26 +548,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                                 __float2bfloat16_rn(__uint_as_float(o[32 * hg + j]) * inv[j]);
                     }
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        p.part_o + (((int64_t)t * p.splits + split) * kVDim + d) * kMlaHeads);
+                    uint4* srow = reinterpret_cast<uint4*>(sQ) + 12 * d;
+                    const int rot = d % 12;
+                    float inv[96];  // the per-head scales, loaded before the stores
+#pragma unroll
+                    for (int j = 0; j < 96; j += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(sF + 256 + j);
+                        inv[j] = v4.x; inv[j + 1] = v4.y; inv[j + 2] = v4.z; inv[j + 3] = v4.w;
+                    }
 #pragma unroll
                     for (int q = 0; q < 12; ++q) {  // heads 8q .. 8q+7
-                        const float4 ia = *reinterpret_cast<const float4*>(sF + 256 + 8 * q);
-                        const float4 ib = *reinterpret_cast<const float4*>(sF + 256 + 8 * q + 4);
                         const float* ov = reinterpret_cast<const float*>(o + 8 * q);
-                        dst[q] = make_uint4(pack_half2(ov[0] * ia.x, ov[1] * ia.y),
-                                            pack_half2(ov[2] * ia.z, ov[3] * ia.w),
-                                            pack_half2(ov[4] * ib.x, ov[5] * ib.y),
-                                            pack_half2(ov[6] * ib.z, ov[7] * ib.w));
+                        const float* iv = inv + 8 * q;
+                        const int c = (q + rot >= 12) ? q + rot - 12 : q + rot;
+                        srow[c] = make_uint4(pack_half2(ov[0] * iv[0], ov[1] * iv[1]),
+                                             pack_half2(ov[2] * iv[2], ov[3] * iv[3]),
+                                             pack_half2(ov[4] * iv[4], ov[5] * iv[5]),
+                                             pack_half2(ov[6] * iv[6], ov[7] * iv[7]));
                     }
                 }
             }
-            if (p.splits == 1) fence_proxy_async_smem();  // the bulk copy reads the staged result
+            fence_proxy_async_smem();  // the bulk copy reads the staged result
         }
-        if (p.splits == 1) {
-            __syncthreads();
-            if (write && tid == 0)
+        __syncthreads();
+        if (write && tid == 0) {
+            if (p.splits == 1)
                 bulk_store_s2g(p.out + (int64_t)t * kMlaHeads * kVDim, sQ, (uint32_t)kOutBytes);
+            else
+                bulk_store_s2g(p.part_o + ((int64_t)t * p.splits + split) * kVDim * kMlaHeads, sQ,
+                               (uint32_t)kOutBytes);
         }
     }
 
@@ -597,11 +608,12 @@ sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __rest
     const int tid = threadIdx.x;
     const int d = dblk * kCombineDims + (tid & (kCombineDims - 1));
     const int h0 = 8 * (tid / kCombineDims);  // 0, 8, ..., 88
+    const int chunk = (h0 / 8 + d) % 12;      // where the partial's row d keeps heads h0..h0+7
     uint4 v[kMaxSplits];
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s)
         v[s] = (s < splits) ? __ldg(reinterpret_cast<const uint4*>(
-                                  part_o + (((int64_t)t * splits + s) * kVDim + d) * kMlaHeads + h0))
+                                  part_o + (((int64_t)t * splits + s) * kVDim + d) * kMlaHeads + 8 * chunk))
                             : make_uint4(0u, 0u, 0u, 0u);
     if (tid < kMlaHeads) {
         const int h = tid;
