@@ -80,3 +80,28 @@ def test_invalid_host_arguments_return_before_launch(lib):
     # MXFP4 append is not provided
     assert lib.dsa_append_cache(ctypes.byref(b), fake, None, 1.0, fake, None, 1, None,
                                 None) == 2
+
+
+def test_topk_workspace_follows_the_split_path(lib):
+    """Only batches of at most 8 query tokens over rows longer than 32,768
+    positions split their rows over the GPU and need top-k scratch; the fused
+    step's workspace includes it, and a missing one is refused before launch."""
+    fake = ctypes.c_void_p(4096)
+    pages = (1 << 20) // 64
+
+    def size(total_q, max_seq):
+        b = _cbatch(total_q=total_q, num_requests=1, max_q_per_request=total_q,
+                    max_seq_len=max_seq, num_pages=pages, max_pages=pages)
+        return b, lib.dsa_topk_workspace_size(ctypes.byref(b), 2048)
+
+    b1, one = size(1, 1 << 20)
+    _, two = size(2, 1 << 20)
+    _, eight = size(8, 1 << 20)
+    assert one > 0 and two > one and eight > 0
+    assert size(9, 1 << 20)[1] == 0       # one cluster per row
+    assert size(8, 32768)[1] == 0         # rows kept in shared memory
+    assert size(1, 32769)[1] > 0
+    scores = (1 << 20) * 4
+    assert lib.dsa_decode_workspace_size(ctypes.byref(b1), 2048) >= scores + one
+    assert lib.dsa_topk(ctypes.byref(b1), fake, 1 << 20, 2048, fake, None, 0, None) == 3
+    assert lib.dsa_topk(ctypes.byref(b1), fake, 1 << 20, 2048, fake, fake, one - 1, None) == 3
