@@ -211,6 +211,25 @@ class ClockSampler:
 
 # ---- GPU arm ----------------------------------------------------------------
 
+def job_elapsed(elapsed, world, device):
+    """The job's time: the longest of the ranks' timed regions, returned on
+    every rank (one all-reduce over the process group's backend: NCCL on the
+    GPUs, gloo in the CPU tests)."""
+    if world == 1:
+        return elapsed
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, tokens_per_rank, steps, elapsed):
+    """Whole-job query tokens/s: every rank's tokens over the job's time
+    (replicas, so per-rank work is fixed as ranks are added: weak scaling)."""
+    return world * tokens_per_rank * steps / elapsed
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dsa_sparse_attention_step_gb300", "csrc")
@@ -340,11 +359,7 @@ def run_ours(args, rank, world, local):
         step(nxt, stream)
     per_step_launches = dsa.dsa_launch_count() - c0
     gpu_launches = per_step_launches * args.steps
-    elapsed = ev0.elapsed_time(ev1) / 1000.0
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = job_elapsed(ev0.elapsed_time(ev1) / 1000.0, world, dev)
     # keep the GPU busy a little longer while the clock sampler runs
     t_end = time.time() + args.soak_seconds
     while time.time() < t_end:
@@ -487,7 +502,7 @@ def run_ours(args, rank, world, local):
 
     if rank == 0:
         step_b = wl.step_bytes(lens, q_counts, fmt)
-        value = world * T * args.steps / elapsed
+        value = job_value(world, T, args.steps, elapsed)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1000.0 * elapsed / args.steps, "higher_is_better": True,
