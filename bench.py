@@ -4,13 +4,18 @@ roofline fraction of the dominant kernel).
 
 A step is one call of the fused dsa_decode (indexer -> exact top-2048 ->
 sparse MLA) over one batch, on one layer's paged caches.  Consecutive steps
-rotate through `--layers` independent layer copies (24 by default, as in the
-24 full-attention layers of the model), so that the working set is far larger
-than the 129 MB L2 and every step reads its caches from HBM.
+rotate through `--layers` independent layer copies (by default as many as make
+the rotated caches at least eight times the 129 MB L2, between 2 and 24 -- the
+model has 24 full-attention layers), so that every step reads its caches from
+HBM.
 
-Default workload: 8 requests, contexts drawn uniformly from [16384, 32768],
-one query token each (batched decode).  `--config` selects another:
-c0_tiny, c1_batched, c2_agentic, c3a_long_fp8, c3b_long_mxfp4.
+Default workload: agentic multi-token decode, 64 requests of 131072 positions
+with 5 causal query tokens each (the largest decode batch).  `--config`
+selects another: c0_tiny, c1_batched, c2_agentic, c3a_long_fp8,
+c3b_long_mxfp4, c4_prefill_append.
+
+Timing: every timed step is replayed from a captured CUDA graph (whatever
+--steps is), with the graph pieces built before the timed region.
 
 Arms
   --impl ours       (default) the CUDA library through its C ABI.
@@ -44,11 +49,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def parse():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2400)
-    ap.add_argument("--warmup", type=int, default=48)
-    ap.add_argument("--config", default="c1_batched")
+    ap.add_argument("--steps", type=int, default=1200)
+    ap.add_argument("--warmup", type=int, default=24)
+    ap.add_argument("--config", default="c2_agentic")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layer copies rotated step by step; 0 = enough for 8x the L2")
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (profiling at a "
                          "smaller scale with the same per-request shape); 0 = all")
@@ -95,15 +101,30 @@ def oracle_step(layer, rows):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, seconds):
-    """The oracle on the host cores: whole layer steps (all query rows of the
-    batch, in parallel over rows) until about `seconds` of CPU work."""
+def oracle_sample_layer(cfg, threads):
+    """A bounded sample of the workload for the CPU oracle: the first requests
+    of the batch (same per-request shape: context lengths, query tokens,
+    causal rule, value recipe), enough of them to give every host thread a
+    query row, built on the host.  The rate metric is per query token, so the
+    sample measures it directly."""
     import dsa_inputs as di
-    import oracle
     lens, q_counts, fmt, seed = config_shape(cfg)
+    n, rows = 0, 0
+    while n < len(lens) and rows < threads:
+        rows += q_counts[n]
+        n += 1
+    lens, q_counts = lens[:n], q_counts[:n]
+    return di.make_layer(lens, q_counts, fmt, seed), lens, q_counts
+
+
+def cpu_baseline(cfg, seconds):
+    """The oracle on the host cores: steps over the sample's query rows (in
+    parallel over rows) until about `seconds` of CPU work."""
+    import oracle
+    threads = max(1, oracle.num_threads())
+    layer, lens, q_counts = oracle_sample_layer(cfg, threads)
     T = sum(q_counts)
-    rows_per_step = min(T, max(1, oracle.num_threads()))
-    layer = di.make_layer(lens, q_counts, fmt, seed)
+    rows_per_step = min(T, threads)
     done_rows, spent, steps = 0, 0.0, 0
     while spent < seconds and steps < 64:
         rows = [(done_rows + i) % T for i in range(rows_per_step)]
@@ -111,25 +132,26 @@ def cpu_baseline(cfg, seconds):
         done_rows += rows_per_step
         steps += 1
     return {"value": done_rows / spent, "unit": UNIT,
-            "cores": min(rows_per_step, oracle.num_threads()), "kind": "oracle",
-            "sample": "%d oracle step(s) of %d query rows of one %s layer (ctx %d..%d), "
-                      "%.1f s" % (steps, rows_per_step, cfg, min(lens), max(lens), spent)}
+            "cores": min(rows_per_step, threads), "kind": "oracle",
+            "sample": "%d oracle step(s) of %d query rows (full indexer over the row's "
+                      "context, top-2048, MLA), from the first %d request(s) of %s "
+                      "(ctx %d..%d), %.1f s" % (steps, rows_per_step, len(lens), cfg,
+                                               min(lens), max(lens), spent)}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    import dsa_inputs as di
     import oracle
-    lens, q_counts, fmt, seed = config_shape(args.config)
+    threads = max(1, oracle.num_threads())
+    layer, lens, q_counts = oracle_sample_layer(args.config, threads)
+    full_lens, full_q, _, _ = config_shape(args.config)
     T = sum(q_counts)
-    layer = di.make_layer(lens, q_counts, fmt, seed)
-    threads = oracle.num_threads()
     rows_per_step = min(T, threads)
     # size each step so that warm-up + timed steps end within ~150 s
     probe = oracle_step(layer, list(range(rows_per_step)))
     budget = 150.0 / max(1, args.steps + args.warmup)
-    while rows_per_step > 1 and probe * rows_per_step / min(rows_per_step, threads) > budget:
+    while rows_per_step > 1 and probe > budget:
         rows_per_step = max(1, rows_per_step // 2)
         probe = oracle_step(layer, list(range(rows_per_step)))
     cursor = 0
@@ -143,14 +165,15 @@ def run_reference(args, rank, world):
     rows = args.steps * rows_per_step
     value = rows / spent
     cores = min(rows_per_step, threads)
-    sample = "%d query rows of one %s layer per step (full indexer + top-k + MLA per row)" % (
-        rows_per_step, args.config)
+    sample = ("%d query rows per step (full indexer over the row's context, top-2048, MLA) "
+              "from the first %d request(s) of %s" % (rows_per_step, len(lens), args.config))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * spent / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config, "requests": len(lens),
-                       "seq_lens": [min(lens), max(lens)], "query_tokens": T},
+            "config": {"workload": args.config, "requests": len(full_lens),
+                       "seq_lens": [min(full_lens), max(full_lens)],
+                       "query_tokens": sum(full_q)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -230,28 +253,62 @@ def job_value(world, tokens_per_rank, steps, elapsed):
     return world * tokens_per_rank * steps / elapsed
 
 
-def kernel_source_hash():
+# Sources each kernel's DRAM traffic depends on (its own file and the shared
+# device headers): a recorded traffic figure is used only while these hash to
+# the value it was measured at.
+KERNEL_SOURCES = {
+    "indexer": ["indexer_tc.cu", "common.cuh", "sm100.cuh"],
+    "topk": ["topk.cu", "common.cuh"],
+    "sparse_mla": ["sparse_mla.cu", "common.cuh", "sm100.cuh"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dsa_sparse_attention_step_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    for n in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, n), "rb") as f:
             h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel, cfg):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    """DRAM bytes (read + write) per full-size launch from a committed ncu
+    summary, when it was measured on the kernel's current sources; else None.
+    A capture of a smaller case carries `scale` (full launch / captured launch,
+    by units processed) and is scaled here."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         e = rec[kernel][cfg]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("measured_at_hash") != kernel_source_hash(kernel):
             return None
-        return float(e["dram_bytes_per_launch"])
+        return float(e["dram_bytes_per_captured_launch"]) * float(e.get("scale", 1.0))
     except Exception:
         return None
+
+
+def auto_layers(lens, fmt, l2_bytes=129e6):
+    """Layer copies to rotate: enough that the rotated caches exceed 8x the L2,
+    at least 2 and at most 24 (the model's full-attention layer count)."""
+    kb = 8448 if fmt == 0 else 4352
+    per_layer = sum((s + 63) // 64 for s in lens) * (kb + 36864)
+    n = int(-(-8 * l2_bytes // per_layer))
+    return max(2, min(24, n))
+
+
+def graph_pieces(first, n, L):
+    """Split n consecutive steps starting at layer `first` into runs that each
+    stay within one pass over the L layers: (start layer, length) pairs."""
+    out = []
+    i = first % L
+    while n > 0:
+        k = min(n, L - i)
+        out.append((i, k))
+        n -= k
+        i = (i + k) % L
+    return out
 
 
 def run_ours(args, rank, world, local):
@@ -279,7 +336,7 @@ def run_ours(args, rank, world, local):
     if args.requests > 0:
         lens, q_counts = lens[:args.requests], q_counts[:args.requests]
     T = sum(q_counts)
-    L = max(1, args.layers)
+    L = args.layers if args.layers > 0 else auto_layers(lens, fmt)
     dev = torch.device("cuda", local)
     layers, batches = [], []
     for l in range(L):
@@ -289,9 +346,13 @@ def run_ours(args, rank, world, local):
         batches.append(dsa.Batch(lay.q_offsets, lay.seq_lens, lay.block_table, lay.num_pages,
                                  lens, q_counts))
     cache_bytes = sum(l.index_pages.numel() + l.latent_pages.numel() for l in layers)
-    out = torch.empty(T, 96, 512, dtype=torch.bfloat16, device=dev)
+    # the step's outputs share one device buffer, so that the end-to-end leg
+    # reads them back with one copy
+    out_bytes = T * 96 * 512 * 2
+    obuf = torch.empty(out_bytes + T * dsa.TOPK * 4, dtype=torch.uint8, device=dev)
+    out = obuf[:out_bytes].view(torch.bfloat16).view(T, 96, 512)
+    idx = obuf[out_bytes:].view(torch.int32).view(T, dsa.TOPK)
     lse = torch.empty(T, 96, dtype=torch.float32, device=dev)
-    idx = torch.empty(T, dsa.TOPK, dtype=torch.int32, device=dev)
     ws = torch.empty(dsa.dsa_decode_workspace_size(batches[0]), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -311,64 +372,69 @@ def run_ours(args, rank, world, local):
                        lay.latent_pages, lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx,
                        ws, status, stream=s)
 
-    # one CUDA graph = one pass over the L layers (L steps)
+    # eager warm-up of every layer (module loading, lazy set-up), then graphs:
+    # one per (start layer, length) piece, all captured before timing
     with torch.cuda.stream(stream):
-        for i in range(min(args.warmup, 2 * L) + 1):
-            step(i, stream)
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
         for i in range(L):
             step(i, stream)
+    stream.synchronize()
+    graphs = {}
 
-    def run_steps(n, first):
-        """n steps starting at layer `first % L` (graph replays + singles)."""
+    def graph(start, n):
+        if (start, n) not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(start, start + n):
+                    step(i, stream)
+            graphs[(start, n)] = g
+        return graphs[(start, n)]
+
+    warm_pieces = graph_pieces(0, args.warmup, L)
+    timed_pieces = graph_pieces(args.warmup, args.steps, L)
+    for s0, n in warm_pieces + timed_pieces:
+        graph(s0, n)
+
+    def replay(pieces):
         with torch.cuda.stream(stream):
-            i = first
-            while n > 0 and i % L != 0:
-                step(i, stream); i += 1; n -= 1
-            while n >= L:
-                graph.replay(); i += L; n -= L
-            while n > 0:
-                step(i, stream); i += 1; n -= 1
-        return i
+            for s0, n in pieces:
+                graphs[(s0, n)].replay()
 
-    nxt = run_steps(args.warmup, 0)
+    replay(warm_pieces)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    l0 = dsa.dsa_launch_count()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     ev0.record(stream)
-    nxt = run_steps(args.steps, nxt)
+    replay(timed_pieces)
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    launches_timed = dsa.dsa_launch_count() - l0
-    # graph replays do not pass through the library's counter: count the
-    # kernels of one step by a direct call, then scale to the timed steps
+    # graph replays do not pass through the library's launch counter: count
+    # the kernels of one step by a direct call, then scale to the timed steps
     c0 = dsa.dsa_launch_count()
     with torch.cuda.stream(stream):
-        step(nxt, stream)
+        step(0, stream)
     per_step_launches = dsa.dsa_launch_count() - c0
     gpu_launches = per_step_launches * args.steps
     elapsed = job_elapsed(ev0.elapsed_time(ev1) / 1000.0, world, dev)
     # keep the GPU busy a little longer while the clock sampler runs
+    soak = graph_pieces(0, L, L)
     t_end = time.time() + args.soak_seconds
     while time.time() < t_end:
-        nxt = run_steps(L * 8, nxt)
+        replay(soak)
         torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     st = int(status.item())
     if st != 0:
         raise RuntimeError("device status %d (%s)" % (st, dsa.dsa_status_string(st)))
+    del graphs
 
     # ---- per-kernel durations (graphs of L launches of one entry point) ----
     ld = ((max(lens) + 127) // 128) * 128
@@ -416,21 +482,31 @@ def run_ours(args, rank, world, local):
               "sparse_mla": wl.mla_bytes(lens, q_counts)}
     dominant = max(kern, key=kern.get)
     hbm, bf16, src = peaks()
+    hashes = {k: kernel_source_hash(k) for k in KERNEL_SOURCES}
     if args.config == "c4_prefill_append":
         # the prefill-append indexer is a dense causal FP8 GEMM: its roofline is
         # the FP8 tensor peak (the measured bf16 GEMM rate x the nominal 2x of
-        # FP8 over bf16), for the indexer kernel alone
+        # FP8 over bf16), for the indexer kernel alone; the kernel runs inside
+        # a multi-millisecond step, so the sustained rate is reported as well
         dominant = "indexer"
         flops = wl.indexer_flops(lens, q_counts)
         fp8_peak = 2.0 * bf16
         achieved = flops / kern["indexer"] / 1e12
+        sustained = None
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                sustained = 2.0 * float(json.load(f)["bf16_tflops_sustained"])
+        except Exception:
+            pass
         roofline = {"bound": "tensor", "kernel": "indexer", "achieved": achieved,
                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                     "traffic": recorded_traffic("indexer", args.config),
                     "peak_source": src + " (bf16 GEMM burst x 2 for FP8)",
+                    "frac_of_sustained": (achieved / sustained) if sustained else None,
                     "algorithmic_flops_per_launch": flops,
                     "avg_launch_us": kern["indexer"] * 1e6,
-                    "kernels_us": {k: v * 1e6 for k, v in kern.items()}}
+                    "kernels_us": {k: v * 1e6 for k, v in kern.items()},
+                    "source_hashes": hashes}
     else:
         achieved = kbytes[dominant] / kern[dominant] / 1e9
         traffic = recorded_traffic(dominant, args.config)
@@ -439,56 +515,82 @@ def run_ours(args, rank, world, local):
                     "peak_source": src + " (burst copy)",
                     "algorithmic_bytes_per_launch": kbytes[dominant],
                     "avg_launch_us": kern[dominant] * 1e6,
-                    "kernels_us": {k: v * 1e6 for k, v in kern.items()}}
+                    "kernels_us": {k: v * 1e6 for k, v in kern.items()},
+                    "kernels_frac": {k: kbytes[k] / kern[k] / 1e9 / hbm for k in kern},
+                    "source_hashes": hashes}
 
     # ---- end to end through the public API with host buffers --------------
+    # per step: one pinned-host -> device copy of the step's inputs (queries
+    # and request metadata packed in one staging buffer), the step, and one
+    # device -> pinned-host copy of its outputs (attention output and indices)
     e2e = None
     if rank == 0:
-        pin = lambda t: t.cpu().pin_memory()
-        hq = [(pin(l.q8), pin(l.qscale), pin(l.w), pin(l.q_lat)) for l in layers]
-        if append:  # the new tokens' keys and latents come from the host too
-            hq = [h + (pin(pl[0]), pin(pl[1])) for h, pl in zip(hq, payloads)]
-        hmeta = [(pin(l.q_offsets), pin(l.seq_lens), pin(l.block_table)) for l in layers]
-        two = [layers[0], layers[0]]  # two device slots, alternated step by step
-        dq = [(torch.empty_like(l.q8), torch.empty_like(l.qscale), torch.empty_like(l.w),
-               torch.empty_like(l.q_lat)) for l in two]
-        if append:
-            dq = [d + (torch.empty_like(payloads[0][0]), torch.empty_like(payloads[0][1]))
-                  for d in dq]
-        dmeta = [(torch.empty_like(l.q_offsets), torch.empty_like(l.seq_lens),
-                  torch.empty_like(l.block_table)) for l in two]
-        dbatch = [dsa.Batch(m[0], m[1], m[2], layers[0].num_pages, lens, q_counts)
-                  for m in dmeta]
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hidx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in hq[0] + hmeta[0])
-        d2h = hout.numel() * hout.element_size() + hidx.numel() * hidx.element_size()
+        def pack(tensors):
+            offs, o = [], 0
+            for t in tensors:
+                offs.append(o)
+                o += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.empty(o, dtype=torch.uint8).pin_memory()
+            for t, off in zip(tensors, offs):
+                n = t.numel() * t.element_size()
+                buf[off:off + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+            return buf, offs
+
+        def host_inputs(j):
+            lay = layers[j]
+            ts = [lay.q8, lay.qscale, lay.w, lay.q_lat, lay.q_offsets, lay.seq_lens,
+                  lay.block_table]
+            if append:
+                ts += list(payloads[j])
+            return [t.cpu() for t in ts]
+
+        hin = [pack(host_inputs(j)) for j in range(L)]
+        shapes = [(t.dtype, tuple(t.shape)) for t in host_inputs(0)]
+        nbytes_in = hin[0][0].numel()
+        offs = hin[0][1]
+        # two device staging slots, alternated step by step
+        din = [torch.empty(nbytes_in, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+        def views(buf):
+            v = []
+            for (dt, shp), off in zip(shapes, offs):
+                n = 1
+                for d in shp:
+                    n *= d
+                esz = torch.empty(0, dtype=dt).element_size()
+                v.append(buf[off:off + n * esz].view(dt).view(shp))
+            return v
+
+        dviews = [views(b) for b in din]
+        dbatch = [dsa.Batch(v[4], v[5], v[6], layers[0].num_pages, lens, q_counts)
+                  for v in dviews]
+        hout = torch.empty(obuf.numel(), dtype=torch.uint8).pin_memory()
+        h2d = nbytes_in
+        d2h = obuf.numel()
 
         def e2e_step(i):
             j = i % L
             slot = i % 2
             lay = layers[j]
-            for d, h in zip(dq[slot] + dmeta[slot], hq[j] + hmeta[j]):
-                d.copy_(h, non_blocking=True)
-            q8, qs, w, ql = dq[slot][:4]
+            din[slot].copy_(hin[j][0], non_blocking=True)
+            v = dviews[slot]
             if append:
-                dsa.dsa_append_cache(dbatch[slot], dq[slot][4], dq[slot][5], lay.kv_scale,
+                dsa.dsa_append_cache(dbatch[slot], v[7], v[8], lay.kv_scale,
                                      lay.index_pages, lay.latent_pages, fmt, status, stream=stream)
             # the block table copied in belongs to layer j's pools
-            dsa.dsa_decode(dbatch[slot], q8, qs, w, lay.index_pages, fmt, ql, lay.latent_pages,
-                           lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx, ws, status,
-                           stream=stream)
-            hout.copy_(out, non_blocking=True)
-            hidx.copy_(idx, non_blocking=True)
+            dsa.dsa_decode(dbatch[slot], v[0], v[1], v[2], lay.index_pages, fmt, v[3],
+                           lay.latent_pages, lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx,
+                           ws, status, stream=stream)
+            hout.copy_(obuf, non_blocking=True)
 
         with torch.cuda.stream(stream):
-            for i in range(args.warmup):
+            for i in range(max(3, min(args.warmup, 2 * L))):
                 e2e_step(i)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             stream.synchronize()
             a.record(stream)
-            n_e2e = min(args.steps, 480)
+            n_e2e = max(1, min(args.steps, 480))
             for i in range(n_e2e):
                 e2e_step(i)
             b.record(stream)
@@ -496,9 +598,10 @@ def run_ours(args, rank, world, local):
         te = a.elapsed_time(b) / 1000.0
         e2e = {"value": T * n_e2e / te, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "note": "per step: pinned H2D of queries and metadata" +
+               "note": "per step: one pinned H2D copy of the packed queries and metadata" +
                        (" and the new tokens' keys and latents, dsa_append_cache" if append else "") +
-                       ", dsa_decode, D2H of output and indices; caches resident"}
+                       ", dsa_decode (eager launches through the C ABI), one D2H copy of "
+                       "output and indices; caches resident"}
 
     if rank == 0:
         step_b = wl.step_bytes(lens, q_counts, fmt)
@@ -513,10 +616,12 @@ def run_ours(args, rank, world, local):
                            "layers_rotated": L, "cache_bytes_rotated": cache_bytes,
                            "l2": "inputs larger than L2: %d layer copies, %.2f GB of caches "
                                  "rotated" % (L, cache_bytes / 1e9),
+                           "timing": "CUDA graphs of the timed steps, replayed back to back",
                            "step": "dsa_append_cache + dsa_decode" if args.config == "c4_prefill_append"
                                    else "dsa_decode",
                            "parallelism": "replicas" if world > 1 else "single"},
                 "step_hbm_gbs": step_b / (elapsed / args.steps) / 1e9,
+                "step_frac": step_b / (elapsed / args.steps) / 1e9 / hbm,
                 "step_bytes": step_b,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": gpu_launches, "clocks": clocks}

@@ -15,7 +15,7 @@ __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path"
            "dsa_status_string", "dsa_launch_count", "dsa_index_scores", "dsa_topk",
            "dsa_topk_workspace_size", "dsa_sparse_mla", "dsa_sparse_mla_workspace_size",
            "dsa_decode", "dsa_decode_workspace_size", "dsa_decode_noalloc",
-           "NOALLOC_SCRATCH_BYTES", "dsa_append_cache"]
+           "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards"]
 
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
@@ -45,6 +45,16 @@ class _CBatch(ctypes.Structure):
                 ("seq_lens", ctypes.c_void_p), ("block_table", ctypes.c_void_p)]
 
 
+class ShardPart(ctypes.Structure):
+    """One part of a request assigned to a rank (dsa_shard_part)."""
+    _fields_ = [("request", ctypes.c_int32), ("token_begin", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int32), ("seq_len", ctypes.c_int32)]
+
+    def __repr__(self):
+        return "ShardPart(request=%d, token_begin=%d, num_tokens=%d, seq_len=%d)" % (
+            self.request, self.token_begin, self.num_tokens, self.seq_len)
+
+
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64
@@ -67,6 +77,11 @@ _SIGS = {
     "dsa_decode_noalloc": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32,
                                           _f32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dsa_append_cache": (ctypes.c_int, [_bp, _vp, _vp, _f32, _vp, _vp, ctypes.c_int, _vp, _vp]),
+    "dsa_plan_token_shards": (ctypes.c_int32, [ctypes.POINTER(ctypes.c_int32),
+                                               ctypes.POINTER(ctypes.c_int32), _i32, _i32, _i32,
+                                               ctypes.POINTER(ShardPart), _i32]),
+    "dsa_test_sparse_mla_wait_timeout": (ctypes.c_int, [_bp, _vp, _vp, _f32, _f32, _vp, _i32, _vp,
+                                                        _vp, _vp, _sz, _vp, _vp]),
 }
 
 
@@ -201,6 +216,20 @@ def dsa_sparse_mla(batch, q_lat, latent_pages, kv_scale, sm_scale, indices, topk
     _check(rc, "dsa_sparse_mla")
 
 
+def dsa_test_sparse_mla_wait_timeout(batch, q_lat, latent_pages, kv_scale, sm_scale, indices,
+                                     topk, out, lse=None, ws=None, dev_status=None, stream=None):
+    """Test-only (include/dsa_testing.h): dsa_sparse_mla with the kernel's
+    bounded-wait failure path forced; the device status becomes 6."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().dsa_test_sparse_mla_wait_timeout(
+        batch.ref(), _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+        _ptr(latent_pages, torch.uint8, "latent_pages"), float(kv_scale), float(sm_scale),
+        _ptr(indices, torch.int32, "indices"), int(topk),
+        _ptr(out, (torch.bfloat16, torch.int16), "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(ws), nbytes, _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_test_sparse_mla_wait_timeout")
+
+
 def dsa_decode_workspace_size(batch, topk=TOPK):
     return int(load().dsa_decode_workspace_size(batch.ref(), int(topk)))
 
@@ -240,6 +269,20 @@ def dsa_decode_noalloc(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat,
                                    _ptr(indices, torch.int32, "indices"),
                                    _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(rc, "dsa_decode_noalloc")
+
+
+def dsa_plan_token_shards(seq_lens, q_counts, world, rank):
+    """Parts of the batch's requests that rank `rank` of `world` runs in a
+    token-sharded prefill (host only; see include/dsa.h)."""
+    n = len(seq_lens)
+    sl = (ctypes.c_int32 * n)(*[int(v) for v in seq_lens])
+    qc = (ctypes.c_int32 * n)(*[int(v) for v in q_counts])
+    cap = 2 * n
+    parts = (ShardPart * max(cap, 1))()
+    rc = load().dsa_plan_token_shards(sl, qc, n, int(world), int(rank), parts, cap)
+    if rc < 0:
+        raise DsaError(-rc, "dsa_plan_token_shards")
+    return [ShardPart(p.request, p.token_begin, p.num_tokens, p.seq_len) for p in parts[:rc]]
 
 
 def dsa_append_cache(batch, new_keys, new_latent, kv_scale, index_pages, latent_pages, key_format,

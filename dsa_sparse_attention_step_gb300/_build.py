@@ -32,7 +32,7 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        [os.path.join(ROOT, "include", "dsa.h"), os.path.abspath(__file__)]
+        glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)]
 
 
 def up_to_date():

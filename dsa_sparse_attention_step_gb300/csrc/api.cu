@@ -4,6 +4,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "../../include/dsa_testing.h"
 
 namespace dsa {
 cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const float* qscale,
@@ -18,7 +19,7 @@ bool topk_supported(int max_seq);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
-                              cudaStream_t stream);
+                              cudaStream_t stream, bool wait_test = false);
 size_t sparse_mla_workspace_bytes(int total_q, int K);
 int sparse_mla_launches(int total_q, int K);
 cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const float* lat,
@@ -223,6 +224,25 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
                               base + off_mla, dev_status, true, s);
     return cuda_status(e);
+}
+
+dsa_status dsa_test_sparse_mla_wait_timeout(const dsa_batch* batch, const uint16_t* q_lat,
+                                           const void* latent_pages, float kv_scale,
+                                           float sm_scale, const int32_t* indices, int32_t topk,
+                                           uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                                           int32_t* dev_status, dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    st = check_mla_args(batch, q_lat, latent_pages, indices, topk, out, kv_scale, sm_scale);
+    if (st != DSA_OK) return st;
+    const size_t need = dsa_sparse_mla_workspace_size(batch, topk);
+    if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0) return DSA_OK;
+    g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk),
+                         std::memory_order_relaxed);
+    return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
+                                         indices, topk, out, lse, ws, dev_status, false,
+                                         (cudaStream_t)stream, true));
 }
 
 dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,

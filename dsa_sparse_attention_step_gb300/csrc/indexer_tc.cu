@@ -338,6 +338,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         const int pw = warp;
         bool ok = true;
         int gcount = 0, pb = -1, pg = -1;
+        int q_issued = 0;      // query groups whose copy was issued (lane 0)
+        int last_issued = -1;  // last unit whose key copies were issued (lane 0)
         Cursor c;
         if (n_units > 0) cursor_seek(c, bt, sReq, G, u_begin);
         int wb = -1, wlp0 = 0, wcur = -1, wnext = -1;
@@ -366,6 +368,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         mbar_arrive_expect_tx(&bars->qfull[x], (uint32_t)N * kIdxDim);
                         tma_load_2d(sQ + x * kQBufBytes, &tm_q, 0, (cq0 + cg * G) * kIdxHeads,
                                     &bars->qfull[x]);
+                        ++q_issued;
                     }
                 }
                 ++gcount;
@@ -398,6 +401,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         const int st = i % C::kStages, kq = i / C::kStages;
                         if (kq >= 1 && !mbar_wait(&bars->empty[st], (kq - 1) & 1, abort_flag)) go = 0;
                         if (go) {
+                            last_issued = i;
                             mbar_arrive_expect_tx(&bars->full[st], bytes);
                             for (int h = 0; h < 2; ++h)
                                 if (pages[h] >= 0) {
@@ -420,6 +424,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                             !mbar_wait(&bars->empty[i % C::kStages], ((i / C::kStages) - 1) & 1, abort_flag))
                             go = 0;
                         if (go) {
+                            last_issued = i;
                             mbar_arrive_expect_tx(&bars->sfull[ss], bytes);
                             for (int h = 0; h < 2; ++h)
                                 if (pages[h] >= 0) {
@@ -442,6 +447,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 }
             }
             cursor_next(c, bt, G);
+        }
+        // The copies this warp issued must have landed before the CTA exits,
+        // also after an abort (their destination is this CTA's shared
+        // memory).  Units are issued in order, so the pending ones are among
+        // the last ring's worth; in a normal run these phases have completed.
+        if (lane == 0) {
+            constexpr int kRing = kMx ? kStgSlots : C::kStages;
+            for (int j = 0; j < kRing; ++j) {
+                const int u = last_issued - j;
+                if (u < 0) break;
+                if (C::kProdWarps > 1 && u % C::kProdWarps != pw) continue;
+                if (kMx) mbar_drain(&bars->sfull[u % kStgSlots], (u / kStgSlots) & 1);
+                else mbar_drain(&bars->full[u % C::kStages], (u / C::kStages) & 1);
+            }
+            for (int gq = q_issued - 1; gq >= 0 && gq >= q_issued - 2; --gq)
+                mbar_drain(&bars->qfull[gq & 1], (gq >> 1) & 1);
         }
         __syncwarp();
     } else if (warp < C::kMmaWarp + C::kMmaWarps) {
@@ -496,9 +517,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             }
         }
         if (lane == 0) {
-            // nothing may still write TMEM when it is released
+            // nothing may still write TMEM when it is released, also after an
+            // abort
             mma_commit(&bars->done);
-            mbar_wait(&bars->done, 0, abort_flag);
+            mbar_drain(&bars->done, 0);
         }
         __syncwarp();
     } else if (warp < C::kEpiWarp0) {

@@ -59,17 +59,31 @@ constexpr long long kWaitCycles = 1ll << 30;
 
 // Wait until the phase with the given parity has completed.  Returns false
 // (and sets *abort) when the budget runs out or another thread aborted.
+template <long long kBudget = kWaitCycles>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > kBudget) {
             *abort = 1;
             return false;
         }
     }
+}
+
+// Wait for work this thread itself put in flight (its MMAs, its copies) to
+// complete before the CTA releases TMEM or exits, also after an abort: the
+// abort flag is not consulted, but the wait is still bounded.  Returns false
+// when the budget ran out.
+template <long long kBudget = kWaitCycles>
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kBudget) return false;
+    }
+    return true;
 }
 
 // ---- proxy fences -----------------------------------------------------------

@@ -159,7 +159,13 @@ struct MlaParams {
     int32_t* status;
 };
 
+// kWaitTest: the variant of the test-only export -- the producers withhold one
+// arrival (the latent slab group 512-575 of the first tile) and every wait has
+// a budget of 2^20 cycles, so the MMA thread's wait runs out and the kernel
+// takes its abort path.
+template <bool kWaitTest>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaParams p) {
+    constexpr long long kBudget = kWaitTest ? (1ll << 20) : kWaitCycles;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -342,13 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 #pragma unroll
             for (int gi = 0; gi < kGroups; ++gi) {
                 const int g = (gi == 0) ? 4 : gi - 1;
-                if (i > 0 && !mbar_wait(&bars->lempty[g], (i - 1) & 1, abort_flag)) {
+                if (i > 0 && !mbar_wait<kBudget>(&bars->lempty[g], (i - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 DSA_MLA_STORE(g)
                 fence_proxy_async_smem();
-                mbar_arrive(&bars->lfull[g]);
+                if (!(kWaitTest && i == 0 && g == 4)) mbar_arrive(&bars->lfull[g]);
                 if (i + 1 < n_tiles) { DSA_MLA_LOAD(i + 1, g) }
             }
         }
@@ -372,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 // S = Q . L^T, slab group by slab group as the producers fill them
 #pragma unroll
                 for (int g = 0; g < kGroups; ++g) {
-                    if (!mbar_wait(&bars->lfull[g], i & 1, abort_flag)) {
+                    if (!mbar_wait<kBudget>(&bars->lfull[g], i & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 mma_commit(&bars->lempty[4]);
                 mma_commit(&bars->sfull);
                 // O^T += V^T . P^T once the softmax has written P
-                if (!mbar_wait(&bars->pfull, i & 1, abort_flag)) break;
+                if (!mbar_wait<kBudget>(&bars->pfull, i & 1, abort_flag)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -403,7 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                     mma_commit(&bars->lempty[c]);
                 }
             }
-            mma_commit(&bars->done);  // also drains whatever is in flight after an abort
+            // TMEM is released only after every MMA issued here has completed,
+            // also after an abort
+            mma_commit(&bars->done);
+            mbar_drain<kBudget>(&bars->done, 0);
         }
         __syncwarp();
     } else {
@@ -411,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         const int h = tid;  // 0..127; rows 96..127 (warp 3) are padding
         float m_ref = -INFINITY, l = 0.f;
         for (int i = 0; i < n_tiles; ++i) {
-            if (!mbar_wait(&bars->sfull, i & 1, abort_flag)) break;
+            if (!mbar_wait<kBudget>(&bars->sfull, i & 1, abort_flag)) break;
             tc_fence_after();
             // S(i) is complete and so is every earlier O^T update; nothing
             // touches O^T again before this thread arrives on pfull
@@ -492,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             mbar_arrive(&bars->pfull);
         }
         // ---------------- end of softmax: per-head normaliser ----------------
-        const bool ok = mbar_wait(&bars->done, 0, abort_flag);
+        const bool ok = mbar_wait<kBudget>(&bars->done, 0, abort_flag);
         tc_fence_after();
         const float scale_out = (p.splits == 1) ? p.kv_scale : 1.f;
         sF[256 + h] = (l > 0.f) ? scale_out / l : 0.f;
@@ -700,7 +709,7 @@ int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool wait_test) {
     if (bt.total_q == 0) return cudaSuccess;
     MlaParams p;
     p.bt = bt;
@@ -719,11 +728,12 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.status = status;
     p.part_o = p.splits > 1 ? reinterpret_cast<__half*>(wsb + w.part_o) : nullptr;
     p.part_lse = p.splits > 1 ? reinterpret_cast<float*>(wsb + w.part_lse) : nullptr;
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    auto kernel = wait_test ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemAlloc);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(sparse_mla_tc_kernel, dim3(bt.total_q * p.splits), dim3(kThreads),
-                      (size_t)kSmemAlloc, stream, pdl, 1, p);
+    e = launch_kernel(kernel, dim3(bt.total_q * p.splits), dim3(kThreads), (size_t)kSmemAlloc,
+                      stream, pdl, 1, p);
     if (e != cudaSuccess || p.splits == 1) return e;
     return launch_kernel(sparse_mla_combine_kernel, dim3(bt.total_q * (kVDim / kCombineDims)),
                          dim3(kCombineThreads), 0, stream, true, 1, (const __half*)p.part_o,

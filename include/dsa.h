@@ -27,7 +27,8 @@
  *     by the caller.  The library allocates nothing, keeps no state between
  *     calls (apart from a launch counter and the fixed scratch array of
  *     dsa_decode_noalloc) and is safe to call from several host threads on
- *     different streams.
+ *     different streams, except dsa_decode_noalloc calls whose executions
+ *     overlap on the GPU (they share that array; see below).
  *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
  *     NULL = legacy default stream).  Argument errors the host can see are
  *     returned before anything is launched; nothing is written then.
@@ -196,9 +197,12 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
  *   - A batch whose dsa_decode_workspace_size() exceeds
  *     DSA_NOALLOC_SCRATCH_BYTES is rejected with DSA_ERR_WORKSPACE before
  *     anything is launched.
- *   - The first call on each device looks up that device's copy of the array
- *     (with the device current); make that first call before any stream
- *     capture on the device.
+ *   - Each call outside stream capture looks up the device address of the
+ *     current device's copy of the array (with that device current); a call
+ *     made while `stream` is capturing uses the address found by the last
+ *     call outside capture.  Make the first call on each device before any
+ *     stream capture on it, and after a cudaDeviceReset make one call outside
+ *     capture before capturing again (the reset may move the array).
  *   - Every GPU that loads the library holds the array until the process exits.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents; nothing in it needs to start at zero.  Calls whose executions
@@ -226,6 +230,36 @@ dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,
                             const float* new_latent, float kv_scale, void* index_pages,
                             void* latent_pages, dsa_key_format key_format,
                             int32_t* dev_status, dsa_stream_t stream);
+
+/* ---- token-sharded prefill planner (host only) ----------------------------------
+ * Section "Token-sharded prefill improves time to first token": for a large
+ * prefill step each rank of W runs the indexer and sparse MLA for a share of
+ * the query tokens (all 96 heads) instead of a share of the heads; to balance
+ * causal work every request is cut into 2W parts (16 for W = 8) and rank r
+ * takes parts r and 2W - 1 - r.  Part i of a request with n new tokens is its
+ * tokens [floor(i n / 2W), floor((i + 1) n / 2W)).
+ * Each part is returned as a sub-request for a dsa_batch of the rank: its
+ * tokens are the batch's query tokens token_begin .. token_begin + num_tokens
+ * - 1 (indices into the original batch, whose request b holds q_counts[b]
+ * tokens in order), its context ends at its last token (seq_len), and its
+ * block-table row is that of `request`.  With that context the step's causal
+ * rule gives every token exactly the positions it sees in the whole request,
+ * so the rank's results for its tokens equal the unsharded step's.
+ *   seq_lens, q_counts  host [num_requests]: context (incl. new tokens), new tokens
+ *   parts               host output, up to max_parts entries (2 per request at
+ *                       most; empty parts are skipped)
+ * Returns the number of parts written, or a negated dsa_status:
+ * -DSA_ERR_INVALID_ARG for bad sizes, -DSA_ERR_WORKSPACE when max_parts is
+ * too small.  Pure host code: no device, stream or allocation. */
+typedef struct {
+    int32_t request;      /* index of the original request */
+    int32_t token_begin;  /* first query token of the part, in the original batch */
+    int32_t num_tokens;   /* query tokens in the part (> 0) */
+    int32_t seq_len;      /* the part's context: position of its last token + 1 */
+} dsa_shard_part;
+int32_t dsa_plan_token_shards(const int32_t* seq_lens, const int32_t* q_counts,
+                              int32_t num_requests, int32_t world, int32_t rank,
+                              dsa_shard_part* parts, int32_t max_parts);
 
 #ifdef __cplusplus
 }

@@ -5,8 +5,11 @@ cudaMalloc/cudaFree).  Its scratch is a fixed array inside the library instead
 of a caller workspace.
 
 Checked through the C ABI against dsa_decode on the same inputs, at the
-tolerances of the other parity tests, on two calls in a row (the second call
-reuses the array with the first call's contents still in it).  The file name
+tolerances of the other parity tests, on calls in a row (each later call
+reuses the array with the earlier calls' contents still in it).  The last
+batch (one query token over a 40,000-position context) takes the split-row
+top-k, whose histograms and counters live in the shared array and must be
+cleared by every call.  The file name
 puts it last in collection order; it also passes on its own in a fresh
 process."""
 import numpy as np
@@ -31,12 +34,13 @@ def _noalloc(gl, status):
     return out, lse, idx
 
 
-def test_noalloc_matches_decode_on_two_calls_in_a_row():
+def test_noalloc_matches_decode_on_calls_in_a_row():
     layers = [di.make_layer([20000, 9000, 31000], [1, 3, 1], seed=71, extra_pages=2),
-              di.make_layer([4096, 2500, 17000], [2, 1, 1], seed=72, extra_pages=1)]
+              di.make_layer([4096, 2500, 17000], [2, 1, 1], seed=72, extra_pages=1),
+              di.make_layer([40000], [1], seed=73, extra_pages=3)]
     assert all(dsa.dsa_decode_workspace_size(GpuLayer(l).batch) <= dsa.NOALLOC_SCRATCH_BYTES
                for l in layers)
-    for layer in layers:  # two different batches, back to back on one stream
+    for layer in layers:  # different batches, back to back on one stream
         gl = GpuLayer(layer)
         ref_out, ref_lse, ref_idx = gl.decode()
         st = gl.status()
