@@ -72,9 +72,20 @@ def lib():
         L.oracle_append_cache.argtypes = [
             ctypes.c_int32, _i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
             _f32p, _f32p, ctypes.c_float, _u8p, _u8p, ctypes.c_int32]
+        L.oracle_bf16_encode.restype = ctypes.c_uint16
+        L.oracle_bf16_encode.argtypes = [ctypes.c_float]
+        L.oracle_bf16_encode_array.argtypes = [_f32p, _u16p, ctypes.c_int64]
+        L.oracle_dcp_topk_row.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_int32, _i32p, _i32p]
+        L.oracle_dcp_topk.argtypes = [_f32p, ctypes.c_int64, _i64p, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
+                                      _i32p]
+        L.oracle_lse_combine.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _f64p,
+                                         _f64p, _f64p, _f64p]
         for name in ("oracle_index_scores", "oracle_topk_row", "oracle_topk", "oracle_visible",
                      "oracle_sparse_mla", "oracle_decode", "oracle_append_cache",
-                     "oracle_constants"):
+                     "oracle_constants", "oracle_dcp_topk_row", "oracle_dcp_topk",
+                     "oracle_lse_combine"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -280,3 +291,53 @@ def append_cache(batch, new_keys, new_latent, kv_scale, index_pages, latent_page
                                      None if lp is None else _p(lp, ctypes.c_uint8),
                                      int(key_format)), "append_cache")
     return ip, lp
+
+
+# ---- decode context parallelism ------------------------------------------------
+
+def bf16_encode(values):
+    """bfloat16 codes (round to nearest even) of binary32 values."""
+    a = _arr(values, np.float32).reshape(-1)
+    out = np.empty(a.size, np.uint16)
+    lib().oracle_bf16_encode_array(_p(a, ctypes.c_float), _p(out, ctypes.c_uint16), a.size)
+    return out.reshape(np.shape(values))
+
+
+def dcp_cand(world, k=2048):
+    """Candidates each rank sends: ceil(1.5 k / world)."""
+    return -(-3 * k // (2 * world))
+
+
+def dcp_topk(scores, n_visible, world, cand=None, k=2048):
+    """Row-wise merged selection of decode context parallelism over `world`
+    ranks (rank r holds positions s = r mod world): the k visible positions
+    with the largest BF16-rounded scores, ties to the lower position, in
+    ascending order, -1 padded; and per row which ranks resend their full local
+    top-k.  scores: [rows, ld] binary32 (the scores as computed)."""
+    s = _arr(scores, np.float32)
+    if s.ndim == 1:
+        s = s.reshape(1, -1)
+    nv = _arr(np.atleast_1d(n_visible), np.int64)
+    cand = dcp_cand(world, k) if cand is None else int(cand)
+    out = np.empty((s.shape[0], k), np.int32)
+    resend = np.empty((s.shape[0], world), np.int32)
+    _check(lib().oracle_dcp_topk(_p(s, ctypes.c_float), s.shape[1], _p(nv, ctypes.c_int64),
+                                 s.shape[0], int(world), cand, int(k), _p(out, ctypes.c_int32),
+                                 _p(resend, ctypes.c_int32)), "dcp_topk")
+    return out, resend
+
+
+def lse_combine(parts, lses):
+    """Log-sum-exp combine of partial attention results over disjoint token
+    sets: parts [world, ..., dim], lses [world, ...] (natural log)."""
+    p = _arr(parts, np.float64)
+    l = _arr(lses, np.float64)
+    world = p.shape[0]
+    dim = p.shape[-1]
+    rows = int(np.prod(p.shape[1:-1])) if p.ndim > 2 else 1
+    out = np.empty((rows, dim), np.float64)
+    lse = np.empty(rows, np.float64)
+    _check(lib().oracle_lse_combine(world, rows, dim, _p(p, ctypes.c_double),
+                                    _p(l, ctypes.c_double), _p(out, ctypes.c_double),
+                                    _p(lse, ctypes.c_double)), "lse_combine")
+    return out.reshape(p.shape[1:]), lse.reshape(l.shape[1:])
