@@ -15,7 +15,8 @@ __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path"
            "dsa_status_string", "dsa_launch_count", "dsa_index_scores", "dsa_topk",
            "dsa_topk_workspace_size", "dsa_sparse_mla", "dsa_sparse_mla_workspace_size",
            "dsa_decode", "dsa_decode_workspace_size", "dsa_decode_noalloc",
-           "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards"]
+           "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards",
+           "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "dsa_lse_combine"]
 
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
@@ -77,6 +78,10 @@ _SIGS = {
     "dsa_decode_noalloc": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32,
                                           _f32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dsa_append_cache": (ctypes.c_int, [_bp, _vp, _vp, _f32, _vp, _vp, ctypes.c_int, _vp, _vp]),
+    "dsa_dcp_topk_workspace_size": (_sz, [_bp, _i32, _i32, _i32]),
+    "dsa_dcp_topk": (ctypes.c_int, [_bp, _vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
+                                    _vp]),
+    "dsa_lse_combine": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dsa_plan_token_shards": (ctypes.c_int32, [ctypes.POINTER(ctypes.c_int32),
                                                ctypes.POINTER(ctypes.c_int32), _i32, _i32, _i32,
                                                ctypes.POINTER(ShardPart), _i32]),
@@ -269,6 +274,31 @@ def dsa_decode_noalloc(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat,
                                    _ptr(indices, torch.int32, "indices"),
                                    _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(rc, "dsa_decode_noalloc")
+
+
+def dsa_dcp_topk_workspace_size(batch, world, cand=0, topk=TOPK):
+    return int(load().dsa_dcp_topk_workspace_size(batch.ref(), int(world), int(cand), int(topk)))
+
+
+def dsa_dcp_topk(batch, scores, score_ld, world, cand, topk, indices, rank_indices=None,
+                 resent=None, ws=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().dsa_dcp_topk(batch.ref(), _ptr(scores, torch.float32, "scores"), int(score_ld),
+                             int(world), int(cand), int(topk),
+                             _ptr(indices, torch.int32, "indices"),
+                             _ptr(rank_indices, torch.int32, "rank_indices"),
+                             _ptr(resent, torch.int32, "resent"), _ptr(ws), nbytes,
+                             _stream(stream))
+    _check(rc, "dsa_dcp_topk")
+
+
+def dsa_lse_combine(total_q, world, part_out, part_lse, out, lse=None, stream=None):
+    rc = load().dsa_lse_combine(int(total_q), int(world),
+                                _ptr(part_out, (torch.bfloat16, torch.int16), "part_out"),
+                                _ptr(part_lse, torch.float32, "part_lse"),
+                                _ptr(out, (torch.bfloat16, torch.int16), "out"),
+                                _ptr(lse, torch.float32, "lse"), _stream(stream))
+    _check(rc, "dsa_lse_combine")
 
 
 def dsa_plan_token_shards(seq_lens, q_counts, world, rank):

@@ -26,6 +26,18 @@ cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const fl
                                 float kv_scale, void* index_pages, void* latent_pages,
                                 int32_t* status, cudaStream_t stream);
 
+int dcp_default_cand(int world, int K);
+struct DcpWs {
+    size_t sent, sent_n, full, full_n, flags, total;
+};
+DcpWs dcp_ws_layout(int total_q, int world, int cand, int K);
+bool dcp_supported(int world, int max_seq);
+cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld, int world,
+                            int cand, int K, int32_t* indices, int32_t* rank_indices,
+                            int32_t* resent, void* ws, cudaStream_t stream);
+cudaError_t launch_lse_combine(int total_q, int world, const uint16_t* part, const float* part_lse,
+                               uint16_t* out, float* lse, cudaStream_t stream);
+
 std::atomic<uint64_t> g_launches{0};
 }  // namespace dsa
 
@@ -224,6 +236,50 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
                               base + off_mla, dev_status, true, s);
     return cuda_status(e);
+}
+
+size_t dsa_dcp_topk_workspace_size(const dsa_batch* batch, int32_t world, int32_t cand,
+                                   int32_t topk) {
+    if (check_batch(batch) != DSA_OK || topk != kTopK || world < 1 || world > 8) return 0;
+    if (cand == 0) cand = dcp_default_cand(world, topk);
+    if (cand < 1 || cand > topk) return 0;
+    return dcp_ws_layout(batch->total_q, world, cand, topk).total;
+}
+
+dsa_status dsa_dcp_topk(const dsa_batch* batch, const float* scores, int64_t score_ld,
+                        int32_t world, int32_t cand, int32_t topk, int32_t* indices,
+                        int32_t* rank_indices, int32_t* resent, void* ws, size_t ws_bytes,
+                        dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (topk != kTopK) return DSA_ERR_UNSUPPORTED;
+    if (world < 1 || world > 8) return DSA_ERR_UNSUPPORTED;
+    if (cand == 0) cand = dcp_default_cand(world, topk);
+    if (cand < 1 || cand > topk) return DSA_ERR_INVALID_ARG;
+    if (!dcp_supported(world, batch->max_seq_len)) return DSA_ERR_UNSUPPORTED;
+    if (!scores || !indices || !aligned16(scores) || !aligned16(indices)) return DSA_ERR_INVALID_ARG;
+    if ((rank_indices && !aligned16(rank_indices)) || (resent && !aligned16(resent)))
+        return DSA_ERR_INVALID_ARG;
+    if (score_ld < batch->max_seq_len || (score_ld % 4) != 0) return DSA_ERR_INVALID_ARG;
+    const size_t need = dsa_dcp_topk_workspace_size(batch, world, cand, topk);
+    if (!ws || !aligned16(ws) || ws_bytes < need) return DSA_ERR_WORKSPACE;
+    if (batch->total_q == 0) return DSA_OK;
+    g_launches.fetch_add(4, std::memory_order_relaxed);
+    return cuda_status(launch_dcp_topk(to_args(batch), scores, score_ld, world, cand, topk,
+                                       indices, rank_indices, resent, ws, (cudaStream_t)stream));
+}
+
+dsa_status dsa_lse_combine(int32_t total_q, int32_t world, const uint16_t* part_out,
+                           const float* part_lse, uint16_t* out, float* lse,
+                           dsa_stream_t stream) {
+    if (total_q < 0) return DSA_ERR_INVALID_ARG;
+    if (world < 1 || world > 8) return DSA_ERR_UNSUPPORTED;
+    if (!part_out || !part_lse || !out || !aligned16(part_out) || !aligned16(out))
+        return DSA_ERR_INVALID_ARG;
+    if (total_q == 0) return DSA_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(launch_lse_combine(total_q, world, part_out, part_lse, out, lse,
+                                          (cudaStream_t)stream));
 }
 
 dsa_status dsa_test_sparse_mla_wait_timeout(const dsa_batch* batch, const uint16_t* q_lat,

@@ -1,0 +1,487 @@
+// dcp.cu -- decode context parallelism (DCP) for the sparse indexer, emulated
+// on one GPU: the exact one-round top-k merge and the log-sum-exp combine.
+//
+// "vLLM's Kimi K3.1 Pro day-0 support", section "Decode context parallelism
+// with the sparse indexer": with DCP over W ranks, rank r stores every W-th
+// token (positions s = r mod W) and ranks only its own tokens, so the global
+// top-2048 must be merged across ranks before attention, and the partial
+// attention outputs are combined by log-sum-exp.  Section "Exact top-k merge
+// with about 10x less traffic": each rank selects its best ceil(1.5 * 2048 /
+// W) candidates directly from BF16 scores and packs each with its score into
+// 32 bits; every rank radix-selects the same global top-2048 from the gathered
+// candidates; a rank holding more of the top-2048 than it sent is detected by
+// that selection and resends its full local top-k for the row.
+//
+// Here the W ranks' shards are the interleaved positions of one score row on
+// one GPU, and an exchange buffer in device memory stands for what the ranks
+// put on the wire.  A candidate word is (k << 16) | i: k = the order-preserving
+// 16-bit key of the BF16-rounded score, i = the position within the rank's
+// shard (s = i * W + r).  The merged order is BF16 score descending, position
+// ascending.
+//
+// Kernels (launched in this order, each one CTA per query row):
+//   dcp_candidates_kernel<false>  every rank's top `cand` (radix select on
+//                                 (k << 16) | (0xFFFF - i), four 8-bit levels)
+//   dcp_merge_kernel<false>       the top-k of the gathered candidates (radix
+//                                 select on 48-bit (k, ~s) keys in shared
+//                                 memory); a rank all of whose candidates are
+//                                 selected while it holds more tokens is
+//                                 flagged; a row without flags is final
+//   dcp_candidates_kernel<true>   flagged ranks only: their local top-k
+//   dcp_merge_kernel<true>        flagged rows only: the top-k of the flagged
+//                                 ranks' full lists and the others' candidates
+// A rank that is not flagged has its lowest candidate outside the top-k of a
+// subset of all tokens, hence outside the global top-k, and so are its unsent
+// tokens (they rank below that candidate); so the second selection is exact.
+#include <climits>
+
+#include "common.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kDcpThreads = 1024;
+constexpr int kDcpMaxWorld = 8;
+constexpr int kDcpMaxCand = kDcpMaxWorld * kTopK;  // 16384 gathered words, at most
+
+// Order-preserving 16-bit key of a score rounded to BF16 (round to nearest
+// even), -0 folded onto +0.
+__device__ __forceinline__ uint32_t bf16_key(float f) {
+    uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    if (b == 0x8000u) b = 0u;
+    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+
+struct DcpArgs {
+    BatchArgs bt;
+    const float* scores;
+    int64_t ld;
+    int world;
+    int cand;               // candidates per rank
+    int K;                  // selected per row
+    uint32_t* sent;         // [T][W][cand]
+    int32_t* sent_n;        // [T][W]
+    uint32_t* full;         // [T][W][K]  flagged ranks' local top-k
+    int32_t* full_n;        // [T][W]
+    int32_t* flags;         // [T][W]
+    int32_t* indices;       // [T][K]
+    int32_t* rank_indices;  // [W][T][K] or null
+    int32_t* resent;        // [T][W] or null
+};
+
+// Warp-wide, over hist[0..256): the digit d with count(> d) < need <=
+// count(>= d), and count(> d); returned to every lane.  Lane l sums bins
+// 255-8l .. 248-8l (descending digits), then a warp scan locates the lane.
+__device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t need, int lane,
+                                           uint32_t& digit, uint32_t& above) {
+    uint32_t v[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        v[j] = hist[255 - 8 * lane - j];
+        sum += v[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const uint32_t excl = incl - sum;
+    const uint32_t ballot = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+    const int src = ballot ? __ffs(ballot) - 1 : 0;
+    uint32_t d = 0, c = excl;
+    if (lane == src) {
+        int j = 0;
+        while (j < 7 && c + v[j] < need) c += v[j++];
+        d = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+    }
+    digit = __shfl_sync(0xffffffffu, d, src);
+    above = __shfl_sync(0xffffffffu, c, src);
+}
+
+// Local top-C of every rank of row t (kResend: only flagged ranks, C = K).
+template <bool kResend>
+__global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpArgs a) {
+    __shared__ uint32_t s_hist[kDcpMaxWorld][256];
+    __shared__ uint32_t s_prefix[kDcpMaxWorld];
+    __shared__ uint32_t s_need[kDcpMaxWorld];
+    __shared__ int s_cnt[kDcpMaxWorld];
+    __shared__ int s_mode[kDcpMaxWorld];  // 0: idle, 1: radix select, 2: take all
+    const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int W = a.world;
+    const int C = kResend ? a.K : a.cand;
+    const int b = request_of(a.bt, t);
+    if (!token_ok(a.bt, b, t, nullptr)) return;
+    const int vis = visible_of(a.bt, b, t);
+    const float* row = a.scores + (int64_t)t * a.ld;
+    if (tid < W) {
+        const int r = tid;
+        const int n_r = vis > r ? (vis - 1 - r) / W + 1 : 0;
+        const int c = min(C, n_r);
+        const bool on = !kResend || a.flags[(int64_t)t * W + r] != 0;
+        s_mode[r] = !on ? 0 : (c == n_r ? 2 : 1);
+        s_prefix[r] = 0u;
+        s_need[r] = (uint32_t)c;
+        s_cnt[r] = 0;
+        if (on) (kResend ? a.full_n : a.sent_n)[(int64_t)t * W + r] = c;
+    }
+    __syncthreads();
+    bool any = false, radix = false;
+    for (int r = 0; r < W; ++r) {
+        any |= s_mode[r] != 0;
+        radix |= s_mode[r] == 1;
+    }
+    if (!any) return;
+    // radix select on comp = (k << 16) | (0xFFFF - i): the C largest are the
+    // best C of the rank (larger score, then lower position); the composite
+    // is unique per token, so the C-th largest, tau, selects exactly C
+    for (int level = 0; radix && level < 4; ++level) {
+        const int shift = 24 - 8 * level;
+        const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+        for (int i = tid; i < W * 256; i += kDcpThreads) (&s_hist[0][0])[i] = 0u;
+        __syncthreads();
+        for (int s = tid; s < vis; s += kDcpThreads) {
+            const int r = s % W;
+            if (s_mode[r] != 1) continue;
+            const uint32_t comp = (bf16_key(__ldcg(row + s)) << 16) | (0xFFFFu - (uint32_t)(s / W));
+            if ((comp & hi_mask) == (s_prefix[r] & hi_mask))
+                atomicAdd(&s_hist[r][(comp >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp < W && s_mode[warp] == 1) {
+            uint32_t d, above;
+            find_digit(s_hist[warp], s_need[warp], lane, d, above);
+            if (lane == 0) {
+                s_prefix[warp] |= d << shift;
+                s_need[warp] -= above;
+            }
+        }
+        __syncthreads();
+    }
+    // output: every token of an active rank with comp >= tau (tau = 0 takes all)
+    uint32_t* out = kResend ? a.full : a.sent;
+    const int stride = kResend ? a.K : a.cand;
+    for (int s = tid; s < vis; s += kDcpThreads) {
+        const int r = s % W;
+        if (s_mode[r] == 0) continue;
+        const uint32_t i = (uint32_t)(s / W);
+        const uint32_t k = bf16_key(__ldcg(row + s));
+        const uint32_t comp = (k << 16) | (0xFFFFu - i);
+        const uint32_t tau = s_mode[r] == 2 ? 0u : s_prefix[r];
+        if (comp >= tau) {
+            const int slot = atomicAdd(&s_cnt[r], 1);
+            if (slot < stride) out[((int64_t)t * W + r) * stride + slot] = (k << 16) | i;
+        }
+    }
+}
+
+// Block-wide exclusive scan of one int per thread (1024 threads); returns the
+// exclusive prefix and sets *total.
+__device__ __forceinline__ int block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int x = s_warp[lane];
+        int wi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        s_warp[lane] = wi - x;
+        if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    const int r = s_warp[warp] + incl - v;
+    *total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+struct MergeSmem {
+    unsigned long long cand[kDcpMaxCand];  // (k << 32) | (0xFFFFFFFF - s)
+    int pos[kTopK];                        // selected positions, sorted
+    uint32_t hist[256];
+    int warp_tot[33];
+    int off[kDcpMaxWorld + 1];
+    int taken[kDcpMaxWorld];
+    int flag[kDcpMaxWorld];
+    unsigned long long prefix;
+    uint32_t need;
+    int count;
+    int any_flag;
+};
+
+// Top-K of the gathered candidates of row t.  Round 1 (kSecond = false): all
+// ranks' candidates; ranks whose candidates were all selected while they hold
+// more tokens are flagged, and a row without flags writes its outputs.
+// Round 2: rows with flags, flagged ranks contributing their local top-K.
+template <bool kSecond>
+__global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    MergeSmem& sm = *reinterpret_cast<MergeSmem*>(smem_raw);
+    const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int W = a.world;
+    const int b = request_of(a.bt, t);
+    if (!token_ok(a.bt, b, t, nullptr)) return;
+    const int vis = visible_of(a.bt, b, t);
+    if (tid == 0) {
+        int any = 0, o = 0;
+        for (int r = 0; r < W; ++r) {
+            const int f = kSecond ? a.flags[(int64_t)t * W + r] : 0;
+            sm.flag[r] = f;
+            any |= f;
+            sm.off[r] = o;
+            o += f ? a.full_n[(int64_t)t * W + r] : a.sent_n[(int64_t)t * W + r];
+            sm.taken[r] = 0;
+        }
+        sm.off[W] = o;
+        sm.any_flag = any;
+        sm.prefix = 0ull;
+        sm.count = 0;
+    }
+    __syncthreads();
+    if (kSecond && !sm.any_flag) return;  // final after round 1
+    const int N = sm.off[W];
+    // gather the candidate words into (k << 32) | ~s keys
+    for (int r = 0; r < W; ++r) {
+        const int n = sm.off[r + 1] - sm.off[r];
+        const uint32_t* src = sm.flag[r] ? a.full + ((int64_t)t * W + r) * a.K
+                                         : a.sent + ((int64_t)t * W + r) * a.cand;
+        for (int j = tid; j < n; j += kDcpThreads) {
+            const uint32_t w = __ldcg(src + j);
+            const uint32_t s = (w & 0xFFFFu) * (uint32_t)W + (uint32_t)r;
+            sm.cand[sm.off[r] + j] = ((unsigned long long)(w >> 16) << 32) | (0xFFFFFFFFu - s);
+        }
+    }
+    const int K = min(a.K, N);
+    if (tid == 0) sm.need = (uint32_t)K;
+    __syncthreads();
+    // radix select of the K-th largest over 48 bits (six 8-bit levels);
+    // keys are unique, so exactly K keys are >= it
+    if (K < N) {
+        for (int level = 0; level < 6; ++level) {
+            const int shift = 40 - 8 * level;
+            const unsigned long long hi_mask = level == 0 ? 0ull : (~0ull << (shift + 8));
+            if (tid < 256) sm.hist[tid] = 0u;
+            __syncthreads();
+            for (int j = tid; j < N; j += kDcpThreads) {
+                const unsigned long long c = sm.cand[j];
+                if ((c & hi_mask) == (sm.prefix & hi_mask)) atomicAdd(&sm.hist[(c >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t d, above;
+                find_digit(sm.hist, sm.need, lane, d, above);
+                if (lane == 0) {
+                    sm.prefix |= (unsigned long long)d << shift;
+                    sm.need -= above;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    const unsigned long long tau = K < N ? sm.prefix : 0ull;
+    for (int j = tid; j < N; j += kDcpThreads) {
+        const unsigned long long c = sm.cand[j];
+        if (c >= tau) {
+            const int s = (int)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
+            const int slot = atomicAdd(&sm.count, 1);
+            if (slot < kTopK) sm.pos[slot] = s;
+            if (!kSecond) atomicAdd(&sm.taken[s % W], 1);
+        }
+    }
+    __syncthreads();
+    if (!kSecond) {
+        if (tid == 0) {
+            int any = 0;
+            for (int r = 0; r < W; ++r) {
+                const int n_r = vis > r ? (vis - 1 - r) / W + 1 : 0;
+                const int sr = sm.off[r + 1] - sm.off[r];
+                const int f = (sr > 0 && sm.taken[r] == sr && n_r > sr) ? 1 : 0;
+                a.flags[(int64_t)t * W + r] = f;
+                if (a.resent) a.resent[(int64_t)t * W + r] = f;
+                any |= f;
+            }
+            sm.any_flag = any;
+        }
+        __syncthreads();
+        if (sm.any_flag) return;  // round 2 finishes this row
+    }
+    // the K positions in ascending order: bitonic sort of 2048 (padded)
+    for (int j = K + tid; j < kTopK; j += kDcpThreads) sm.pos[j] = INT_MAX;
+    __syncthreads();
+    for (int size = 2; size <= kTopK; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int j = tid; j < kTopK / 2; j += kDcpThreads) {
+                const int lo = 2 * j - (j & (stride - 1));
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const int x = sm.pos[lo], y = sm.pos[hi];
+                if ((x > y) == up) {
+                    sm.pos[lo] = y;
+                    sm.pos[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int j = tid; j < a.K; j += kDcpThreads)
+        a.indices[(int64_t)t * a.K + j] = j < K ? sm.pos[j] : -1;
+    if (a.rank_indices) {
+        // each rank's share of the selection, ascending, -1 padded
+        constexpr int kPer = kTopK / kDcpThreads;  // 2 positions per thread
+        for (int r = 0; r < W; ++r) {
+            int mine = 0;
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int j = kPer * tid + u;
+                mine += (j < K && sm.pos[j] % W == r);
+            }
+            int total;
+            int o = block_scan(mine, sm.warp_tot, &total);
+            int32_t* dst = a.rank_indices + ((int64_t)r * a.bt.total_q + t) * a.K;
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int j = kPer * tid + u;
+                if (j < K && sm.pos[j] % W == r) dst[o++] = sm.pos[j];
+            }
+            for (int j = total + tid; j < a.K; j += kDcpThreads) dst[j] = -1;
+        }
+    }
+}
+
+// out[t,h,:] = sum_r exp(lse_r - L) part_r[t,h,:], L = log sum_r exp(lse_r);
+// thread = (row (t, h), 8 dims): one 16-byte load per rank, all in flight.
+constexpr int kCombThreads = 128;  // two (t, h) rows per block
+__global__ void __launch_bounds__(kCombThreads)
+dcp_lse_combine_kernel(int total_q, int world, const __nv_bfloat16* __restrict__ part,
+                       const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
+                       float* __restrict__ lse) {
+    const int64_t rows = (int64_t)total_q * kMlaHeads;
+    const int64_t row = (int64_t)blockIdx.x * 2 + (threadIdx.x >> 6);
+    if (row >= rows) return;
+    const int d0 = 8 * (threadIdx.x & 63);
+    float l[kDcpMaxWorld];
+    uint4 v[kDcpMaxWorld];
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kDcpMaxWorld; ++r) {
+        l[r] = r < world ? __ldg(part_lse + (int64_t)r * rows + row) : -INFINITY;
+        v[r] = r < world ? __ldg(reinterpret_cast<const uint4*>(part + ((int64_t)r * rows + row) * kVDim + d0))
+                         : make_uint4(0u, 0u, 0u, 0u);
+        M = fmaxf(M, l[r]);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float tot = 0.f;
+    if (M > -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kDcpMaxWorld; ++r) {
+            const float wgt = __expf(l[r] - M);  // 0 for an absent or empty rank
+            tot += wgt;
+            const uint32_t wv[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[2 * k] = fmaf(wgt, __uint_as_float(wv[k] << 16), acc[2 * k]);
+                acc[2 * k + 1] = fmaf(wgt, __uint_as_float(wv[k] & 0xFFFF0000u), acc[2 * k + 1]);
+            }
+        }
+    }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 p2 = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+        o[k] = *reinterpret_cast<const uint32_t*>(&p2);
+    }
+    *reinterpret_cast<uint4*>(out + row * kVDim + d0) = make_uint4(o[0], o[1], o[2], o[3]);
+    if (lse && d0 == 0) lse[row] = tot > 0.f ? M + __logf(tot) : -INFINITY;
+}
+
+}  // namespace
+
+// ceil(1.5 K / W), capped at K (a rank never needs to send more than K)
+int dcp_default_cand(int world, int K) {
+    const int c = (3 * K + 2 * world - 1) / (2 * world);
+    return c < K ? c : K;
+}
+
+struct DcpWs {
+    size_t sent, sent_n, full, full_n, flags, total;
+};
+
+DcpWs dcp_ws_layout(int total_q, int world, int cand, int K) {
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    const size_t tw = (size_t)total_q * world;
+    DcpWs w;
+    w.sent = 0;
+    w.sent_n = up(tw * cand * 4);
+    w.full = w.sent_n + up(tw * 4);
+    w.full_n = w.full + up(tw * (size_t)K * 4);
+    w.flags = w.full_n + up(tw * 4);
+    w.total = w.flags + up(tw * 4);
+    return w;
+}
+
+bool dcp_supported(int world, int max_seq) {
+    return world >= 1 && world <= kDcpMaxWorld && (int64_t)max_seq <= (int64_t)65536 * world;
+}
+
+cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld, int world,
+                            int cand, int K, int32_t* indices, int32_t* rank_indices,
+                            int32_t* resent, void* ws, cudaStream_t stream) {
+    if (bt.total_q == 0) return cudaSuccess;
+    const DcpWs w = dcp_ws_layout(bt.total_q, world, cand, K);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    DcpArgs a;
+    a.bt = bt;
+    a.scores = scores;
+    a.ld = ld;
+    a.world = world;
+    a.cand = cand;
+    a.K = K;
+    a.sent = reinterpret_cast<uint32_t*>(base + w.sent);
+    a.sent_n = reinterpret_cast<int32_t*>(base + w.sent_n);
+    a.full = reinterpret_cast<uint32_t*>(base + w.full);
+    a.full_n = reinterpret_cast<int32_t*>(base + w.full_n);
+    a.flags = reinterpret_cast<int32_t*>(base + w.flags);
+    a.indices = indices;
+    a.rank_indices = rank_indices;
+    a.resent = resent;
+    const size_t msmem = sizeof(MergeSmem);
+    cudaError_t e = cudaFuncSetAttribute(dcp_merge_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(dcp_merge_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    const dim3 grid((unsigned)bt.total_q);
+    if (e == cudaSuccess)
+        e = launch_kernel(dcp_candidates_kernel<false>, grid, dim3(kDcpThreads), 0, stream, false, 1, a);
+    if (e == cudaSuccess)
+        e = launch_kernel(dcp_merge_kernel<false>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
+    if (e == cudaSuccess)
+        e = launch_kernel(dcp_candidates_kernel<true>, grid, dim3(kDcpThreads), 0, stream, false, 1, a);
+    if (e == cudaSuccess)
+        e = launch_kernel(dcp_merge_kernel<true>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
+    return e;
+}
+
+cudaError_t launch_lse_combine(int total_q, int world, const uint16_t* part, const float* part_lse,
+                               uint16_t* out, float* lse, cudaStream_t stream) {
+    const int64_t rows = (int64_t)total_q * kMlaHeads;
+    if (rows == 0) return cudaSuccess;
+    return launch_kernel(dcp_lse_combine_kernel, dim3((unsigned)((rows + 1) / 2)),
+                         dim3(kCombThreads), 0, stream, false, 1, total_q, world,
+                         reinterpret_cast<const __nv_bfloat16*>(part), part_lse,
+                         reinterpret_cast<__nv_bfloat16*>(out), lse);
+}
+
+}  // namespace dsa

@@ -231,6 +231,58 @@ dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,
                             void* latent_pages, dsa_key_format key_format,
                             int32_t* dev_status, dsa_stream_t stream);
 
+/* ---- decode context parallelism: exact top-k merge and LSE combine ---------------
+ * Section "Decode context parallelism with the sparse indexer": with DCP over
+ * W ranks, rank r holds every W-th token (positions s = r mod W) and ranks only
+ * its own tokens, so the global top-2048 is merged across ranks before
+ * attention, and the ranks' partial attention outputs are combined by
+ * log-sum-exp.  Section "Exact top-k merge with about 10x less traffic": each
+ * rank sends its best ceil(1.5 * 2048 / W) candidates, chosen from BF16
+ * scores and packed with the score into 32 bits; every rank radix-selects the
+ * same global top-2048 from the gathered candidates; a rank holding more of
+ * it than it sent is detected and resends its full local top-k for that row.
+ *
+ * dsa_dcp_topk runs that protocol for all W ranks of each query row on one
+ * GPU, the ranks' shards being the interleaved positions of the row in
+ * `scores` (as dsa_index_scores writes them) and the exchange going through
+ * the workspace.  Result: for each query token t, the topk visible positions
+ * with the largest BF16-rounded scores (round to nearest even), ties to the
+ * lower position, in ascending order, -1 padded -- exactly, whatever the
+ * distribution of winners over ranks.
+ *   world         W, 1..8
+ *   cand          candidates per rank, 1..topk; 0 = min(ceil(1.5 * topk / W), topk)
+ *   indices       [T, topk] int32 output
+ *   rank_indices  [W, T, topk] int32 output (may be NULL): rank r's share of
+ *                 the selection (the positions with s mod W == r), ascending,
+ *                 -1 padded -- the index list rank r attends over
+ *   resent        [T, W] int32 output (may be NULL): 1 where rank r had to
+ *                 resend its local top-k for the row, else 0
+ *   ws            device scratch of dsa_dcp_topk_workspace_size() bytes (the
+ *                 exchanged candidate words and resend lists), 16-byte aligned
+ * The packed word keeps a rank-local position in 16 bits, so max_seq_len must
+ * be at most 65536 * W (DSA_ERR_UNSUPPORTED otherwise).  topk must be 2048.
+ * Scores must not be NaN.  Four kernel launches. */
+size_t dsa_dcp_topk_workspace_size(const dsa_batch* batch, int32_t world, int32_t cand,
+                                   int32_t topk);
+dsa_status dsa_dcp_topk(const dsa_batch* batch, const float* scores, int64_t score_ld,
+                        int32_t world, int32_t cand, int32_t topk, int32_t* indices,
+                        int32_t* rank_indices, int32_t* resent, void* ws, size_t ws_bytes,
+                        dsa_stream_t stream);
+
+/* The log-sum-exp combine of W partial attention results over disjoint token
+ * sets (for instance the outputs of dsa_sparse_mla over each rank's
+ * rank_indices):
+ *   L = log sum_r exp(part_lse[r,t,h]),
+ *   out[t,h,:] = sum_r exp(part_lse[r,t,h] - L) * part_out[r,t,h,:]
+ *   part_out  [W, T, 96, 512] bf16 (16-byte aligned)
+ *   part_lse  [W, T, 96] fp32, natural log; -inf for a rank with no tokens
+ *   out       [T, 96, 512] bf16 output; lse [T, 96] fp32 output (may be NULL)
+ * A (t, h) with no tokens on any rank gives out = 0 and lse = -inf.
+ * world must be 1..8. */
+dsa_status dsa_lse_combine(int32_t total_q, int32_t world, const uint16_t* part_out,
+                           const float* part_lse, uint16_t* out, float* lse,
+                           dsa_stream_t stream);
+
 /* ---- token-sharded prefill planner (host only) ----------------------------------
  * Section "Token-sharded prefill improves time to first token": for a large
  * prefill step each rank of W runs the indexer and sparse MLA for a share of

@@ -304,8 +304,9 @@ def bf16_encode(values):
 
 
 def dcp_cand(world, k=2048):
-    """Candidates each rank sends: ceil(1.5 k / world)."""
-    return -(-3 * k // (2 * world))
+    """Candidates each rank sends: ceil(1.5 k / world), at most k (no rank
+    needs to send more than the k it could contribute)."""
+    return min(-(-3 * k // (2 * world)), k)
 
 
 def dcp_topk(scores, n_visible, world, cand=None, k=2048):
