@@ -15,7 +15,11 @@ Value recipe (one layer):
   head weights w ~ N(0,1)/sqrt(32) [T,32] fp32
   MLA query q_lat ~ N(0,1) [T,96,576] bf16
   latents ~ N(0,1) [pool tokens, 576] FP8 E4M3 with one scale per layer
-             kv_scale = amax(pool)/448
+             kv_scale = amax(pool)/448; or NVFP4 (352 B per token): dims
+             0..511 as E2M1 elements with one E4M3 scale per block of 16
+             (block scale = E4M3(amax_block / 6 / kv_scale), element = nearest
+             E2M1 value of x / (block scale * kv_scale)), dims 512..575 as
+             E4M3(x / kv_scale)
   pages: each request's logical pages are placed on a seeded random
          permutation of one shared physical pool; unused block-table entries
          are -1.
@@ -36,6 +40,10 @@ TOPK = 2048
 FP8_PAGE_BYTES = PAGE * IDX_DIM + PAGE * 4        # 8448
 MXFP4_PAGE_BYTES = PAGE * IDX_DIM // 2 + PAGE * 4  # 4352
 LAT_PAGE_BYTES = PAGE * LAT_DIM                    # 36864
+NVFP4_LAT_BYTES = V_DIM // 2 + V_DIM // 16 + (LAT_DIM - V_DIM)   # 256 + 32 + 64 = 352
+NVFP4_LAT_PAGE_BYTES = PAGE * NVFP4_LAT_BYTES      # 22528
+LATENT_FP8 = 0
+LATENT_NVFP4 = 1
 SM_SCALE = 1.0 / math.sqrt(192.0)
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
@@ -57,11 +65,12 @@ class Layer:
     w: torch.Tensor              # float32 [T,32]
     index_pages: torch.Tensor    # uint8 [num_pages, page_bytes]
     q_lat: torch.Tensor          # bfloat16 [T,96,576]
-    latent_pages: torch.Tensor   # uint8 [num_pages, 36864]
+    latent_pages: torch.Tensor   # uint8 [num_pages, 36864] (or [num_pages, 22528] NVFP4)
     kv_scale: float
     sm_scale: float = SM_SCALE
     seq_lens_host: List[int] = field(default_factory=list)
     q_counts_host: List[int] = field(default_factory=list)
+    latent_format: int = LATENT_FP8
 
     @property
     def num_requests(self):
@@ -113,12 +122,36 @@ def _mxfp4_rows(x: torch.Tensor):
     return packed.contiguous(), scale_byte.contiguous()
 
 
+def _e2m1_codes(y):
+    """Nearest E2M1 code (sign in bit 3) of y, magnitudes clamped to 6."""
+    mag = torch.tensor(_E2M1_MAG, device=y.device)
+    bounds = (mag[1:] + mag[:-1]) / 2
+    code = torch.bucketize(y.abs().clamp(max=6.0), bounds).to(torch.uint8)
+    return code | ((y < 0).to(torch.uint8) << 3)
+
+
+def _nvfp4_latent_rows(x, kv_scale):
+    """x [n, 576] fp32 -> NVFP4 latent rows [n, 352]: packed E2M1 of dims
+    0..511 (element 2i in the low nibble), 32 E4M3 block scales, E4M3 of
+    dims 512..575."""
+    n = x.shape[0]
+    ks = torch.tensor(kv_scale, dtype=torch.float32, device=x.device)
+    v = x[:, :V_DIM].reshape(n, V_DIM // 16, 16)
+    sc = (v.abs().amax(dim=-1) / 6.0 / ks).to(torch.float8_e4m3fn)
+    step = sc.to(torch.float32) * ks
+    y = torch.where(step.unsqueeze(-1) > 0, v / step.unsqueeze(-1), torch.zeros_like(v))
+    code = _e2m1_codes(y.reshape(n, V_DIM))
+    packed = code[:, 0::2] | (code[:, 1::2] << 4)
+    tail = (x[:, V_DIM:] / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+    return torch.cat([packed, sc.view(torch.uint8), tail], dim=1).contiguous()
+
+
 def _randn(g, shape, device):
     return torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
 
 
 def make_layer(seq_lens, n_q=1, key_format=KEYS_FP8, seed=0, device="cpu",
-               extra_pages=0, chunk_tokens=1 << 18) -> Layer:
+               extra_pages=0, chunk_tokens=1 << 18, latent_format=LATENT_FP8) -> Layer:
     """Build one layer for requests with the given context lengths (counted
     including the request's own query tokens) and n_q query tokens each."""
     seq_lens = [int(s) for s in seq_lens]
@@ -173,7 +206,8 @@ def make_layer(seq_lens, n_q=1, key_format=KEYS_FP8, seed=0, device="cpu",
 
     # latent pool: one scale for the whole layer -> two passes over the same
     # seeded chunks (first for amax, then to quantise)
-    lat = torch.empty((num_pages, LAT_PAGE_BYTES), dtype=torch.uint8, device=device)
+    lat_bytes = LAT_PAGE_BYTES if latent_format == LATENT_FP8 else NVFP4_LAT_PAGE_BYTES
+    lat = torch.empty((num_pages, lat_bytes), dtype=torch.uint8, device=device)
     state = g.get_state()
     amax = torch.zeros((), device=device)
     for t0 in range(0, ntok, chunk_tokens):
@@ -185,16 +219,19 @@ def make_layer(seq_lens, n_q=1, key_format=KEYS_FP8, seed=0, device="cpu",
         t1 = min(ntok, t0 + chunk_tokens)
         p0, p1 = t0 // PAGE, t1 // PAGE
         x = _randn(g, (t1 - t0, LAT_DIM), device)
-        codes = (x / torch.tensor(kv_scale, dtype=torch.float32, device=device)).to(
-            torch.float8_e4m3fn).view(torch.uint8)
-        lat[p0:p1] = codes.view(p1 - p0, LAT_PAGE_BYTES)
+        if latent_format == LATENT_FP8:
+            codes = (x / torch.tensor(kv_scale, dtype=torch.float32, device=device)).to(
+                torch.float8_e4m3fn).view(torch.uint8)
+            lat[p0:p1] = codes.view(p1 - p0, LAT_PAGE_BYTES)
+        else:
+            lat[p0:p1] = _nvfp4_latent_rows(x, kv_scale).view(p1 - p0, NVFP4_LAT_PAGE_BYTES)
 
     return Layer(q_offsets=q_offsets, seq_lens=torch.tensor(seq_lens, dtype=torch.int32,
                                                             device=device),
                  block_table=block_table, num_pages=num_pages, key_format=key_format,
                  q8=q8, qscale=qscale, w=w, index_pages=pages, q_lat=q_lat,
                  latent_pages=lat, kv_scale=kv_scale, seq_lens_host=seq_lens,
-                 q_counts_host=q_counts)
+                 q_counts_host=q_counts, latent_format=latent_format)
 
 
 def _cumsum(v):

@@ -72,6 +72,18 @@ def lib():
         L.oracle_append_cache.argtypes = [
             ctypes.c_int32, _i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
             _f32p, _f32p, ctypes.c_float, _u8p, _u8p, ctypes.c_int32]
+        L.oracle_latent_row.argtypes = [ctypes.c_int32, _u8p, ctypes.c_double, _f64p]
+        L.oracle_sparse_mla_fmt.argtypes = [
+            ctypes.c_int32, _i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
+            _u16p, _u8p, ctypes.c_int32, ctypes.c_double, ctypes.c_double, _i32p, ctypes.c_int32,
+            _i32p, ctypes.c_int32, _f64p, _f64p]
+        L.oracle_decode_fmt.argtypes = [
+            ctypes.c_int32, _i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
+            _u8p, _f32p, _f32p, _u8p, ctypes.c_int32, _u16p, _u8p, ctypes.c_int32,
+            ctypes.c_double, ctypes.c_double, ctypes.c_int32, _i32p, ctypes.c_int32, _i32p, _f64p,
+            _f64p]
+        for name in ("oracle_latent_row", "oracle_sparse_mla_fmt", "oracle_decode_fmt"):
+            getattr(L, name).restype = ctypes.c_int
         L.oracle_bf16_encode.restype = ctypes.c_uint16
         L.oracle_bf16_encode.argtypes = [ctypes.c_float]
         L.oracle_bf16_encode_array.argtypes = [_f32p, _u16p, ctypes.c_int64]
@@ -236,10 +248,22 @@ def topk(scores, n_visible, k=2048):
     return out
 
 
-def sparse_mla(batch, q_lat_bf16, latent_pages, kv_scale, sm_scale, indices, rows=None):
+def latent_row(row_bytes, kv_scale, latent_format=0):
+    """Dequantised latent [576] of one token from its stored bytes (576 B FP8
+    or 352 B NVFP4)."""
+    r = _arr(row_bytes, np.uint8)
+    out = np.empty(576, np.float64)
+    _check(lib().oracle_latent_row(int(latent_format), _p(r, ctypes.c_uint8), float(kv_scale),
+                                   _p(out, ctypes.c_double)), "latent_row")
+    return out
+
+
+def sparse_mla(batch, q_lat_bf16, latent_pages, kv_scale, sm_scale, indices, rows=None,
+               latent_format=0):
     """fp64 absorbed sparse MLA over the selected positions of each row.
     q_lat_bf16: bf16 bit patterns [T, 96, 576] (uint16 or torch.bfloat16).
-    indices: [nrows, k] logical positions (-1 = unused)."""
+    indices: [nrows, k] logical positions (-1 = unused).
+    latent_format: 0 = FP8 pages (576 B per token), 1 = NVFP4 pages (352 B)."""
     rows = _rows(batch, rows)
     q = _arr(q_lat_bf16, np.uint16)
     lat = _arr(latent_pages, np.uint8)
@@ -247,16 +271,17 @@ def sparse_mla(batch, q_lat_bf16, latent_pages, kv_scale, sm_scale, indices, row
     k = idx.shape[1]
     out = np.empty((rows.size, 96, 512), np.float64)
     lse = np.empty((rows.size, 96), np.float64)
-    _check(lib().oracle_sparse_mla(*batch.args(), _p(q, ctypes.c_uint16),
-                                   _p(lat, ctypes.c_uint8), float(kv_scale), float(sm_scale),
-                                   _p(idx, ctypes.c_int32), k, _p(rows, ctypes.c_int32),
-                                   rows.size, _p(out, ctypes.c_double),
-                                   _p(lse, ctypes.c_double)), "sparse_mla")
+    _check(lib().oracle_sparse_mla_fmt(*batch.args(), _p(q, ctypes.c_uint16),
+                                       _p(lat, ctypes.c_uint8), int(latent_format),
+                                       float(kv_scale), float(sm_scale),
+                                       _p(idx, ctypes.c_int32), k, _p(rows, ctypes.c_int32),
+                                       rows.size, _p(out, ctypes.c_double),
+                                       _p(lse, ctypes.c_double)), "sparse_mla")
     return out, lse
 
 
 def decode(batch, q8, qscale, w, index_pages, key_format, q_lat_bf16, latent_pages, kv_scale,
-           sm_scale, k=2048, rows=None):
+           sm_scale, k=2048, rows=None, latent_format=0):
     """The whole step (scores -> top-k -> sparse MLA) for the listed rows."""
     rows = _rows(batch, rows)
     q8 = _arr(q8, np.uint8)
@@ -268,10 +293,12 @@ def decode(batch, q8, qscale, w, index_pages, key_format, q_lat_bf16, latent_pag
     idx = np.empty((rows.size, k), np.int32)
     out = np.empty((rows.size, 96, 512), np.float64)
     lse = np.empty((rows.size, 96), np.float64)
-    _check(lib().oracle_decode(*batch.args(), _p(q8, ctypes.c_uint8), _p(qscale, ctypes.c_float),
-                               _p(w, ctypes.c_float), _p(pages, ctypes.c_uint8), int(key_format),
-                               _p(q, ctypes.c_uint16), _p(lat, ctypes.c_uint8), float(kv_scale),
-                               float(sm_scale), k, _p(rows, ctypes.c_int32), rows.size,
+    _check(lib().oracle_decode_fmt(*batch.args(), _p(q8, ctypes.c_uint8),
+                                   _p(qscale, ctypes.c_float), _p(w, ctypes.c_float),
+                                   _p(pages, ctypes.c_uint8), int(key_format),
+                                   _p(q, ctypes.c_uint16), _p(lat, ctypes.c_uint8),
+                                   int(latent_format), float(kv_scale),
+                                   float(sm_scale), k, _p(rows, ctypes.c_int32), rows.size,
                                _p(idx, ctypes.c_int32), _p(out, ctypes.c_double),
                                _p(lse, ctypes.c_double)), "decode")
     return idx, out, lse

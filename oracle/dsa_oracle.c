@@ -65,6 +65,12 @@
 #define MXFP4_KEY_BYTES_PER_TOKEN (IDX_DIM / 2 + IDX_DIM / 32)     /* 68 */
 #define MXFP4_PAGE_BYTES (PAGE_TOKENS * IDX_DIM / 2 + PAGE_TOKENS * 4) /* 4352 */
 /* Latent page: 64 x 576 E4M3 bytes, one scale per layer (passed separately). */
+/* NVFP4 latent page ([K31 "Packed KV cache"]: 352 B per token; the split is
+ * not printed -- reading: 64 rows of [256 B packed E2M1 of dims 0..511
+ * (element 2i in the low nibble) | 32 E4M3 scales, one per block of 16
+ * elements | 64 E4M3 bytes of dims 512..575]), one fp32 scale per layer. */
+#define NVFP4_LAT_BYTES 352
+#define NVFP4_LAT_PAGE_BYTES (PAGE_TOKENS * NVFP4_LAT_BYTES)
 #define LAT_BYTES_PER_TOKEN LAT_DIM                                /* 576 */
 #define LAT_PAGE_BYTES (PAGE_TOKENS * LAT_DIM)                     /* 36864 */
 
@@ -382,6 +388,29 @@ int oracle_visible(int32_t num_requests, const int32_t* q_offsets, const int32_t
     return ORC_OK;
 }
 
+/* ---- latent rows ------------------------------------------------------------ */
+
+/* Dequantised latent of one token, lhat[0..575], from its stored bytes.
+ * format 0 (FP8):   lhat[d] = E4M3(row[d]) * kv_scale
+ * format 1 (NVFP4): lhat[d] = E2M1(nibble d of row[0..255]) * E4M3(row[256 + d/16])
+ *                             * kv_scale                       for d < 512
+ *                   lhat[d] = E4M3(row[288 + d - 512]) * kv_scale  for d >= 512 */
+int oracle_latent_row(int32_t format, const uint8_t* row, double kv_scale, double* out) {
+    if (format == 0) {
+        for (int d = 0; d < LAT_DIM; ++d) out[d] = oracle_e4m3_decode(row[d]) * kv_scale;
+        return ORC_OK;
+    }
+    if (format != 1) return ORC_BAD_ARG;
+    for (int d = 0; d < V_DIM; ++d) {
+        const uint8_t byte = row[d / 2];
+        const uint8_t nib = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+        out[d] = oracle_e2m1_decode(nib) * oracle_e4m3_decode(row[V_DIM / 2 + d / 16]) * kv_scale;
+    }
+    for (int d = V_DIM; d < LAT_DIM; ++d)
+        out[d] = oracle_e4m3_decode(row[V_DIM / 2 + V_DIM / 16 + (d - V_DIM)]) * kv_scale;
+    return ORC_OK;
+}
+
 /* ---- sparse MLA, absorbed form -------------------------------------------- */
 
 /* For query row t and the selected positions I (entries >= 0 of indices[r,:]):
@@ -392,8 +421,9 @@ int oracle_visible(int32_t num_requests, const int32_t* q_offsets, const int32_t
  *   lse[h] = max_s z[h,s] + log(sum_s exp(z[h,s] - max_s z[h,s]))
  * An empty selection gives o = 0 and lse = -inf. */
 static int sparse_mla_row(const obatch* bt, int32_t t, const uint16_t* q_lat,
-                          const uint8_t* latent_pages, double kv_scale, double sm_scale,
-                          const int32_t* idx, int32_t k, double* o, double* lse) {
+                          const uint8_t* latent_pages, int32_t lat_format, double kv_scale,
+                          double sm_scale, const int32_t* idx, int32_t k, double* o,
+                          double* lse) {
     int32_t b;
     int64_t vis;
     int rc = locate(bt, t, &b, &vis);
@@ -421,9 +451,10 @@ static int sparse_mla_row(const obatch* bt, int32_t t, const uint16_t* q_lat,
         int32_t slot;
         rc = page_of(bt, b, idx[j], &page, &slot);
         if (rc) { free(L); free(q); free(z); return rc; }
-        const uint8_t* src = latent_pages + page * (int64_t)LAT_PAGE_BYTES + slot * LAT_DIM;
-        for (int d = 0; d < LAT_DIM; ++d)
-            L[(int64_t)c * LAT_DIM + d] = oracle_e4m3_decode(src[d]) * kv_scale;
+        const int64_t row_bytes = lat_format == 1 ? NVFP4_LAT_BYTES : LAT_DIM;
+        const uint8_t* src = latent_pages + (page * PAGE_TOKENS + slot) * row_bytes;
+        rc = oracle_latent_row(lat_format, src, kv_scale, L + (int64_t)c * LAT_DIM);
+        if (rc) { free(L); free(q); free(z); return rc; }
         ++c;
     }
     for (int i = 0; i < MLA_HEADS * LAT_DIM; ++i)
@@ -453,16 +484,18 @@ static int sparse_mla_row(const obatch* bt, int32_t t, const uint16_t* q_lat,
     return ORC_OK;
 }
 
-int oracle_sparse_mla(int32_t num_requests, const int32_t* q_offsets, const int32_t* seq_lens,
-                      const int32_t* block_table, int32_t max_pages, int32_t num_pages,
-                      const uint16_t* q_lat, const uint8_t* latent_pages, double kv_scale,
-                      double sm_scale, const int32_t* indices, int32_t k, const int32_t* rows,
-                      int32_t nrows, double* out, double* lse) {
+int oracle_sparse_mla_fmt(int32_t num_requests, const int32_t* q_offsets,
+                          const int32_t* seq_lens, const int32_t* block_table, int32_t max_pages,
+                          int32_t num_pages, const uint16_t* q_lat, const uint8_t* latent_pages,
+                          int32_t lat_format, double kv_scale, double sm_scale,
+                          const int32_t* indices, int32_t k, const int32_t* rows, int32_t nrows,
+                          double* out, double* lse) {
     obatch bt = {num_requests, q_offsets, seq_lens, block_table, max_pages, num_pages};
+    if (lat_format != 0 && lat_format != 1) return ORC_BAD_ARG;
     int err = ORC_OK;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t r = 0; r < nrows; ++r) {
-        int rc = sparse_mla_row(&bt, rows[r], q_lat, latent_pages, kv_scale, sm_scale,
+        int rc = sparse_mla_row(&bt, rows[r], q_lat, latent_pages, lat_format, kv_scale, sm_scale,
                                 indices + (int64_t)r * k, k,
                                 out + (int64_t)r * MLA_HEADS * V_DIM, lse + (int64_t)r * MLA_HEADS);
         if (rc) {
@@ -473,19 +506,30 @@ int oracle_sparse_mla(int32_t num_requests, const int32_t* q_offsets, const int3
     return err;
 }
 
+int oracle_sparse_mla(int32_t num_requests, const int32_t* q_offsets, const int32_t* seq_lens,
+                      const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                      const uint16_t* q_lat, const uint8_t* latent_pages, double kv_scale,
+                      double sm_scale, const int32_t* indices, int32_t k, const int32_t* rows,
+                      int32_t nrows, double* out, double* lse) {
+    return oracle_sparse_mla_fmt(num_requests, q_offsets, seq_lens, block_table, max_pages,
+                                 num_pages, q_lat, latent_pages, 0, kv_scale, sm_scale, indices,
+                                 k, rows, nrows, out, lse);
+}
+
 /* ---- the whole decode step for a set of query rows ----------------------- */
 
 /* scores -> top-k -> sparse MLA, row by row (what one layer's step computes for
  * those query tokens).  Outputs: indices [nrows, k], out [nrows, 96, 512],
  * lse [nrows, 96]. */
-int oracle_decode(int32_t num_requests, const int32_t* q_offsets, const int32_t* seq_lens,
-                  const int32_t* block_table, int32_t max_pages, int32_t num_pages,
-                  const uint8_t* q8, const float* qscale, const float* w,
-                  const uint8_t* index_pages, int32_t key_format, const uint16_t* q_lat,
-                  const uint8_t* latent_pages, double kv_scale, double sm_scale, int32_t k,
-                  const int32_t* rows, int32_t nrows, int32_t* indices, double* out,
-                  double* lse) {
+int oracle_decode_fmt(int32_t num_requests, const int32_t* q_offsets, const int32_t* seq_lens,
+                      const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                      const uint8_t* q8, const float* qscale, const float* w,
+                      const uint8_t* index_pages, int32_t key_format, const uint16_t* q_lat,
+                      const uint8_t* latent_pages, int32_t lat_format, double kv_scale,
+                      double sm_scale, int32_t k, const int32_t* rows, int32_t nrows,
+                      int32_t* indices, double* out, double* lse) {
     obatch bt = {num_requests, q_offsets, seq_lens, block_table, max_pages, num_pages};
+    if (lat_format != 0 && lat_format != 1) return ORC_BAD_ARG;
     int err = ORC_OK;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t r = 0; r < nrows; ++r) {
@@ -501,8 +545,8 @@ int oracle_decode(int32_t num_requests, const int32_t* q_offsets, const int32_t*
             rc = index_scores_row(&bt, rows[r], q8, qscale, w, index_pages, key_format, vis, S, NULL);
         if (!rc) rc = oracle_topk_row(S, vis, k, indices + (int64_t)r * k);
         if (!rc)
-            rc = sparse_mla_row(&bt, rows[r], q_lat, latent_pages, kv_scale, sm_scale,
-                                indices + (int64_t)r * k, k,
+            rc = sparse_mla_row(&bt, rows[r], q_lat, latent_pages, lat_format, kv_scale,
+                                sm_scale, indices + (int64_t)r * k, k,
                                 out + (int64_t)r * MLA_HEADS * V_DIM, lse + (int64_t)r * MLA_HEADS);
         free(S);
         if (rc) {
@@ -511,6 +555,19 @@ int oracle_decode(int32_t num_requests, const int32_t* q_offsets, const int32_t*
         }
     }
     return err;
+}
+
+int oracle_decode(int32_t num_requests, const int32_t* q_offsets, const int32_t* seq_lens,
+                  const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                  const uint8_t* q8, const float* qscale, const float* w,
+                  const uint8_t* index_pages, int32_t key_format, const uint16_t* q_lat,
+                  const uint8_t* latent_pages, double kv_scale, double sm_scale, int32_t k,
+                  const int32_t* rows, int32_t nrows, int32_t* indices, double* out,
+                  double* lse) {
+    return oracle_decode_fmt(num_requests, q_offsets, seq_lens, block_table, max_pages,
+                             num_pages, q8, qscale, w, index_pages, key_format, q_lat,
+                             latent_pages, 0, kv_scale, sm_scale, k, rows, nrows, indices, out,
+                             lse);
 }
 
 /* ---- cache append ---------------------------------------------------------- */
