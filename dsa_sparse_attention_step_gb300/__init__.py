@@ -16,10 +16,13 @@ __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path"
            "dsa_topk_workspace_size", "dsa_sparse_mla", "dsa_sparse_mla_workspace_size",
            "dsa_decode", "dsa_decode_workspace_size", "dsa_decode_noalloc",
            "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards",
-           "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "dsa_lse_combine"]
+           "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "dsa_lse_combine",
+           "LATENT_FP8", "LATENT_NVFP4", "dsa_sparse_mla_ex", "dsa_decode_ex"]
 
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
+LATENT_FP8 = 0
+LATENT_NVFP4 = 1
 TOPK = 2048
 PAGE = 64
 NOALLOC_SCRATCH_BYTES = 16 << 20  # DSA_NOALLOC_SCRATCH_BYTES of include/dsa.h
@@ -73,6 +76,10 @@ _SIGS = {
     "dsa_sparse_mla": (ctypes.c_int, [_bp, _vp, _vp, _f32, _f32, _vp, _i32, _vp, _vp, _vp, _sz,
                                       _vp, _vp]),
     "dsa_decode_workspace_size": (_sz, [_bp, _i32]),
+    "dsa_sparse_mla_ex": (ctypes.c_int, [_bp, _vp, _vp, ctypes.c_int, _f32, _f32, _vp, _i32, _vp,
+                                         _vp, _vp, _sz, _vp, _vp]),
+    "dsa_decode_ex": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, ctypes.c_int,
+                                     _f32, _f32, _i32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "dsa_decode": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32, _f32,
                                   _i32, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "dsa_decode_noalloc": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _f32,
@@ -233,6 +240,36 @@ def dsa_test_sparse_mla_wait_timeout(batch, q_lat, latent_pages, kv_scale, sm_sc
         _ptr(out, (torch.bfloat16, torch.int16), "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(ws), nbytes, _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(rc, "dsa_test_sparse_mla_wait_timeout")
+
+
+def dsa_sparse_mla_ex(batch, q_lat, latent_pages, latent_format, kv_scale, sm_scale, indices,
+                      topk, out, lse=None, ws=None, dev_status=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().dsa_sparse_mla_ex(batch.ref(), _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+                                  _ptr(latent_pages, torch.uint8, "latent_pages"),
+                                  int(latent_format), float(kv_scale), float(sm_scale),
+                                  _ptr(indices, torch.int32, "indices"), int(topk),
+                                  _ptr(out, (torch.bfloat16, torch.int16), "out"),
+                                  _ptr(lse, torch.float32, "lse"), _ptr(ws), nbytes,
+                                  _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_sparse_mla_ex")
+
+
+def dsa_decode_ex(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages,
+                  latent_format, kv_scale, sm_scale, topk, out, lse, indices, ws,
+                  dev_status=None, stream=None):
+    nbytes = ws.numel() * ws.element_size()
+    rc = load().dsa_decode_ex(batch.ref(), _ptr(q_fp8, torch.uint8, "q_fp8"),
+                              _ptr(q_scale, torch.float32, "q_scale"), _ptr(w, torch.float32, "w"),
+                              _ptr(index_pages, torch.uint8, "index_pages"), int(key_format),
+                              _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+                              _ptr(latent_pages, torch.uint8, "latent_pages"),
+                              int(latent_format), float(kv_scale), float(sm_scale), int(topk),
+                              _ptr(out, (torch.bfloat16, torch.int16), "out"),
+                              _ptr(lse, torch.float32, "lse"),
+                              _ptr(indices, torch.int32, "indices"), _ptr(ws), nbytes,
+                              _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_decode_ex")
 
 
 def dsa_decode_workspace_size(batch, topk=TOPK):

@@ -19,7 +19,7 @@ bool topk_supported(int max_seq);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
-                              cudaStream_t stream, bool wait_test = false);
+                              cudaStream_t stream, bool wait_test = false, int latent_format = 0);
 size_t sparse_mla_workspace_bytes(int total_q, int K);
 int sparse_mla_launches(int total_q, int K);
 cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const float* lat,
@@ -180,6 +180,17 @@ dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const v
                           float kv_scale, float sm_scale, const int32_t* indices, int32_t topk,
                           uint16_t* out, float* lse, void* ws, size_t ws_bytes,
                           int32_t* dev_status, dsa_stream_t stream) {
+    return dsa_sparse_mla_ex(batch, q_lat, latent_pages, DSA_LATENT_FP8_E4M3, kv_scale, sm_scale,
+                             indices, topk, out, lse, ws, ws_bytes, dev_status, stream);
+}
+
+dsa_status dsa_sparse_mla_ex(const dsa_batch* batch, const uint16_t* q_lat,
+                             const void* latent_pages, dsa_latent_format latent_format,
+                             float kv_scale, float sm_scale, const int32_t* indices, int32_t topk,
+                             uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                             int32_t* dev_status, dsa_stream_t stream) {
+    if (latent_format != DSA_LATENT_FP8_E4M3 && latent_format != DSA_LATENT_NVFP4)
+        return DSA_ERR_UNSUPPORTED;
     dsa_status st = check_batch(batch);
     if (st != DSA_OK) return st;
     st = check_mla_args(batch, q_lat, latent_pages, indices, topk, out, kv_scale, sm_scale);
@@ -191,7 +202,7 @@ dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat, const v
                          std::memory_order_relaxed);
     return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
                                          indices, topk, out, lse, ws, dev_status, false,
-                                         (cudaStream_t)stream));
+                                         (cudaStream_t)stream, false, (int)latent_format));
 }
 
 size_t dsa_decode_workspace_size(const dsa_batch* batch, int32_t topk) {
@@ -206,6 +217,19 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
                       const uint16_t* q_lat, const void* latent_pages, float kv_scale,
                       float sm_scale, int32_t topk, uint16_t* out, float* lse, int32_t* indices,
                       void* ws, size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream) {
+    return dsa_decode_ex(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages,
+                         DSA_LATENT_FP8_E4M3, kv_scale, sm_scale, topk, out, lse, indices, ws,
+                         ws_bytes, dev_status, stream);
+}
+
+dsa_status dsa_decode_ex(const dsa_batch* batch, const uint8_t* q_fp8, const float* q_scale,
+                         const float* w, const void* index_pages, dsa_key_format key_format,
+                         const uint16_t* q_lat, const void* latent_pages,
+                         dsa_latent_format latent_format, float kv_scale, float sm_scale,
+                         int32_t topk, uint16_t* out, float* lse, int32_t* indices, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream) {
+    if (latent_format != DSA_LATENT_FP8_E4M3 && latent_format != DSA_LATENT_NVFP4)
+        return DSA_ERR_UNSUPPORTED;
     dsa_status st = check_batch(batch);
     if (st != DSA_OK) return st;
     const int64_t ld = score_ld_for(batch);
@@ -234,7 +258,7 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
     if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, base + off_topk, true, s);
     if (e == cudaSuccess)
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
-                              base + off_mla, dev_status, true, s);
+                              base + off_mla, dev_status, true, s, false, (int)latent_format);
     return cuda_status(e);
 }
 

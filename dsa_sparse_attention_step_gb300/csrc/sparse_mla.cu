@@ -142,6 +142,35 @@ __device__ __forceinline__ void e4m3x8_to_f16x8(uint32_t w0, uint32_t w1, uint32
     }
 }
 
+// Eight packed E2M1 elements (element 2i in the low nibble of byte i) -> eight
+// f16 values, exact.  Every E2M1 magnitude (0, 0.5, 1, 1.5, 2, 3, 4, 6) is an
+// f16 whose low byte is zero, so one byte-permute per pair picks the two high
+// bytes from a table and zero low bytes; the sign bits are moved to bits 15
+// and 31.
+__device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
+    constexpr uint32_t kHiLo = 0x3E3C3800u;  // f16 high bytes of magnitudes 0..3
+    constexpr uint32_t kHiHi = 0x46444240u;  // magnitudes 4..7
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t byte = (w >> (8 * j)) & 0xFFu;
+        const uint32_t sel = ((byte & 0x7u) << 4) | ((byte & 0x70u) << 8);
+        o[j] = __byte_perm(kHiLo, kHiHi, sel) | ((byte & 0x8u) << 12) | ((byte & 0x80u) << 24);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// NVFP4 latent row (352 B): packed E2M1 of dims 0..511, 32 E4M3 block scales
+// (one per 16 elements), E4M3 of dims 512..575.
+constexpr int kNvRowBytes = kVDim / 2 + kVDim / 16 + (kLatDim - kVDim);  // 352
+constexpr int kNvScaleOff = kVDim / 2;                                   // 256
+constexpr int kNvTailOff = kNvScaleOff + kVDim / 16;                     // 288
+
 struct MlaParams {
     BatchArgs bt;
     const __nv_bfloat16* q_lat;  // [T][96][576]
@@ -162,8 +191,9 @@ struct MlaParams {
 // kWaitTest: the variant of the test-only export -- the producers withhold one
 // arrival (the latent slab group 512-575 of the first tile) and every wait has
 // a budget of 2^20 cycles, so the MMA thread's wait runs out and the kernel
-// takes its abort path.
-template <bool kWaitTest>
+// takes its abort path.  kLat: latent pages as FP8 (0, 576 B per token) or
+// NVFP4 (1, 352 B per token); both are lifted exactly to f16 by the producers.
+template <bool kWaitTest, int kLat>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaParams p) {
     constexpr long long kBudget = kWaitTest ? (1ll << 20) : kWaitCycles;
     extern __shared__ uint8_t smem_raw[];
@@ -306,7 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         // as soon as it is free, and its next tile is then loaded into the
         // same registers.
         const int pt = tid - 128;
-        uint4 raw[kGroups][6];
+        // NVFP4 (kLat == 1): group g < 4 is 64 rows x 4 items of 32 elements
+        // (16 packed bytes + their two block scales), group 4 is 64 rows x 4
+        // chunks of 16 E4M3 bytes (dims 512-575): 256 items per group, three
+        // per thread of warps 4-5, two per thread of warp 6
+        uint4 raw[kGroups][kLat == 0 ? 6 : 3];
+        uint32_t rsc[4][kLat == 0 ? 1 : 3];
+        (void)rsc;
 #define DSA_MLA_CHUNK(g_, u_, r_, c_)                                          \
     const int r_ = ((g_) < 4) ? ((ptv >> 3) + 12 * (u_)) : ((ptv >> 2) + 24 * (u_)); \
     const int c_ = ((g_) < 4) ? (8 * (g_) + (ptv & 7)) : (32 + (ptv & 3));
@@ -320,6 +356,52 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         raw[g_][u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(          \
                                             p.latent_pages + (int64_t)row * kLatDim) + c) \
                                 : make_uint4(0u, 0u, 0u, 0u);                   \
+    }
+#define DSA_NV_HAS(u_) (pt + kProducers * (u_) < 256)
+#define DSA_NV_LOAD(i_, g_)                                                    \
+    _Pragma("unroll") for (int u = 0; u < 3; ++u) {                             \
+        if (!DSA_NV_HAS(u)) continue;                                           \
+        const int q = ptv + kProducers * u, r = q >> 2, h = q & 3;              \
+        const int row = sRow[(i_) * kTileKeys + r];                             \
+        const uint8_t* src = p.latent_pages + (int64_t)(row >= 0 ? row : 0) * kNvRowBytes; \
+        if ((g_) < 4) {                                                         \
+            raw[g_][u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + 64 * (g_) + 16 * h)) \
+                                    : make_uint4(0u, 0u, 0u, 0u);               \
+            rsc[(g_) & 3][u] = (row >= 0) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>( \
+                                                src + kNvScaleOff + 8 * (g_) + 2 * h)) : 0u; \
+        } else {                                                                \
+            raw[g_][u] = (row >= 0) ? __ldg(reinterpret_cast<const uint4*>(src + kNvTailOff + 16 * h)) \
+                                    : make_uint4(0u, 0u, 0u, 0u);               \
+        }                                                                       \
+    }
+#define DSA_NV_STORE(g_)                                                       \
+    _Pragma("unroll") for (int u = 0; u < 3; ++u) {                             \
+        if (!DSA_NV_HAS(u)) continue;                                           \
+        const int q = ptv + kProducers * u, r = q >> 2, h = q & 3;              \
+        if ((g_) < 4) {                                                         \
+            const __half2_raw sc = __nv_cvt_fp8x2_to_halfraw2(                  \
+                (__nv_fp8x2_storage_t)(rsc[(g_) & 3][u] & 0xFFFFu), __NV_E4M3);   \
+            const uint32_t s_lo = (uint32_t)sc.x | ((uint32_t)sc.x << 16);      \
+            const uint32_t s_hi = (uint32_t)sc.y | ((uint32_t)sc.y << 16);      \
+            uint8_t* base = sL + (2 * (g_) + (h >> 1)) * kLSlabBytes;           \
+            const uint32_t wv[4] = {raw[g_][u].x, raw[g_][u].y, raw[g_][u].z, raw[g_][u].w}; \
+            _Pragma("unroll") for (int j = 0; j < 4; ++j) {                     \
+                const uint4 f = e2m1x8_to_f16x8(wv[j]);                         \
+                const uint32_t sj = (j < 2) ? s_lo : s_hi;                       \
+                *reinterpret_cast<uint4*>(base + sw128(r, (h & 1) * 64 + 16 * j)) = \
+                    make_uint4(hmul2_u32(f.x, sj), hmul2_u32(f.y, sj), hmul2_u32(f.z, sj), \
+                               hmul2_u32(f.w, sj));                              \
+            }                                                                   \
+        } else {                                                                \
+            uint32_t h0[4], h1[4];                                              \
+            e4m3x8_to_f16x8(raw[g_][u].x, raw[g_][u].y, h0);                    \
+            e4m3x8_to_f16x8(raw[g_][u].z, raw[g_][u].w, h1);                    \
+            uint8_t* base = sL + 8 * kLSlabBytes;                               \
+            *reinterpret_cast<uint4*>(base + sw128(r, h * 32)) =                \
+                make_uint4(h0[0], h0[1], h0[2], h0[3]);                         \
+            *reinterpret_cast<uint4*>(base + sw128(r, h * 32 + 16)) =           \
+                make_uint4(h1[0], h1[1], h1[2], h1[3]);                         \
+        }                                                                       \
     }
 #define DSA_MLA_STORE(g_)                                                      \
     _Pragma("unroll") for (int u = 0; u < DSA_MLA_NCHUNK(g_); ++u) {            \
@@ -337,7 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         if (n_tiles > 0) {
             const int ptv = pt;
 #pragma unroll
-            for (int g = 0; g < kGroups; ++g) { DSA_MLA_LOAD(0, g) }
+            for (int g = 0; g < kGroups; ++g) {
+                if constexpr (kLat == 0) { DSA_MLA_LOAD(0, g) }
+                else { DSA_NV_LOAD(0, g) }
+            }
         }
         bool ok = true;
         for (int i = 0; i < n_tiles && ok; ++i) {
@@ -352,10 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                     ok = false;
                     break;
                 }
-                DSA_MLA_STORE(g)
+                if constexpr (kLat == 0) { DSA_MLA_STORE(g) }
+                else { DSA_NV_STORE(g) }
                 fence_proxy_async_smem();
                 if (!(kWaitTest && i == 0 && g == 4)) mbar_arrive(&bars->lfull[g]);
-                if (i + 1 < n_tiles) { DSA_MLA_LOAD(i + 1, g) }
+                if (i + 1 < n_tiles) {
+                    if constexpr (kLat == 0) { DSA_MLA_LOAD(i + 1, g) }
+                    else { DSA_NV_LOAD(i + 1, g) }
+                }
             }
         }
 #undef DSA_MLA_CHUNK
@@ -363,6 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 #undef DSA_MLA_HAS
 #undef DSA_MLA_LOAD
 #undef DSA_MLA_STORE
+#undef DSA_NV_HAS
+#undef DSA_NV_LOAD
+#undef DSA_NV_STORE
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one thread) ----------------
         // descriptors are built once; operand offsets are added in 16-byte
@@ -709,7 +801,7 @@ int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
-                              cudaStream_t stream, bool wait_test) {
+                              cudaStream_t stream, bool wait_test, int latent_format) {
     if (bt.total_q == 0) return cudaSuccess;
     MlaParams p;
     p.bt = bt;
@@ -728,7 +820,10 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.status = status;
     p.part_o = p.splits > 1 ? reinterpret_cast<__half*>(wsb + w.part_o) : nullptr;
     p.part_lse = p.splits > 1 ? reinterpret_cast<float*>(wsb + w.part_lse) : nullptr;
-    auto kernel = wait_test ? sparse_mla_tc_kernel<true> : sparse_mla_tc_kernel<false>;
+    auto kernel = latent_format == DSA_LATENT_NVFP4
+                      ? sparse_mla_tc_kernel<false, DSA_LATENT_NVFP4>
+                      : (wait_test ? sparse_mla_tc_kernel<true, DSA_LATENT_FP8_E4M3>
+                                   : sparse_mla_tc_kernel<false, DSA_LATENT_FP8_E4M3>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemAlloc);
     if (e != cudaSuccess) return e;

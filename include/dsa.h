@@ -79,6 +79,11 @@ typedef enum {
 
 typedef enum { DSA_KEYS_FP8_E4M3 = 0, DSA_KEYS_MXFP4 = 1 } dsa_key_format;
 
+/* Latent page format (section "Packed KV cache": 576 B FP8 or 352 B NVFP4 per
+ * token).  The pages print only the NVFP4 width; the byte split used is the
+ * one described at dsa_sparse_mla_ex. */
+typedef enum { DSA_LATENT_FP8_E4M3 = 0, DSA_LATENT_NVFP4 = 1 } dsa_latent_format;
+
 enum {
     DSA_PAGE_SIZE = 64,
     DSA_INDEX_HEADS = 32,
@@ -89,7 +94,8 @@ enum {
     DSA_TOPK = 2048,
     DSA_FP8_INDEX_PAGE_BYTES = 8448,
     DSA_MXFP4_INDEX_PAGE_BYTES = 4352,
-    DSA_LATENT_PAGE_BYTES = 36864
+    DSA_LATENT_PAGE_BYTES = 36864,
+    DSA_NVFP4_LATENT_PAGE_BYTES = 22528
 };
 
 /* Request metadata of one step.  The struct lives in host memory; the three
@@ -173,6 +179,23 @@ dsa_status dsa_sparse_mla(const dsa_batch* batch, const uint16_t* q_lat,
                           void* ws, size_t ws_bytes, int32_t* dev_status,
                           dsa_stream_t stream);
 
+/* dsa_sparse_mla with the latent format as an argument.  DSA_LATENT_FP8_E4M3 is
+ * dsa_sparse_mla.  DSA_LATENT_NVFP4: section "Packed KV cache" (NVFP4
+ * latents, 352 bytes per token); each token's 352 bytes, 64 tokens per page
+ * (22528 B), are
+ *   bytes   0..255  dims 0..511 as E2M1 (element 2i in the low nibble of byte i)
+ *   bytes 256..287  one E4M3 scale per block of 16 of those elements
+ *   bytes 288..351  dims 512..575 as E4M3
+ * and the latent is lhat[d] = E2M1 * E4M3(block scale) * kv_scale for d < 512,
+ * E4M3 * kv_scale for d >= 512.  Every such value is exact in f16, and the
+ * kernel lifts it exactly, so the arithmetic after the lift is that of FP8
+ * latents. */
+dsa_status dsa_sparse_mla_ex(const dsa_batch* batch, const uint16_t* q_lat,
+                             const void* latent_pages, dsa_latent_format latent_format,
+                             float kv_scale, float sm_scale, const int32_t* indices, int32_t topk,
+                             uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                             int32_t* dev_status, dsa_stream_t stream);
+
 /* ---- the fused step ---------------------------------------------------------
  * dsa_index_scores -> dsa_topk -> dsa_sparse_mla on one stream, the scores
  * kept in the workspace (section "Fused low-latency decode for DSA layers").
@@ -184,6 +207,15 @@ dsa_status dsa_decode(const dsa_batch* batch, const uint8_t* q_fp8, const float*
                       float sm_scale, int32_t topk, uint16_t* out, float* lse,
                       int32_t* indices, void* ws, size_t ws_bytes, int32_t* dev_status,
                       dsa_stream_t stream);
+
+/* dsa_decode with the latent format as an argument (see dsa_sparse_mla_ex);
+ * DSA_LATENT_FP8_E4M3 is dsa_decode.  Same workspace size. */
+dsa_status dsa_decode_ex(const dsa_batch* batch, const uint8_t* q_fp8, const float* q_scale,
+                         const float* w, const void* index_pages, dsa_key_format key_format,
+                         const uint16_t* q_lat, const void* latent_pages,
+                         dsa_latent_format latent_format, float kv_scale, float sm_scale,
+                         int32_t topk, uint16_t* out, float* lse, int32_t* indices, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, dsa_stream_t stream);
 
 /* ---- the fused step without caller scratch ------------------------------------
  * No counterpart on the pages: an addition of this library.  Same arguments,
