@@ -84,6 +84,11 @@ def lib():
             _f64p]
         for name in ("oracle_latent_row", "oracle_sparse_mla_fmt", "oracle_decode_fmt"):
             getattr(L, name).restype = ctypes.c_int
+        L.oracle_indexer_front.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _u16p,
+                                           _u16p, _u16p, _u16p, _u16p, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_quantize_rows.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int32, _u8p, _f32p]
+        for name in ("oracle_indexer_front", "oracle_quantize_rows"):
+            getattr(L, name).restype = ctypes.c_int
         L.oracle_bf16_encode.restype = ctypes.c_uint16
         L.oracle_bf16_encode.argtypes = [ctypes.c_float]
         L.oracle_bf16_encode_array.argtypes = [_f32p, _u16p, ctypes.c_int64]
@@ -369,3 +374,42 @@ def lse_combine(parts, lses):
                                     _p(l, ctypes.c_double), _p(out, ctypes.c_double),
                                     _p(lse, ctypes.c_double)), "lse_combine")
     return out.reshape(p.shape[1:]), lse.reshape(l.shape[1:])
+
+
+# ---- fused indexer front ------------------------------------------------------
+
+def indexer_front(q_c, x, w_q, w_k, w_w):
+    """fp64 indexer front for T tokens: q [T, 4096] (normed query projection),
+    w [T, 32] head weights, key [T, 128] new index keys, inv_rms [T].
+    Inputs are bf16 bit patterns (uint16 / int16 / torch.bfloat16):
+    q_c [T, dq], x [T, dh], w_q [4096, dq], w_k [128, dh], w_w [32, dh]."""
+    qc = _arr(q_c, np.uint16)
+    xx = _arr(x, np.uint16)
+    T, dq = qc.shape
+    dh = xx.shape[1]
+    wq = _arr(w_q, np.uint16)
+    wk = _arr(w_k, np.uint16)
+    ww = _arr(w_w, np.uint16)
+    assert wq.shape == (4096, dq) and wk.shape == (128, dh) and ww.shape == (32, dh)
+    q = np.empty((T, 4096), np.float64)
+    w = np.empty((T, 32), np.float64)
+    key = np.empty((T, 128), np.float64)
+    inv = np.empty(T, np.float64)
+    _check(lib().oracle_indexer_front(T, dq, dh, _p(qc, ctypes.c_uint16), _p(xx, ctypes.c_uint16),
+                                      _p(wq, ctypes.c_uint16), _p(ww, ctypes.c_uint16),
+                                      _p(wk, ctypes.c_uint16), _p(q, ctypes.c_double),
+                                      _p(w, ctypes.c_double), _p(key, ctypes.c_double),
+                                      _p(inv, ctypes.c_double)), "indexer_front")
+    return q, w, key, inv
+
+
+def quantize_rows(x, dim):
+    """The cache writer's per-row FP8 rule on binary32 values: codes [n, dim]
+    (uint8) and scales [n] (float32)."""
+    v = _arr(x, np.float32).reshape(-1, dim)
+    codes = np.empty(v.shape, np.uint8)
+    scales = np.empty(v.shape[0], np.float32)
+    _check(lib().oracle_quantize_rows(_p(v, ctypes.c_float), v.shape[0], dim,
+                                      _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_float)),
+           "quantize_rows")
+    return codes, scales

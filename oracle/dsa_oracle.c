@@ -760,3 +760,82 @@ int oracle_lse_combine(int32_t world, int64_t nrows, int32_t dim, const double* 
     }
     return ORC_OK;
 }
+
+/* ---- fused indexer front ---------------------------------------------------- */
+
+/* [K31 "Fused low-latency decode for DSA layers"], second step: one kernel
+ * does the query norm, the indexer query projection, FP8 quantisation with the
+ * head weights folded in, and the new token's index key.  The pages give
+ * neither dimensions nor formulas; the reading is
+ *   inv_rms[t] = 1 / sqrt( (1/dq) sum_k q_c[t,k]^2 + 1e-6 )        (query norm;
+ *                its gain is part of the synthetic projection W_q)
+ *   q[t,j]     = inv_rms[t] * sum_k W_q[j,k] q_c[t,k]    j < 32*128: head j/128
+ *   w[t,h]     = sum_k W_w[h,k] x[t,k]                   h < 32 head weights
+ *   key[t,d]   = sum_k W_k[d,k] x[t,k]                   d < 128 the new index key
+ * with q_c the token's query latent [dq], x its hidden state [dh], all bf16
+ * inputs decoded exactly and the arithmetic in fp64.  Quantising q per head
+ * and the key (and writing the key into the cache) follow the cache writer's
+ * rule: oracle_quantize_rows below and oracle_append_cache. */
+int oracle_indexer_front(int32_t T, int32_t dq, int32_t dh, const uint16_t* q_c, const uint16_t* x,
+                         const uint16_t* w_q, const uint16_t* w_w, const uint16_t* w_k,
+                         double* q, double* w, double* key, double* inv_rms) {
+    if (T < 0 || dq < 1 || dh < 1) return ORC_BAD_ARG;
+    int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t t = 0; t < T; ++t) {
+        double* qc = (double*)malloc(sizeof(double) * (size_t)dq);
+        double* xx = (double*)malloc(sizeof(double) * (size_t)dh);
+        if (!qc || !xx) {
+            free(qc); free(xx);
+#pragma omp critical
+            err = ORC_NOMEM;
+            continue;
+        }
+        double ss = 0.0;
+        for (int32_t k = 0; k < dq; ++k) {
+            qc[k] = oracle_bf16_decode(q_c[(int64_t)t * dq + k]);
+            ss += qc[k] * qc[k];
+        }
+        for (int32_t k = 0; k < dh; ++k) xx[k] = oracle_bf16_decode(x[(int64_t)t * dh + k]);
+        const double r = 1.0 / sqrt(ss / dq + 1e-6);
+        inv_rms[t] = r;
+        for (int32_t j = 0; j < IDX_HEADS * IDX_DIM; ++j) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < dq; ++k) acc += oracle_bf16_decode(w_q[(int64_t)j * dq + k]) * qc[k];
+            q[(int64_t)t * IDX_HEADS * IDX_DIM + j] = r * acc;
+        }
+        for (int32_t h = 0; h < IDX_HEADS; ++h) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < dh; ++k) acc += oracle_bf16_decode(w_w[(int64_t)h * dh + k]) * xx[k];
+            w[(int64_t)t * IDX_HEADS + h] = acc;
+        }
+        for (int32_t d = 0; d < IDX_DIM; ++d) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < dh; ++k) acc += oracle_bf16_decode(w_k[(int64_t)d * dh + k]) * xx[k];
+            key[(int64_t)t * IDX_DIM + d] = acc;
+        }
+        free(qc);
+        free(xx);
+    }
+    return err;
+}
+
+/* Per-row FP8 quantisation, the cache writer's rule: scale = amax/448 in fp32
+ * (1 when amax == 0), code = E4M3_rne_satfinite(x / scale) with an fp32
+ * division.  x [nrows][dim] binary32 -> codes [nrows][dim], scales [nrows]. */
+int oracle_quantize_rows(const float* x, int64_t nrows, int32_t dim, uint8_t* codes,
+                         float* scales) {
+    if (nrows < 0 || dim < 1) return ORC_BAD_ARG;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const float* v = x + r * dim;
+        float amax = 0.0f;
+        for (int32_t d = 0; d < dim; ++d) {
+            const float a = fabsf(v[d]);
+            if (a > amax) amax = a;
+        }
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        for (int32_t d = 0; d < dim; ++d) codes[r * dim + d] = oracle_e4m3_encode(v[d] / scale);
+        scales[r] = scale;
+    }
+    return ORC_OK;
+}
