@@ -17,12 +17,15 @@ __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path"
            "dsa_decode", "dsa_decode_workspace_size", "dsa_decode_noalloc",
            "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards",
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "dsa_lse_combine",
-           "LATENT_FP8", "LATENT_NVFP4", "dsa_sparse_mla_ex", "dsa_decode_ex"]
+           "LATENT_FP8", "LATENT_NVFP4", "dsa_sparse_mla_ex", "dsa_decode_ex",
+           "dsa_indexer_front", "FRONT_QLAT_DIM", "FRONT_HIDDEN_DIM"]
 
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
 LATENT_FP8 = 0
 LATENT_NVFP4 = 1
+FRONT_QLAT_DIM = 1536    # query latent of dsa_indexer_front
+FRONT_HIDDEN_DIM = 7168  # hidden state of dsa_indexer_front
 TOPK = 2048
 PAGE = 64
 NOALLOC_SCRATCH_BYTES = 16 << 20  # DSA_NOALLOC_SCRATCH_BYTES of include/dsa.h
@@ -89,6 +92,8 @@ _SIGS = {
     "dsa_dcp_topk": (ctypes.c_int, [_bp, _vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz,
                                     _vp]),
     "dsa_lse_combine": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "dsa_indexer_front": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         ctypes.c_int, _vp, _vp, _vp, _vp]),
     "dsa_plan_token_shards": (ctypes.c_int32, [ctypes.POINTER(ctypes.c_int32),
                                                ctypes.POINTER(ctypes.c_int32), _i32, _i32, _i32,
                                                ctypes.POINTER(ShardPart), _i32]),
@@ -336,6 +341,21 @@ def dsa_lse_combine(total_q, world, part_out, part_lse, out, lse=None, stream=No
                                 _ptr(out, (torch.bfloat16, torch.int16), "out"),
                                 _ptr(lse, torch.float32, "lse"), _stream(stream))
     _check(rc, "dsa_lse_combine")
+
+
+def dsa_indexer_front(batch, q_c, x, w_q, w_k, w_w, q_fp8, q_scale, w, index_pages=None,
+                      key_format=KEYS_FP8, q_f32=None, k_f32=None, dev_status=None, stream=None):
+    bf = (torch.bfloat16, torch.int16)
+    rc = load().dsa_indexer_front(batch.ref(), _ptr(q_c, bf, "q_c"), _ptr(x, bf, "x"),
+                                  _ptr(w_q, bf, "w_q"), _ptr(w_k, bf, "w_k"), _ptr(w_w, bf, "w_w"),
+                                  _ptr(q_fp8, torch.uint8, "q_fp8"),
+                                  _ptr(q_scale, torch.float32, "q_scale"),
+                                  _ptr(w, torch.float32, "w"),
+                                  _ptr(index_pages, torch.uint8, "index_pages"), int(key_format),
+                                  _ptr(q_f32, torch.float32, "q_f32"),
+                                  _ptr(k_f32, torch.float32, "k_f32"),
+                                  _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(rc, "dsa_indexer_front")
 
 
 def dsa_plan_token_shards(seq_lens, q_counts, world, rank):

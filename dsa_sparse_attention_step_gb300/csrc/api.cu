@@ -38,6 +38,11 @@ cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld
 cudaError_t launch_lse_combine(int total_q, int world, const uint16_t* part, const float* part_lse,
                                uint16_t* out, float* lse, cudaStream_t stream);
 
+cudaError_t launch_indexer_front(const BatchArgs& bt, const uint16_t* q_c, const uint16_t* x,
+                                 const uint16_t* w_q, const uint16_t* w_k, const uint16_t* w_w,
+                                 uint8_t* q8, float* qscale, float* w, void* index_pages,
+                                 float* q_f32, float* k_f32, int32_t* status, cudaStream_t stream);
+
 std::atomic<uint64_t> g_launches{0};
 }  // namespace dsa
 
@@ -304,6 +309,28 @@ dsa_status dsa_lse_combine(int32_t total_q, int32_t world, const uint16_t* part_
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cuda_status(launch_lse_combine(total_q, world, part_out, part_lse, out, lse,
                                           (cudaStream_t)stream));
+}
+
+dsa_status dsa_indexer_front(const dsa_batch* batch, const uint16_t* q_c, const uint16_t* x,
+                             const uint16_t* w_q, const uint16_t* w_k, const uint16_t* w_w,
+                             uint8_t* q_fp8, float* q_scale, float* w, void* index_pages,
+                             dsa_key_format key_format, float* q_f32, float* k_f32,
+                             int32_t* dev_status, dsa_stream_t stream) {
+    dsa_status st = check_batch(batch);
+    if (st != DSA_OK) return st;
+    if (index_pages && key_format != DSA_KEYS_FP8_E4M3) return DSA_ERR_UNSUPPORTED;
+    if (!q_c || !x || !w_q || !w_k || !w_w || !q_fp8 || !q_scale || !w) return DSA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q_c, x, w_q, w_k, w_w, q_fp8, q_scale, w};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return DSA_ERR_INVALID_ARG;
+    if ((index_pages && !aligned16(index_pages)) || (q_f32 && !aligned16(q_f32)) ||
+        (k_f32 && !aligned16(k_f32)))
+        return DSA_ERR_INVALID_ARG;
+    if (batch->total_q == 0) return DSA_OK;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(launch_indexer_front(to_args(batch), q_c, x, w_q, w_k, w_w, q_fp8, q_scale,
+                                            w, index_pages, q_f32, k_f32, dev_status,
+                                            (cudaStream_t)stream));
 }
 
 dsa_status dsa_test_sparse_mla_wait_timeout(const dsa_batch* batch, const uint16_t* q_lat,

@@ -708,6 +708,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     if (warp == C::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
+}  // namespace
+
+// The driver's tensor-map encoder, looked up once (shared with front.cu).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -723,6 +726,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     });
     return fn;
 }
+
+namespace {
 
 // 2-D byte tensor [rows, 128] with 128-byte rows, box [box_rows, 128], 128-B swizzle.
 bool encode_rows128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t box_rows) {

@@ -263,6 +263,37 @@ dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,
                             void* latent_pages, dsa_key_format key_format,
                             int32_t* dev_status, dsa_stream_t stream);
 
+/* ---- fused indexer front --------------------------------------------------------
+ * Section "Fused low-latency decode for DSA layers", second step: one kernel
+ * does the query norm, the indexer query projection, FP8 quantisation with the
+ * head weights folded in, and the new token's index key.  The pages give no
+ * dimensions or formulas; this library reads them as follows, for each of the
+ * batch's T query tokens (all matrices bf16, row-major):
+ *   q_c  [T, 1536]   the token's query latent
+ *   x    [T, 7168]   the token's hidden state
+ *   w_q  [4096, 1536] indexer query projection (the query norm's gain folded in)
+ *   w_k  [128, 7168]  index-key projection
+ *   w_w  [32, 7168]   head-weight projection
+ *   inv_rms = 1 / sqrt(mean(q_c^2) + 1e-6)
+ *   q[t, h, :] = inv_rms * (w_q q_c)[128 h .. 128 h + 127]
+ *   q_fp8[t, h, :] = E4M3(q / q_scale[t, h]),  q_scale[t, h] = amax(|q[t, h, :]|) / 448
+ *   w[t, h] = (w_w x)[h]            (the indexer applies w * q_scale per head)
+ *   key = w_k x -> 128 E4M3 codes with scale amax / 448, written into the token's
+ *                  slot of the FP8 index cache (position seq_lens[b] - n_b + j,
+ *                  as dsa_append_cache places it); index_pages may be NULL
+ * Quantisation: the scale is 1 when amax is 0; codes are round-to-nearest-even
+ * saturating of x / scale (fp32 division), as in dsa_append_cache.
+ *   q_fp8 [T, 32, 128], q_scale [T, 32], w [T, 32]: outputs (16-byte aligned)
+ *   q_f32 [T, 4096], k_f32 [T, 128]: optional fp32 outputs of the projections
+ *          before quantisation (NULL to skip), for checking the codes
+ * The outputs q_fp8, q_scale and w are the indexer's inputs (dsa_index_scores).
+ * An MXFP4 index pool returns DSA_ERR_UNSUPPORTED for the key write. */
+dsa_status dsa_indexer_front(const dsa_batch* batch, const uint16_t* q_c, const uint16_t* x,
+                             const uint16_t* w_q, const uint16_t* w_k, const uint16_t* w_w,
+                             uint8_t* q_fp8, float* q_scale, float* w, void* index_pages,
+                             dsa_key_format key_format, float* q_f32, float* k_f32,
+                             int32_t* dev_status, dsa_stream_t stream);
+
 /* ---- decode context parallelism: exact top-k merge and LSE combine ---------------
  * Section "Decode context parallelism with the sparse indexer": with DCP over
  * W ranks, rank r holds every W-th token (positions s = r mod W) and ranks only
