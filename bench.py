@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-seconds", type=float, default=1.5,
                     help="extra untimed replay while GPU clocks are sampled")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the NVFP4 / DCP / fused-front measurements")
     return ap.parse_args()
 
 
@@ -519,6 +521,12 @@ def run_ours(args, rank, world, local):
                     "kernels_frac": {k: kbytes[k] / kern[k] / 1e9 / hbm for k in kern},
                     "source_hashes": hashes}
 
+    # ---- the other rows of the path, on the same workload --------------------
+    extras = None
+    if rank == 0 and not args.no_extras and not append:
+        extras = measure_extras(args, dsa, di, wl, lens, q_counts, fmt, seed, L, layers, batches,
+                                scores, ld, idx, stream, time_graph, hbm, bf16)
+
     # ---- end to end through the public API with host buffers --------------
     # per step: one pinned-host -> device copy of the step's inputs (queries
     # and request metadata packed in one staging buffer), the step, and one
@@ -623,13 +631,87 @@ def run_ours(args, rank, world, local):
                 "step_hbm_gbs": step_b / (elapsed / args.steps) / 1e9,
                 "step_frac": step_b / (elapsed / args.steps) / 1e9 / hbm,
                 "step_bytes": step_b,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "extras": extras,
                 "gpu_launches": gpu_launches, "clocks": clocks}
         print(json.dumps(line))
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def measure_extras(args, dsa, di, wl, lens, q_counts, fmt, seed, L, layers, batches, scores, ld,
+                   idx, stream, time_graph, hbm, bf16):
+    """Per-launch times of the other rows of the path on the bench workload,
+    each timed like the step's kernels (graphs of L launches, CUDA events):
+    sparse MLA over NVFP4 latents, the DCP merge for W = 8 ranks with the
+    per-rank attention and LSE combine, and the fused indexer front."""
+    import torch
+    dev = scores.device
+    T = sum(q_counts)
+    reps = max(3, min(50, args.steps // L))
+    out = {}
+    # NVFP4 latents: same requests and page placement, 352-B latent pages
+    nv = [di.make_layer(lens, q_counts, fmt, seed + 7919 * (l + 1), device=dev,
+                        latent_format=di.LATENT_NVFP4) for l in range(L)]
+    o = torch.empty(T, 96, 512, dtype=torch.bfloat16, device=dev)
+    ls = torch.empty(T, 96, dtype=torch.float32, device=dev)
+    mws = torch.empty(max(16, dsa.dsa_sparse_mla_workspace_size(batches[0])), dtype=torch.uint8,
+                      device=dev)
+    t_nv = time_graph(lambda i: dsa.dsa_sparse_mla_ex(
+        batches[i], nv[i].q_lat, nv[i].latent_pages, dsa.LATENT_NVFP4, nv[i].kv_scale,
+        nv[i].sm_scale, idx, dsa.TOPK, o, ls, mws, stream=stream), reps)
+    b_nv = wl.mla_bytes(lens, q_counts, wl.NVFP4_LATENT_BYTES)
+    out["sparse_mla_nvfp4"] = {"us": t_nv * 1e6, "algorithmic_bytes": b_nv,
+                               "gbs": b_nv / t_nv / 1e9, "frac_of_hbm": b_nv / t_nv / 1e9 / hbm}
+    del nv
+    # DCP, W = 8: candidate merge on the step's scores, then per-rank attention
+    W = 8
+    if max(lens) <= 65536 * W:
+        cand = -(-3 * dsa.TOPK // (2 * W))
+        didx = torch.empty(T, dsa.TOPK, dtype=torch.int32, device=dev)
+        ridx = torch.empty(W, T, dsa.TOPK, dtype=torch.int32, device=dev)
+        res = torch.zeros(T, W, dtype=torch.int32, device=dev)
+        dws = torch.empty(dsa.dsa_dcp_topk_workspace_size(batches[0], W), dtype=torch.uint8,
+                          device=dev)
+        # the scores buffer holds the last layer's rows
+        j = L - 1
+        t_merge = time_graph(lambda i: dsa.dsa_dcp_topk(batches[j], scores, ld, W, 0, dsa.TOPK,
+                                                        didx, ridx, res, dws, stream=stream), reps)
+        parts = torch.empty(W, T, 96, 512, dtype=torch.bfloat16, device=dev)
+        plse = torch.empty(W, T, 96, dtype=torch.float32, device=dev)
+
+        def attend(i):
+            for r in range(W):
+                dsa.dsa_sparse_mla(batches[j], layers[j].q_lat, layers[j].latent_pages,
+                                   layers[j].kv_scale, layers[j].sm_scale, ridx[r], dsa.TOPK,
+                                   parts[r], plse[r], mws, stream=stream)
+            dsa.dsa_lse_combine(T, W, parts, plse, o, ls, stream=stream)
+        t_att = time_graph(attend, max(3, reps // 4))
+        ex_c, ex_g = wl.dcp_exchange_bytes(W, cand)
+        out["dcp8"] = {"merge_us": t_merge * 1e6, "attention_and_combine_us": t_att * 1e6,
+                       "resent_row_rank_fraction": float(res.float().mean().item()),
+                       "exchange_bytes_per_row": ex_c, "generic_merge_bytes_per_row": ex_g,
+                       "exchange_reduction": ex_g / ex_c,
+                       "note": "W ranks emulated on one GPU: the exchange is a device buffer"}
+    # fused indexer front for the workload's T tokens (synthetic projections)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    mk = lambda *sh, k: (torch.randn(*sh, generator=g, device=dev) / k ** 0.5).to(torch.bfloat16)
+    q_c = torch.randn(T, wl.FRONT_QLAT, generator=g, device=dev).to(torch.bfloat16)
+    x = torch.randn(T, wl.FRONT_HIDDEN, generator=g, device=dev).to(torch.bfloat16)
+    w_q, w_k, w_w = mk(4096, wl.FRONT_QLAT, k=wl.FRONT_QLAT), mk(128, wl.FRONT_HIDDEN, k=wl.FRONT_HIDDEN), \
+        mk(32, wl.FRONT_HIDDEN, k=wl.FRONT_HIDDEN)
+    q8 = torch.empty(T, 32, 128, dtype=torch.uint8, device=dev)
+    qs = torch.empty(T, 32, dtype=torch.float32, device=dev)
+    ww = torch.empty(T, 32, dtype=torch.float32, device=dev)
+    pages = layers[0].index_pages.clone() if fmt == di.KEYS_FP8 else None
+    t_front = time_graph(lambda i: dsa.dsa_indexer_front(batches[0], q_c, x, w_q, w_k, w_w, q8, qs,
+                                                         ww, pages, fmt, stream=stream), reps)
+    fb, ff = wl.front_bytes(T), wl.front_flops(T)
+    out["indexer_front"] = {"us": t_front * 1e6, "algorithmic_bytes": fb, "flops": ff,
+                            "frac_of_hbm": fb / t_front / 1e9 / hbm,
+                            "frac_of_bf16_tensor": ff / t_front / 1e12 / bf16}
+    return out
 
 
 def main():

@@ -100,6 +100,29 @@ __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t need, 
     above = __shfl_sync(0xffffffffu, c, src);
 }
 
+// Shared-memory histogram increment aggregated over the warp: lanes with the
+// same bin are counted by one atomic (the top digits of BF16 keys take few
+// distinct values, so unaggregated atomics would serialise on a few bins).
+// Called by every lane of the warp; `active` lanes contribute.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active, int lane) {
+    const unsigned am = __ballot_sync(0xffffffffu, active);
+    if (active) {
+        const unsigned peers = __match_any_sync(am, bin);
+        if ((int)(__ffs(peers) - 1) == lane) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+    }
+}
+
+// Rank and rank-local index of position s (shifts when W is a power of two).
+__device__ __forceinline__ void rank_of(int s, int W, int lw, int& r, uint32_t& i) {
+    if (lw >= 0) {
+        r = s & (W - 1);
+        i = (uint32_t)(s >> lw);
+    } else {
+        r = s % W;
+        i = (uint32_t)(s / W);
+    }
+}
+
 // Local top-C of every rank of row t (kResend: only flagged ranks, C = K).
 template <bool kResend>
 __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpArgs a) {
@@ -115,6 +138,7 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
     if (!token_ok(a.bt, b, t, nullptr)) return;
     const int vis = visible_of(a.bt, b, t);
     const float* row = a.scores + (int64_t)t * a.ld;
+    const int lw = (W & (W - 1)) == 0 ? __ffs(W) - 1 : -1;
     if (tid < W) {
         const int r = tid;
         const int n_r = vis > r ? (vis - 1 - r) / W + 1 : 0;
@@ -141,12 +165,21 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
         const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
         for (int i = tid; i < W * 256; i += kDcpThreads) (&s_hist[0][0])[i] = 0u;
         __syncthreads();
-        for (int s = tid; s < vis; s += kDcpThreads) {
-            const int r = s % W;
-            if (s_mode[r] != 1) continue;
-            const uint32_t comp = (bf16_key(__ldcg(row + s)) << 16) | (0xFFFFu - (uint32_t)(s / W));
-            if ((comp & hi_mask) == (s_prefix[r] & hi_mask))
-                atomicAdd(&s_hist[r][(comp >> shift) & 255u], 1u);
+        for (int base = 0; base < vis; base += kDcpThreads) {  // warp-uniform trip count
+            const int s = base + tid;
+            bool act = false;
+            uint32_t bin = 0;
+            if (s < vis) {
+                int r;
+                uint32_t i;
+                rank_of(s, W, lw, r, i);
+                if (s_mode[r] == 1) {
+                    const uint32_t comp = (bf16_key(__ldcg(row + s)) << 16) | (0xFFFFu - i);
+                    act = (comp & hi_mask) == (s_prefix[r] & hi_mask);
+                    bin = (uint32_t)r * 256u + ((comp >> shift) & 255u);
+                }
+            }
+            hist_add(&s_hist[0][0], bin, act, lane);
         }
         __syncthreads();
         if (warp < W && s_mode[warp] == 1) {
@@ -163,9 +196,10 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
     uint32_t* out = kResend ? a.full : a.sent;
     const int stride = kResend ? a.K : a.cand;
     for (int s = tid; s < vis; s += kDcpThreads) {
-        const int r = s % W;
+        int r;
+        uint32_t i;
+        rank_of(s, W, lw, r, i);
         if (s_mode[r] == 0) continue;
-        const uint32_t i = (uint32_t)(s / W);
         const uint32_t k = bf16_key(__ldcg(row + s));
         const uint32_t comp = (k << 16) | (0xFFFFu - i);
         const uint32_t tau = s_mode[r] == 2 ? 0u : s_prefix[r];
@@ -273,9 +307,11 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a)
             const unsigned long long hi_mask = level == 0 ? 0ull : (~0ull << (shift + 8));
             if (tid < 256) sm.hist[tid] = 0u;
             __syncthreads();
-            for (int j = tid; j < N; j += kDcpThreads) {
-                const unsigned long long c = sm.cand[j];
-                if ((c & hi_mask) == (sm.prefix & hi_mask)) atomicAdd(&sm.hist[(c >> shift) & 255u], 1u);
+            for (int base = 0; base < N; base += kDcpThreads) {  // warp-uniform trip count
+                const int j = base + tid;
+                const unsigned long long c = j < N ? sm.cand[j] : 0ull;
+                const bool act = j < N && (c & hi_mask) == (sm.prefix & hi_mask);
+                hist_add(sm.hist, (uint32_t)((c >> shift) & 255u), act, lane);
             }
             __syncthreads();
             if (warp == 0) {

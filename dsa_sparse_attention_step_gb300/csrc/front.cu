@@ -15,22 +15,32 @@
 // (the indexer applies w * q_scale per head: the fold of the head weights into
 // the quantised query).
 //
-// One CTA = one output tile (32 query heads, the key, the head weights) x 64
-// tokens: D[128 features x 64 tokens] = W_tile[128 x K] . X[64 x K]^T with
-// tcgen05.mma kind::f16 (bf16 x bf16, fp32 accumulator in TMEM), operands by
-// TMA (128-byte swizzle) into a 6-stage ring.  Warp 0 issues the copies, warp
-// 1 the MMAs, warp 2 (query tiles) sums the squares of the query latents from
-// the same shared-memory tiles, warps 4-7 run the epilogue (thread = feature,
-// one TMEM lane each): per-token amax over the tile's 128 features by warp
-// max-reductions, the scale, the E4M3 codes (fp32 division, round to nearest
-// even, saturating) and the stores.  Every wait is bounded.
+// One CTA = one output tile x 128 tokens: D[128 features x 128 tokens] =
+// W_tile[128 x K] . X[128 x K]^T with tcgen05.mma kind::f16 (bf16 x bf16, fp32
+// accumulator in TMEM), operands by TMA (128-byte swizzle) into a 6-stage ring.
+// The grid is launched as clusters of 8 CTAs: 4 clusters of query heads (8
+// heads each, K = 1536), then the key and the head weights (K = 7168), each
+// split over the 8 CTAs of its cluster by K (896 each); after its K range a
+// split CTA leaves its fp32 partial in shared memory and rank 0 of the cluster
+// adds the 8 partials in rank order through distributed shared memory (a fixed
+// order: the result does not depend on timing) before the epilogue.
+// Warp 0 issues the copies, warp 1 the MMAs, warp 2 (query tiles) sums the
+// squares of the query latents from the same shared-memory tiles, warps 4-7
+// run the epilogue (thread = feature, one TMEM lane each) in two halves of 64
+// tokens: per-token amax over the tile's 128 features by warp max-reductions,
+// the scale, the E4M3 codes (fp32 division, round to nearest even, saturating)
+// and the stores.  Every wait is bounded.
 #include <cstring>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "sm100.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 
@@ -42,19 +52,21 @@ using namespace sm100;
 
 constexpr int kDq = 1536;              // query latent
 constexpr int kDh = 7168;              // hidden state
-constexpr int kFTok = 64;              // tokens per CTA (MMA N)
+constexpr int kFTok = 128;             // tokens per CTA (MMA N)
+constexpr int kFHalf = 64;             // epilogue columns per pass
 constexpr int kFStages = 6;
 constexpr int kFAStage = 128 * 128;    // 128 rows x 64 bf16
-constexpr int kFBStage = kFTok * 128;  // 64 tokens x 64 bf16
+constexpr int kFBStage = kFTok * 128;  // 128 tokens x 64 bf16
 constexpr int kFThreads = 256;
+constexpr int kFCluster = 8;           // CTAs per cluster; K splits of the x tiles
 constexpr int kTilesQ = kIdxHeads;     // 32 query tiles (one head each)
-constexpr int kTileKey = kTilesQ;      // 32
-constexpr int kTileW = kTilesQ + 1;    // 33
-constexpr int kFTiles = kTilesQ + 2;   // 34
+constexpr int kTileKey = kTilesQ;      // 32: key, split 8 ways (CTAs 32..39)
+constexpr int kTileW = kTilesQ + 1;    // 33: head weights (CTAs 40..47)
+constexpr int kFGridX = kTilesQ + 2 * kFCluster;  // 48
 constexpr int kFOffA = 0;
 constexpr int kFOffB = kFOffA + kFStages * kFAStage;
-constexpr int kFOffF = kFOffB + kFStages * kFBStage;   // floats: inv_rms[64], amax[4][64]
-constexpr int kFOffSlot = kFOffF + (kFTok + 4 * kFTok) * 4;  // int64 key slot per token
+constexpr int kFOffF = kFOffB + kFStages * kFBStage;   // floats: inv_rms[128], amax[4][64]
+constexpr int kFOffSlot = kFOffF + (kFTok + 4 * kFHalf) * 4;  // int64 key slot per token
 constexpr int kFOffBar = kFOffSlot + kFTok * 8;
 constexpr int kFSmemAlloc = kFOffBar + 256 + 1024;
 static_assert(kFSmemAlloc <= 227 * 1024, "shared memory budget");
@@ -97,11 +109,12 @@ indexer_front_kernel(const __grid_constant__ CUtensorMap tm_wq,
     int64_t* sSlot = reinterpret_cast<int64_t*>(sm + kFOffSlot);
     FrontBars* bars = reinterpret_cast<FrontBars*>(sm + kFOffBar);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x;
+    const bool is_q = (int)blockIdx.x < kTilesQ;
+    const int tile = is_q ? (int)blockIdx.x : kTilesQ + ((int)blockIdx.x - kTilesQ) / kFCluster;
+    const int split = is_q ? 0 : ((int)blockIdx.x - kTilesQ) % kFCluster;  // = cluster rank
     const int t0 = blockIdx.y * kFTok;
-    const bool is_q = tile < kTilesQ;
-    const int K = is_q ? kDq : kDh;
-    const int nk = K / 64;
+    const int nk = is_q ? kDq / 64 : kDh / 64 / kFCluster;   // 24 or 14 chunks
+    const int kc0 = split * nk;
     const CUtensorMap* tmA = is_q ? &tm_wq : (tile == kTileKey ? &tm_wk : &tm_ww);
     const CUtensorMap* tmB = is_q ? &tm_qc : &tm_x;
     const uint32_t a_bytes = (tile == kTileW) ? (uint32_t)(kIdxHeads * 128) : (uint32_t)kFAStage;
@@ -126,7 +139,7 @@ indexer_front_kernel(const __grid_constant__ CUtensorMap tm_wq,
     }
     // key slots of this CTA's tokens (byte offset of the token's key in the
     // index pool, -1 when absent or out of range)
-    if (tile == kTileKey && tid < kFTok) {
+    if (tile == kTileKey && split == 0 && tid < kFTok) {
         int64_t off = -1;
         const int t = t0 + tid;
         if (t < p.T && p.index_pages) {
@@ -154,8 +167,8 @@ indexer_front_kernel(const __grid_constant__ CUtensorMap tm_wq,
                     !mbar_wait(&bars->empty[st], ((kc / kFStages) - 1) & 1, abort_flag))
                     break;
                 mbar_arrive_expect_tx(&bars->full[st], a_bytes + b_bytes);
-                tma_load_2d(sA + st * kFAStage, tmA, kc * 64, is_q ? tile * 128 : 0, &bars->full[st]);
-                tma_load_2d(sB + st * kFBStage, tmB, kc * 64, t0, &bars->full[st]);
+                tma_load_2d(sA + st * kFAStage, tmA, (kc0 + kc) * 64, is_q ? tile * 128 : 0, &bars->full[st]);
+                tma_load_2d(sB + st * kFBStage, tmB, (kc0 + kc) * 64, t0, &bars->full[st]);
                 last = kc;
             }
             // the copies must have landed before the CTA exits
@@ -188,14 +201,14 @@ indexer_front_kernel(const __grid_constant__ CUtensorMap tm_wq,
         __syncwarp();
     } else if (warp == 2 && is_q) {
         // ---------------- query norm: sum of squares per token ----------------
-        // lane l takes tokens l and l + 32 of each 64-element chunk
-        float ss[2] = {0.f, 0.f};
+        // lane l takes tokens l, l + 32, l + 64, l + 96 of each 64-element chunk
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kc = 0; kc < nk; ++kc) {
             const int st = kc % kFStages;
             if (!mbar_wait(&bars->full[st], (kc / kFStages) & 1, abort_flag)) break;
             const uint8_t* tileB = sB + st * kFBStage;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < 4; ++h) {
                 const int r = lane + 32 * h;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -212,55 +225,91 @@ indexer_front_kernel(const __grid_constant__ CUtensorMap tm_wq,
             if (lane == 0) mbar_arrive(&bars->empty[st]);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) sInv[lane + 32 * h] = 1.0f / sqrtf(ss[h] / (float)kDq + 1e-6f);
+        for (int h = 0; h < 4; ++h) sInv[lane + 32 * h] = 1.0f / sqrtf(ss[h] / (float)kDq + 1e-6f);
     }
 
     // ---------------- epilogue (warps 4-7: thread = feature row) ----------------
     __syncthreads();  // the norm warp's 1/rms are in shared memory
+    const int q4 = warp & 3;
+    const int d = 32 * q4 + lane;  // feature row of the tile
+    bool ok = true;
     if (warp >= 4) {
-        const int q4 = warp & 3;
-        const int d = 32 * q4 + lane;  // feature row of the tile
-        const bool ok = mbar_wait(&bars->done, 0, abort_flag);
+        ok = mbar_wait(&bars->done, 0, abort_flag);
         tc_fence_after();
-        uint32_t v[64];
-        if (ok) {
-            tmem_ld32(tmem_addr(tmem, 32 * q4, 0), *reinterpret_cast<uint32_t(*)[32]>(v));
-            tmem_ld32(tmem_addr(tmem, 32 * q4, 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            tmem_wait_ld();
-        }
-        if (tile == kTileW) {
-            if (ok && q4 == 0 && p.w) {
+    }
+    // split tiles: each CTA's fp32 partial [128 rows][128 tokens] goes to its
+    // own shared memory (the operand ring is idle now), rank 0 adds them
+    float* sPart = reinterpret_cast<float*>(sA);
+    if (!is_q) {
+        if (warp >= 4 && ok) {
+            for (int c = 0; c < kFTok; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_addr(tmem, 32 * q4, c), v);
+                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < kFTok; ++j)
-                    if (t0 + j < p.T) p.w[(int64_t)(t0 + j) * kIdxHeads + d] = __uint_as_float(v[j]);
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(sPart + d * kFTok + c + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
             }
-        } else if (ok) {
+        }
+        cg::this_cluster().sync();  // every partial is written
+    }
+    if (warp >= 4 && ok && (is_q || split == 0)) {
+        for (int half = 0; half < kFTok / kFHalf; ++half) {
+            const int c0 = half * kFHalf;
+            float v[kFHalf];
             if (is_q) {
+                uint32_t u[kFHalf];
+                tmem_ld32(tmem_addr(tmem, 32 * q4, c0), *reinterpret_cast<uint32_t(*)[32]>(u));
+                tmem_ld32(tmem_addr(tmem, 32 * q4, c0 + 32), *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < kFTok; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * sInv[j]);
+                for (int j = 0; j < kFHalf; ++j) v[j] = __uint_as_float(u[j]) * sInv[c0 + j];
+            } else {
+                // the 8 partials of this row, added in rank order
+#pragma unroll
+                for (int j = 0; j < kFHalf; ++j) v[j] = 0.f;
+                cg::cluster_group cl = cg::this_cluster();
+                for (int r = 0; r < kFCluster; ++r) {
+                    const float* src = cl.map_shared_rank(sPart, r) + d * kFTok + c0;
+#pragma unroll
+                    for (int j = 0; j < kFHalf; j += 4) {
+                        const float4 x4 = *reinterpret_cast<const float4*>(src + j);
+                        v[j] += x4.x; v[j + 1] += x4.y; v[j + 2] += x4.z; v[j + 3] += x4.w;
+                    }
+                }
+            }
+            if (tile == kTileW) {
+                if (q4 == 0 && p.w) {
+#pragma unroll
+                    for (int j = 0; j < kFHalf; ++j)
+                        if (t0 + c0 + j < p.T) p.w[(int64_t)(t0 + c0 + j) * kIdxHeads + d] = v[j];
+                }
+                continue;
             }
             // per-token amax over the 128 features: |x| compares as unsigned
 #pragma unroll
-            for (int j = 0; j < kFTok; ++j) {
-                const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(__uint_as_float(v[j])) & 0x7FFFFFFFu);
-                if (lane == 0) sAmax[q4 * kFTok + j] = __uint_as_float(m);
+            for (int j = 0; j < kFHalf; ++j) {
+                const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                if (lane == 0) sAmax[q4 * kFHalf + j] = __uint_as_float(m);
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll
-            for (int j = 0; j < kFTok; ++j) {
-                const int t = t0 + j;
+            for (int j = 0; j < kFHalf; ++j) {
+                const int t = t0 + c0 + j;
                 if (t >= p.T) continue;
-                const float amax = fmaxf(fmaxf(sAmax[j], sAmax[kFTok + j]),
-                                         fmaxf(sAmax[2 * kFTok + j], sAmax[3 * kFTok + j]));
+                const float amax = fmaxf(fmaxf(sAmax[j], sAmax[kFHalf + j]),
+                                         fmaxf(sAmax[2 * kFHalf + j], sAmax[3 * kFHalf + j]));
                 const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-                const float x = __uint_as_float(v[j]);
+                const float x = v[j];
                 const uint8_t code = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
                 if (is_q) {
                     p.q8[(int64_t)t * (kIdxHeads * kIdxDim) + tile * kIdxDim + d] = code;
                     if (p.q_f32) p.q_f32[(int64_t)t * (kIdxHeads * kIdxDim) + tile * kIdxDim + d] = x;
                     if (d == 0) p.qscale[(int64_t)t * kIdxHeads + tile] = scale;
                 } else {
-                    const int64_t off = sSlot[j];
+                    const int64_t off = sSlot[c0 + j];
                     if (off >= 0) {
                         p.index_pages[off + d] = code;
                         if (d == 0) {
@@ -272,8 +321,10 @@ indexer_front_kernel(const __grid_constant__ CUtensorMap tm_wq,
                     if (p.k_f32) p.k_f32[(int64_t)t * kIdxDim + d] = x;
                 }
             }
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // sAmax is reused by the next half
         }
     }
+    if (!is_q) cg::this_cluster().sync();  // rank 0 has read every partial
 
     tc_fence_before();
     __syncthreads();
@@ -328,9 +379,9 @@ cudaError_t launch_indexer_front(const BatchArgs& bt, const uint16_t* q_c, const
     cudaError_t e = cudaFuncSetAttribute(indexer_front_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmemAlloc);
     if (e != cudaSuccess) return e;
-    const dim3 grid(kFTiles, (unsigned)((T + kFTok - 1) / kFTok));
+    const dim3 grid(kFGridX, (unsigned)((T + kFTok - 1) / kFTok));
     return launch_kernel(indexer_front_kernel, grid, dim3(kFThreads), (size_t)kFSmemAlloc, stream,
-                         false, 1, tm_wq, tm_wk, tm_ww, tm_qc, tm_x, p);
+                         false, kFCluster, tm_wq, tm_wk, tm_ww, tm_qc, tm_x, p);
 }
 
 }  // namespace dsa

@@ -37,6 +37,8 @@
 // allocation and the single MMA-issuing thread; all eight warps share the
 // epilogue (thread = latent dim), which stages the result in shared memory and
 // writes it with one bulk copy.  Every wait is bounded.
+#include <cuda_fp4.h>
+
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -143,19 +145,15 @@ __device__ __forceinline__ void e4m3x8_to_f16x8(uint32_t w0, uint32_t w1, uint32
 }
 
 // Eight packed E2M1 elements (element 2i in the low nibble of byte i) -> eight
-// f16 values, exact.  Every E2M1 magnitude (0, 0.5, 1, 1.5, 2, 3, 4, 6) is an
-// f16 whose low byte is zero, so one byte-permute per pair picks the two high
-// bytes from a table and zero low bytes; the sign bits are moved to bits 15
-// and 31.
+// f16 values, exact (every E2M1 value is an f16 value): one hardware
+// conversion per byte.
 __device__ __forceinline__ uint4 e2m1x8_to_f16x8(uint32_t w) {
-    constexpr uint32_t kHiLo = 0x3E3C3800u;  // f16 high bytes of magnitudes 0..3
-    constexpr uint32_t kHiHi = 0x46444240u;  // magnitudes 4..7
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t byte = (w >> (8 * j)) & 0xFFu;
-        const uint32_t sel = ((byte & 0x7u) << 4) | ((byte & 0x70u) << 8);
-        o[j] = __byte_perm(kHiLo, kHiHi, sel) | ((byte & 0x8u) << 12) | ((byte & 0x80u) << 24);
+        const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w >> (8 * j)) & 0xFFu),
+                                                         __NV_E2M1);
+        o[j] = (uint32_t)h.x | ((uint32_t)h.y << 16);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -326,6 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
     const uint32_t tmem = bars->tmem_base;
     // z in log2 units per unit of the f16 accumulator
     const float zscale = p.sm_scale * p.kv_scale * ldexpf(1.0f, e) * 1.4426950408889634f;
+    // tiles after the last one holding a selected position have only empty
+    // slots (p = 0, zero latents): every role stops before them, which leaves
+    // the result bit-for-bit unchanged
+    int n_used = n_tiles;
+    while (n_used > 0 && sMask[n_used - 1] == 0ull) --n_used;
 
     if (warp >= 4 && warp < kMmaWarp) {
         // ---------------- producers: gather + E4M3 -> f16 ----------------
@@ -416,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         *reinterpret_cast<uint4*>(base + sw128(r, (c & 3) * 32 + 16)) =         \
             make_uint4(h1[0], h1[1], h1[2], h1[3]);                             \
     }
-        if (n_tiles > 0) {
+        if (n_used > 0) {
             const int ptv = pt;
 #pragma unroll
             for (int g = 0; g < kGroups; ++g) {
@@ -425,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             }
         }
         bool ok = true;
-        for (int i = 0; i < n_tiles && ok; ++i) {
+        for (int i = 0; i < n_used && ok; ++i) {
             // index arithmetic is redone every tile rather than kept live
             int ptv = pt;
             asm volatile("" : "+r"(ptv));
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 else { DSA_NV_STORE(g) }
                 fence_proxy_async_smem();
                 if (!(kWaitTest && i == 0 && g == 4)) mbar_arrive(&bars->lfull[g]);
-                if (i + 1 < n_tiles) {
+                if (i + 1 < n_used) {
                     if constexpr (kLat == 0) { DSA_MLA_LOAD(i + 1, g) }
                     else { DSA_NV_LOAD(i + 1, g) }
                 }
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             const uint64_t vd = smem_desc(smem_u32(sL), kLSlabBytes, 1024, kSwizzle128B);
             const uint64_t pd = smem_desc(smem_u32(sP), 16, 1024, kSwizzle128B);
             bool ok = true;
-            for (int i = 0; i < n_tiles && ok; ++i) {
+            for (int i = 0; i < n_used && ok; ++i) {
                 // S = Q . L^T, slab group by slab group as the producers fill them
 #pragma unroll
                 for (int g = 0; g < kGroups; ++g) {
@@ -511,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         // ---------------- softmax (thread = head) ----------------
         const int h = tid;  // 0..127; rows 96..127 (warp 3) are padding
         float m_ref = -INFINITY, l = 0.f;
-        for (int i = 0; i < n_tiles; ++i) {
+        for (int i = 0; i < n_used; ++i) {
             if (!mbar_wait<kBudget>(&bars->sfull, i & 1, abort_flag)) break;
             tc_fence_after();
             // S(i) is complete and so is every earlier O^T update; nothing

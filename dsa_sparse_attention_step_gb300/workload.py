@@ -44,14 +44,37 @@ def topk_bytes(seq_lens, q_counts):
     return tot
 
 
-def mla_bytes(seq_lens, q_counts):
-    """Latents of each query token's selection plus its MLA query."""
+def mla_bytes(seq_lens, q_counts, latent_bytes=LATENT_BYTES):
+    """Latents of each query token's selection plus its MLA query (latent_bytes
+    per key: 576 FP8, 352 NVFP4)."""
     tot = 0
     for s, n in zip(seq_lens, q_counts):
         for j in range(n):
             vis = s - n + j + 1
-            tot += min(TOPK, vis) * LATENT_BYTES + QUERY_BYTES_MLA
+            tot += min(TOPK, vis) * latent_bytes + QUERY_BYTES_MLA
     return tot
+
+
+NVFP4_LATENT_BYTES = 352
+FRONT_QLAT, FRONT_HIDDEN = 1536, 7168
+
+
+def front_bytes(T):
+    """Fused indexer front: the projections (bf16) once, each token's query
+    latent and hidden state (bf16), and its outputs (q8, q_scale, w, key)."""
+    weights = 2 * (4096 * FRONT_QLAT + (128 + 32) * FRONT_HIDDEN)
+    return weights + T * (2 * (FRONT_QLAT + FRONT_HIDDEN) + 4096 + 4 * 32 + 4 * 32 + 132)
+
+
+def front_flops(T):
+    return 2 * T * (4096 * FRONT_QLAT + (128 + 32) * FRONT_HIDDEN)
+
+
+def dcp_exchange_bytes(world, cand, k=TOPK):
+    """Bytes one row puts on the wire in the candidate exchange (32-bit words
+    from every rank) and in a merge of every rank's full top-k as fp32 score +
+    int32 id pairs."""
+    return world * cand * 4, world * k * 8
 
 
 def indexer_flops(seq_lens, q_counts):
