@@ -22,14 +22,16 @@
 // and store fp32 scores.
 //
 // Roles: producer warps (each looks up pages and one lane issues the copies),
-// then MMA warps (the first allocates TMEM; lane 0 issues MMAs), then for FP8
-// keys twelve epilogue warps (three per TMEM lane quarter, each taking every
-// third token of a query group) -- 512 threads; for MXFP4 keys four converter
-// warps and eight epilogue warps -- 448 threads.  With FP8 keys there are two
-// producer and two MMA warps, each pair taking alternate units: one thread
-// spends about a thousand cycles of instruction latency on a unit's copies
-// (or on its waits, MMAs and commits), more than the unit's share of the
-// memory bandwidth allows.  Every wait is bounded.
+// then MMA warps (the first allocates TMEM; lane 0 issues MMAs), then for
+// MXFP4 keys four converter warps, then eight epilogue warps in two sets of
+// four (one warp per TMEM lane quarter): with FP8 keys a set takes every
+// second unit and all of its tokens (so a unit's bookkeeping runs on four
+// warps, and the two sets drain different accumulators at once); with MXFP4
+// keys a set takes every second token.  With FP8 keys and query groups of one
+// or two tokens there are two producer and two MMA warps, each pair taking
+// alternate units: one thread spends about a thousand cycles of instruction
+// latency on a unit's copies (or on its waits, MMAs and commits), more than
+// the unit's share of the memory bandwidth allows.  Every wait is bounded.
 #include <cstring>
 #include <mutex>
 
@@ -59,23 +61,29 @@ constexpr int kMetaBytes = 2 * kPage * 4;        // 512: the 64 scale words of t
 // and each 32-element block gets its own accumulator (its E8M0 scale is
 // applied in the epilogue), which limits a query group to 2 tokens.
 // kDual (FP8 keys, query groups of one or two tokens, where the epilogue
-// has time to spare): two producer and two MMA warps taking alternate units.
+// has time to spare): two MMA warps taking alternate units as well.
 template <int kFmt, bool kDual>
 struct IdxCfg {
     static constexpr bool kMx = (kFmt == DSA_KEYS_MXFP4);
     static_assert(!(kMx && kDual), "MXFP4 keys use one producer and one MMA warp");
-    static constexpr int kProdWarps = kDual ? 2 : 1;
+    // FP8 keys: two producer warps taking alternate units (one thread's copy
+    // issue for a unit takes longer than the unit's keys take to arrive);
+    // MXFP4 keys: one (the converters pace the stream)
+    static constexpr int kProdWarps = kMx ? 1 : 2;
     static constexpr int kMmaWarp = kProdWarps;    // allocates TMEM
     static constexpr int kMmaWarps = kDual ? 2 : 1;  // MMA-issuing threads (alternate units)
     static constexpr int kConvWarp0 = kMmaWarp + kMmaWarps;
     static constexpr int kConvWarps = kMx ? 4 : 0;
     static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
-    // FP8: 12 epilogue warps, three per TMEM lane quarter, each taking every
-    // third token of a group; MXFP4: 8 warps (registers), every second token
-    static constexpr int kEpiWarps = kMx ? 8 : 12;
+    // epilogue warps in sets of four (one warp per TMEM lane quarter).  FP8:
+    // a set takes whole units, round robin (two sets with two MMA threads,
+    // else one set per TMEM accumulator, so every accumulator is drained while
+    // the MMA fills another); MXFP4: two sets, each every second token
+    static constexpr int kEpiSets = (kMx || kDual) ? 2 : 3;
+    static constexpr int kEpiWarps = 4 * kEpiSets;
     static constexpr int kEpiThreads = kEpiWarps * 32;
-    static constexpr int kTokSplit = kEpiWarps / 4;            // token stride
-    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 512 (kDual) or 448
+    static constexpr int kTokSplit = 2;                        // MXFP4 token stride
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 384 (kDual), 480 or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
     // enough key bytes in flight per SM to cover the memory latency at full load
     static constexpr int kStages = kMx ? 6 : 8;
@@ -92,6 +100,23 @@ struct IdxCfg {
     static constexpr int kSmemAlloc = kOffBar + 512 + 1024;
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
 };
+
+// Scale words of a page that is absent (past the sequence) or out of range:
+// all bits set, which is NaN as an fp32 key scale and NaN in every E8M0 byte.
+// The producers copy them into the unit's scale slot in place of the page's
+// own, through the same barrier as the keys, and the epilogue masks every key
+// whose scale word reads so (valid key scales are positive).
+__device__ __align__(16) uint32_t g_absent_scales[kPage] = {
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu,
+    0xFFFFFFFFu};
 
 struct Bars {
     uint64_t full[kMaxStages];   // TMA / converters -> MMA: key tile ready
@@ -264,8 +289,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         }
         for (int i = 0; i < 6; ++i) {
             mbar_init(&bars->tfull[i], 1);
-            // FP8: the min(G, 3) warp groups that take items of a unit arrive
-            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : 128 * min(G, 3));
+            // FP8: the set of four warps that takes the unit arrives
+            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : 128);
         }
         for (int i = 0; i < kStgSlots; ++i) {
             mbar_init(&bars->sfull[i], 1);
@@ -392,8 +417,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 if (lane == 0 && go) {
                     uint32_t bytes = 0;
                     for (int h = 0; h < 2; ++h)
-                        if (pages[h] >= 0)
-                            bytes += (kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim) + kPage * 4;
+                        bytes += (pages[h] >= 0 ? (kMx ? kPage * kIdxDim / 2 : kPage * kIdxDim) : 0) +
+                                 kPage * 4;
                     // the 64 scale words of each page land in meta slot
                     // i % (S + 3), completing on the same barrier as the keys
                     uint8_t* meta = sMeta + (i % C::kMetaSlots) * kMetaBytes;
@@ -403,16 +428,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         if (go) {
                             last_issued = i;
                             mbar_arrive_expect_tx(&bars->full[st], bytes);
-                            for (int h = 0; h < 2; ++h)
-                                if (pages[h] >= 0) {
+                            for (int h = 0; h < 2; ++h) {
+                                if (pages[h] >= 0)
                                     tma_load_2d(sStage + st * kStageBytes + h * (kPage * kIdxDim),
                                                 &tm_keys, 0, pages[h] * (kFp8PageBytes / kIdxDim),
                                                 &bars->full[st]);
-                                    bulk_copy_g2s(meta + h * kPage * 4,
-                                                  p.pages + (int64_t)pages[h] * kFp8PageBytes +
-                                                      kPage * kIdxDim,
-                                                  (uint32_t)(kPage * 4), &bars->full[st]);
-                                }
+                                bulk_copy_g2s(meta + h * kPage * 4,
+                                              pages[h] >= 0 ? (const void*)(p.pages + (int64_t)pages[h] * kFp8PageBytes +
+                                                                            kPage * kIdxDim)
+                                                            : (const void*)g_absent_scales,
+                                              (uint32_t)(kPage * 4), &bars->full[st]);
+                            }
                         }
                     } else {
                         // packed E2M1 bytes of the two pages into a staging
@@ -426,16 +452,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         if (go) {
                             last_issued = i;
                             mbar_arrive_expect_tx(&bars->sfull[ss], bytes);
-                            for (int h = 0; h < 2; ++h)
-                                if (pages[h] >= 0) {
+                            for (int h = 0; h < 2; ++h) {
+                                if (pages[h] >= 0)
                                     bulk_copy_g2s(sStg + ss * kStgBytes + h * (kPage * kIdxDim / 2),
                                                   p.pages + (int64_t)pages[h] * kMxPageBytes,
                                                   (uint32_t)(kPage * kIdxDim / 2), &bars->sfull[ss]);
-                                    bulk_copy_g2s(meta + h * kPage * 4,
-                                                  p.pages + (int64_t)pages[h] * kMxPageBytes +
-                                                      kPage * kIdxDim / 2,
-                                                  (uint32_t)(kPage * 4), &bars->sfull[ss]);
-                                }
+                                bulk_copy_g2s(meta + h * kPage * 4,
+                                              pages[h] >= 0 ? (const void*)(p.pages + (int64_t)pages[h] * kMxPageBytes +
+                                                                            kPage * kIdxDim / 2)
+                                                            : (const void*)g_absent_scales,
+                                              (uint32_t)(kPage * 4), &bars->sfull[ss]);
+                            }
                         }
                     }
                 }
@@ -551,7 +578,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         // ---------------- epilogue (thread = key) ----------------
         const int etid = tid - 32 * C::kEpiWarp0;
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter..+31
-        const int half = (warp - C::kEpiWarp0) >> 2;  // warp group (FP8: 0..2, MXFP4: token parity)
+        const int half = (warp - C::kEpiWarp0) >> 2;  // warp set (FP8: unit parity, MXFP4: token parity)
         constexpr int kTS = C::kTokSplit;
         if (n_units > 0) {
             Cursor c;
@@ -560,12 +587,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             for (int i = 0; i < n_units; ++i) {
                 const int gtok0 = c.g * G;                    // first token of the group
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
-                // FP8: the (unit, token) items k = i * G + j go round-robin to
-                // the three warp groups (group k % 3), so with one or two
-                // tokens per unit different groups drain different
-                // accumulators at the same time.  j0 = this group's first token.
-                const int j0 = kMx ? half : (half - (i * G) % 3 + 3) % 3;
-                if (!kMx && j0 >= G) {  // no item of this unit (only when G < 3)
+                // FP8: the warp sets take whole units round robin (the
+                // per-unit bookkeeping runs on four warps, and the sets drain
+                // different accumulators at once); with one MMA thread there
+                // is a set per accumulator (a third set idles when only two
+                // accumulators fit)
+                if (!kMx && (kDual ? (i & 1) : (i % nacc)) != half) {
                     cursor_next(c, bt, G);
                     continue;
                 }
@@ -579,8 +606,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         }
                         asm volatile("bar.sync 2, %0;" ::"n"(C::kEpiThreads) : "memory");
                     } else {
-                        // each warp group keeps its own copy (barrier 3 + group
-                        // over its 128 threads, which follow the same units)
+                        // each warp set keeps its own copy (barrier 3 + set over
+                        // its 128 threads, which follow the same units)
                         float* wdst = sW + half * (8 * kIdxHeads);
                         asm volatile("bar.sync %0, 128;" ::"r"(3 + half) : "memory");
                         for (int e = etid - 128 * half; e < gr * kIdxHeads; e += 128) {
@@ -598,18 +625,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                       : sW + half * (8 * kIdxHeads);
                 const int s = c.tile * kTile + quarter * 32 + lane;
                 const bool in_seq = s < c.seq;
-                // page validity from the table (independent of the MMA wait)
-                bool page_ok = false;
-                if (in_seq) {
-                    const int pg2 = __ldg(bt.block_table + (int64_t)c.b * bt.max_pages + s / kPage);
-                    page_ok = pg2 >= 0 && pg2 < bt.num_pages;
-                }
                 const int acc = acc_of(i);
                 if (!mbar_wait(&bars->tfull[acc], use_of(i) & 1, abort_flag)) break;
                 tc_fence_after();
                 // the unit's scale words arrived with its keys (before tfull)
                 const uint32_t sw = reinterpret_cast<const uint32_t*>(
                     sMeta + (i % C::kMetaSlots) * kMetaBytes)[quarter * 32 + lane];
+                // a key of an absent or out-of-range page has all scale bits set
+                const bool page_ok = sw != 0xFFFFFFFFu;
                 float kscale = 0.f;                   // FP8: per-key scale
                 float bsc[4] = {0.f, 0.f, 0.f, 0.f};  // MXFP4: block scales 2^(e-127)
                 if (!kMx) {
@@ -622,49 +645,44 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     }
                 }
                 if (!kMx) {
-                    // the TMEM loads of two of this thread's tokens (half + 3k),
-                    // then one wait
-                  for (int jp = 0; jp < 2; ++jp) {
-                    if (j0 + 2 * kTS * jp >= gr) break;
-                    uint32_t v[2][32];
+                    // tokens two at a time: both TMEM loads, then one wait
+                    for (int j = 0; j < gr; j += 2) {
+                        uint32_t v[2][32];
+                        tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * j), v[0]);
+                        if (j + 1 < gr)
+                            tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * (j + 1)), v[1]);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int j = j0 + 2 * kTS * jp + kTS * jj;
-                        if (j < gr) tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * j), v[jj]);
-                    }
-                    tmem_wait_ld();
+                        for (int jj = 0; jj < 2; ++jj) {
+                            if (j + jj >= gr) break;
+                            const float4* w4 = reinterpret_cast<const float4*>(wq + (j + jj) * kIdxHeads);
+                            // four independent packed (f32x2) partial sums
+                            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int j = j0 + 2 * kTS * jp + kTS * jj;
-                        if (j >= gr) break;
-                        const float4* w4 = reinterpret_cast<const float4*>(wq + j * kIdxHeads);
-                        // four independent packed (f32x2) partial sums
-                        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-                        for (int h4 = 0; h4 < 8; ++h4) {
-                            const float4 ww = w4[h4];
-                            acc2[(2 * h4) & 3] = fma_f32x2(
-                                pack_f32x2(ww.x, ww.y),
-                                pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 0]), 0.f),
-                                           fmaxf(__uint_as_float(v[jj][4 * h4 + 1]), 0.f)),
-                                acc2[(2 * h4) & 3]);
-                            acc2[(2 * h4 + 1) & 3] = fma_f32x2(
-                                pack_f32x2(ww.z, ww.w),
-                                pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 2]), 0.f),
-                                           fmaxf(__uint_as_float(v[jj][4 * h4 + 3]), 0.f)),
-                                acc2[(2 * h4 + 1) & 3]);
-                        }
-                        const float sc = (((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
-                                           (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
-                                          ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
-                                           (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
-                        if (in_seq) {
-                            const int vis = c.seq - c.nb + gtok0 + j + 1;
-                            p.scores[(int64_t)(c.q0 + gtok0 + j) * p.ld + s] =
-                                (s < vis && page_ok) ? sc : -INFINITY;
+                            for (int h4 = 0; h4 < 8; ++h4) {
+                                const float4 ww = w4[h4];
+                                acc2[(2 * h4) & 3] = fma_f32x2(
+                                    pack_f32x2(ww.x, ww.y),
+                                    pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 0]), 0.f),
+                                               fmaxf(__uint_as_float(v[jj][4 * h4 + 1]), 0.f)),
+                                    acc2[(2 * h4) & 3]);
+                                acc2[(2 * h4 + 1) & 3] = fma_f32x2(
+                                    pack_f32x2(ww.z, ww.w),
+                                    pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 2]), 0.f),
+                                               fmaxf(__uint_as_float(v[jj][4 * h4 + 3]), 0.f)),
+                                    acc2[(2 * h4 + 1) & 3]);
+                            }
+                            const float sc = (((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
+                                               (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
+                                              ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
+                                               (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
+                            if (in_seq) {
+                                const int vis = c.seq - c.nb + gtok0 + j + jj + 1;
+                                p.scores[(int64_t)(c.q0 + gtok0 + j + jj) * p.ld + s] =
+                                    (s < vis && page_ok) ? sc : -INFINITY;
+                            }
                         }
                     }
-                  }
                 } else {
                     for (int j = half; j < gr; j += kTS) {
                         float x[32];
