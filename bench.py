@@ -260,7 +260,7 @@ def job_value(world, tokens_per_rank, steps, elapsed):
 # the value it was measured at.
 KERNEL_SOURCES = {
     "indexer": ["indexer_tc.cu", "common.cuh", "sm100.cuh"],
-    "topk": ["topk.cu", "common.cuh"],
+    "topk": ["topk.cu", "topk_rows.cu", "common.cuh", "sm100.cuh"],
     "sparse_mla": ["sparse_mla.cu", "common.cuh", "sm100.cuh"],
 }
 

@@ -9,11 +9,14 @@
 // position order.  Scores are mapped to order-preserving uint32 keys (-0
 // folded onto +0); tau denotes the k-th largest key.
 //
-// Three paths, by batch shape:
+// Four paths, by batch shape:
 //   - rows of at most 32,768 positions: one CTA per query token with the row
 //     resident in shared memory (topk_resident_kernel, below);
 //   - at most 8 query tokens over longer rows: every row split over the whole
 //     GPU by radix levels (topk_split_*, below);
+//   - more query tokens over rows of at most 2^18 positions: a sampled
+//     threshold, one candidate pass over all rows at once and a per-row exact
+//     select (topk_rows.cu);
 //   - otherwise one thread-block cluster of `cs` CTAs per query token, as
 //     follows.  CTA r owns a contiguous, 32-aligned slice of the positions.
 //   1. Threshold estimate.  A histogram over the top 12 key bits of a sample
@@ -1235,6 +1238,11 @@ cudaError_t launch_resident(const BatchArgs& bt, const float* scores, int64_t ld
 
 }  // namespace
 
+bool topk_rows_eligible(int total_q, int max_seq, bool split);
+size_t topk_rows_workspace_bytes(int total_q);
+cudaError_t launch_topk_rows(const BatchArgs& bt, const float* scores, int64_t ld, int K,
+                             int32_t* out, void* ws, bool pdl, cudaStream_t stream);
+
 // CTAs per query token for rows that stream from global memory: spread few
 // tokens over more SMs, and keep every slice within the per-CTA bitmap.
 int topk_cluster_size(int total_q, int max_seq) {
@@ -1246,19 +1254,27 @@ int topk_cluster_size(int total_q, int max_seq) {
 
 bool topk_supported(int max_seq) { return max_seq <= kSliceMax * kMaxCluster; }
 
-// Device scratch of the top-k: the split path's histograms and counts.
+// Device scratch of the top-k: the split path's histograms and counts, or the
+// many-rows path's thresholds and candidate lists.
 size_t topk_workspace_bytes(int total_q, int max_seq) {
+    if (topk_rows_eligible(total_q, max_seq, use_split(total_q, max_seq)))
+        return topk_rows_workspace_bytes(total_q);
     if (!use_split(total_q, max_seq)) return 0;
     return ((size_t)total_q * kAccWords +
             (size_t)total_q * split_row_words(split_ctas(total_q, max_seq))) * sizeof(uint32_t);
 }
 
-int topk_launches(int total_q, int max_seq) { return use_split(total_q, max_seq) ? 4 : 1; }
+int topk_launches(int total_q, int max_seq) {
+    if (use_split(total_q, max_seq)) return 4;
+    return topk_rows_eligible(total_q, max_seq, false) ? 3 : 1;
+}
 
 cudaError_t launch_topk(const BatchArgs& bt, const float* scores, int64_t ld, int K,
                         int32_t* out, void* ws, bool pdl, cudaStream_t stream) {
     if (bt.total_q == 0) return cudaSuccess;
     if (use_split(bt.total_q, bt.max_seq)) return launch_split(bt, scores, ld, K, out, ws, pdl, stream);
+    if (topk_rows_eligible(bt.total_q, bt.max_seq, false))
+        return launch_topk_rows(bt, scores, ld, K, out, ws, pdl, stream);
     if (bt.max_seq <= kResidentMax) return launch_resident(bt, scores, ld, K, out, pdl, stream);
     return launch_streaming(bt, scores, ld, K, out, topk_cluster_size(bt.total_q, bt.max_seq), pdl,
                             stream);

@@ -2,8 +2,10 @@
 against the oracle's selection on the same fp32 scores: heavy ties, signed
 zeros, negative scores, rows of every length class, and batches that take
 each path: rows kept in shared memory (up to 32768 positions), rows split over
-the whole GPU (at most 8 query tokens), and one cluster per row (more tokens),
-including inputs that force the cluster path's exact fallback."""
+the whole GPU (at most 8 query tokens), many rows of up to 2^18 positions
+(sampled threshold, candidate pass, per-row select) and one cluster per row
+(more tokens over longer rows), including inputs that force the exact
+fallbacks."""
 import numpy as np
 import pytest
 import torch
@@ -66,7 +68,8 @@ def _scores(rng, T, ld, kind):
 @pytest.mark.parametrize("kind", ["normal", "few_levels", "signed_zero", "offset"])
 @pytest.mark.parametrize("shape", [([30000, 2049, 4096], [1, 1, 2]),     # resident rows
                                    ([131072], [1]),                      # one long row: split
-                                   ([40000] * 5, [2] * 5),               # 10 tokens: clusters
+                                   ([40000] * 5, [2] * 5),               # 10 tokens: many rows
+                                   ([300000, 40000], [6, 4]),            # 10 tokens: clusters
                                    ([9000] * 40, [2] * 40)])             # 80 tokens: one CTA each
 def test_topk_crafted(kind, shape):
     lens, counts = shape
@@ -76,25 +79,65 @@ def test_topk_crafted(kind, shape):
     _run(lens, counts, _scores(rng, T, ld, kind))
 
 
-@pytest.mark.parametrize("counts", [[1, 1], [5, 5]])
-def test_topk_all_equal_long_rows(counts):
-    # split rows (2 tokens): every key equals tau; cluster rows (10 tokens): the
-    # threshold bin holds far more keys than the candidate buffers
-    lens = [70000, 300000]
+@pytest.mark.parametrize("lens,counts", [([70000, 300000], [1, 1]),   # split rows
+                                         ([70000, 262144], [5, 5]),   # many rows
+                                         ([70000, 300000], [5, 5])])  # clusters
+def test_topk_all_equal_long_rows(lens, counts):
+    # every key equals tau: split rows take the lowest positions across their
+    # slices; on the other paths the threshold holds far more keys than the
+    # candidate buffers, and the exact fallback selects by position
     ld = ((max(lens) + 127) // 128) * 128
     _run(lens, counts, np.full((sum(counts), ld), 2.5))
 
 
-def test_topk_sample_misses_the_top():
+@pytest.mark.parametrize("lens", [[131072, 200000],    # 10 tokens: many rows
+                                  [131072, 300000]])   # 10 tokens: one cluster per row
+def test_topk_sample_misses_the_top(lens):
     """The large scores sit exactly in the sampled chunks (every 16th run of 32
     positions), so the sampled threshold is far too high: the candidate pass
     finds fewer than k keys and the exact fallback must take over."""
-    lens, counts = [131072, 200000], [5, 5]  # 10 tokens: one cluster per row
+    counts = [5, 5]
     ld = ((max(lens) + 127) // 128) * 128
     rng = np.random.default_rng(5)
     s = rng.standard_normal((10, ld))
     pos = np.arange(ld)
     s[:, (pos // 32) % 16 == 0] += 100.0
+    _run(lens, counts, s)
+
+
+@pytest.mark.parametrize("kind", ["normal", "few_levels", "signed_zero", "offset"])
+def test_topk_many_rows_ragged(kind):
+    """Many-rows path: rows at and below k (all visible positions, then -1),
+    a row of exactly 2^18 positions, ragged unit ends, causal multi-token
+    requests; the workspace starts filled with garbage."""
+    lens, counts = [40000, 1000, 2049, 262144, 33001], [3, 1, 1, 3, 2]
+    rng = np.random.default_rng(31)
+    ld = ((max(lens) + 127) // 128) * 128
+    _run(lens, counts, _scores(rng, sum(counts), ld, kind))
+
+
+def test_topk_many_rows_ties_within_the_candidates():
+    """3,000 copies of one value near the 2048th largest score of each row:
+    tau is that value, the candidates hold every copy, and the lowest
+    positions among them are found by the select over positions."""
+    lens, counts = [131072] * 4, [3] * 4
+    rng = np.random.default_rng(17)
+    T = sum(counts)
+    s = rng.standard_normal((T, lens[0]))
+    for r in range(T):
+        s[r, rng.choice(lens[0], 3000, replace=False)] = 2.3
+    _run(lens, counts, s)
+
+
+def test_topk_many_rows_overflow():
+    """A sample that draws low: the large scores sit outside the sampled
+    chunks, so every row holds more candidates than its list keeps and the
+    exact fallback over the row takes over."""
+    lens, counts = [100000] * 5, [2] * 5
+    rng = np.random.default_rng(19)
+    s = rng.standard_normal((10, lens[0]))
+    pos = np.arange(lens[0])
+    s[:, (pos // 32) % 16 != 0] += 100.0
     _run(lens, counts, s)
 
 
