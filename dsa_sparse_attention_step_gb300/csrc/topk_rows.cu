@@ -524,9 +524,15 @@ rows_candidates_kernel(RowsArgs a) {
 // the threads of a warp, reading word i of their runs, hit 32 different banks.
 constexpr int kSelWordsMax = (kRowsMaxSeq / 32 / kSelThreads) | 1;
 
+constexpr int kSmallBin = 128;  // a bin this small is finished by pairwise ranks
+
 struct SelSmem {
     union {
         uint32_t hist[kBins0];
+        struct {
+            uint32_t key[kSmallBin];
+            int32_t pos[kSmallBin];
+        } list;  // the items of the threshold bin
         struct {
             uint32_t bits[kSelWordsMax * kSelThreads];  // the selection
             uint32_t pre[kSelWordsMax * kSelThreads];   // selected positions before word w
@@ -534,6 +540,7 @@ struct SelSmem {
     } u;
     int wsum[kSelThreads / 32 + 1];
     uint32_t res[4];
+    uint32_t n_list;
 };
 
 // The candidates, held in registers: thread i has candidates i + 256 j.
@@ -598,19 +605,72 @@ struct EqPosSource {
 template <bool kMerge, typename Src>
 __device__ __forceinline__ void select_and_write(SelSmem& S, const Src& src, uint32_t base, int L,
                                                  int vis, int K, int32_t* o) {
-    const int tid = threadIdx.x;
-    // tau, the K-th largest key; rem = how many keys equal to tau the
-    // selection takes, eq = how many there are
-    const RadixResult r = radix_select_desc<kSelThreads, 8, kMerge>(S.u.hist, S.wsum, S.res, src,
-                                                                 base, L, (uint32_t)K, 4);
-    const uint32_t tau = base + r.value;
-    // of the keys equal to tau, positions <= pthr are taken: the rem-th
-    // smallest such position
+    const int tid = threadIdx.x, lane = tid & 31;
+    // The selection is every key above tau (the K-th largest key) and, of
+    // the keys equal to tau, those at positions <= pthr.  Radix digits narrow
+    // tau down to a bin [bin_lo, bin_lo + 2^low) holding eq items, of which
+    // the rem largest (by key, then lower position) are taken.
+    uint32_t bin_lo = base, rem = (uint32_t)K, eq = 0u;
+    int low = L;
+    do {
+        const RadixResult r = radix_select_desc<kSelThreads, 8, kMerge>(S.u.hist, S.wsum, S.res,
+                                                                        src, bin_lo, low, rem, 1);
+        bin_lo += r.value << r.low;
+        rem = r.rem;
+        eq = r.eq;
+        low = r.low;
+    } while (low > 0 && eq > (uint32_t)kSmallBin);
+    uint32_t tau;
     int pthr = INT_MAX;
-    if (r.rem < r.eq) {
+    if (eq <= (uint32_t)kSmallBin) {
+        // gather the bin's items; the one ranked rem-th (key descending, then
+        // position ascending) gives tau and pthr
+        if (tid == 0) S.n_list = 0u;
+        __syncthreads();
+        const uint32_t span = (low >= 32) ? 0xFFFFFFFFu : ((1u << low) - 1u);
+        src.each([&](uint32_t key, int p, bool valid) {
+            const bool in = valid && key - bin_lo <= span;
+            const unsigned m = __ballot_sync(0xffffffffu, in);
+            if (m == 0u) return;
+            uint32_t b0 = 0u;
+            if (lane == __ffs(m) - 1) b0 = atomicAdd(&S.n_list, (uint32_t)__popc(m));
+            b0 = __shfl_sync(0xffffffffu, b0, __ffs(m) - 1);
+            if (in) {
+                const uint32_t slot = b0 + (uint32_t)__popc(m & ((1u << lane) - 1u));
+                if (slot < (uint32_t)kSmallBin) {
+                    S.u.list.key[slot] = key;
+                    S.u.list.pos[slot] = p;
+                }
+            }
+        });
+        __syncthreads();
+        const int m = (int)min(S.n_list, (uint32_t)kSmallBin);
+        for (int i = tid; i < m; i += kSelThreads) {
+            const uint32_t ki = S.u.list.key[i];
+            const int pi = S.u.list.pos[i];
+            uint32_t before = 0u;
+#pragma unroll 8
+            for (int j = 0; j < m; ++j) {
+                const uint32_t kj = S.u.list.key[j];
+                const int pj = S.u.list.pos[j];
+                before += (kj > ki) | ((kj == ki) & (pj < pi));
+            }
+            if (before == rem - 1u) {
+                S.res[0] = ki;
+                S.res[1] = (uint32_t)pi;
+            }
+        }
+        __syncthreads();
+        tau = S.res[0];
+        pthr = (int)S.res[1];
+        __syncthreads();  // the list is overwritten by the bitmap below
+    } else {
+        // every item of the bin carries the key bin_lo: the rem lowest
+        // positions among them
+        tau = bin_lo;
         const EqPosSource<Src> eqs{src, tau};
         const RadixResult pr = radix_select_desc<kSelThreads, 8, kMerge>(
-            S.u.hist, S.wsum, S.res, eqs, 0u, 18, r.rem, 3);
+            S.u.hist, S.wsum, S.res, eqs, 0u, 18, rem, 3);
         pthr = kRowsMaxSeq - 1 - (int)pr.value;
     }
     // bitmap of the selection; thread i owns words [wpt i, wpt i + wpt)
