@@ -9,7 +9,10 @@
 // selected tokens only).
 //
 // One CTA = one query token x one contiguous split of its index slots, taken
-// in tiles of 64 selected tokens.
+// in tiles of 64 selected tokens.  The batch runs as whole waves of one CTA
+// per token, and the tokens left for a last, partial wave are split into as
+// many pieces as keep that wave full (powers of two, up to 16); the pieces'
+// partial results are merged by a second kernel.
 //   S   = Q . L^T    tcgen05 kind::f16, M = 128 (96 heads + 32 unused rows),
 //                    N = 64 selected tokens, K = 576; accumulator in TMEM
 //   O^T = V^T . P^T  M = 128 latent dims (4 tiles cover 512), N = 96 heads,
@@ -175,14 +178,14 @@ struct MlaParams {
     const uint8_t* latent_pages;
     const int32_t* indices;
     int K;                 // index slots per token
-    int splits;            // CTAs per token
-    int split_keys;        // index slots per CTA (multiple of 64)
+    int full_tokens;       // tokens [0, full_tokens) run as one CTA each
+    int tail_splits;       // the other tokens as tail_splits CTAs each
     float kv_scale;
     float sm_scale;
-    __nv_bfloat16* out;    // final output (splits == 1)
-    float* lse;            // final lse (splits == 1), nullable
-    __half* part_o;        // [T, splits, 512, 96] normalised partial outputs (splits > 1)
-    float* part_lse;       // [T, splits, 96] partial lse, log2 domain (splits > 1)
+    __nv_bfloat16* out;    // final outputs (tokens run whole)
+    float* lse;            // final lse, nullable
+    __half* part_o;        // [T - full_tokens, tail_splits, 512, 96] normalised partial outputs
+    float* part_lse;       // [T - full_tokens, tail_splits, 96] partial lse, log2 domain
     int32_t* status;
 };
 
@@ -208,13 +211,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     grid_dependents_launch();
-    const int t = blockIdx.x / p.splits;
-    const int split = blockIdx.x % p.splits;
+    const bool whole = (int)blockIdx.x < p.full_tokens;
+    const int tail_cta = (int)blockIdx.x - p.full_tokens;  // >= 0 for a split token
+    const int t = whole ? (int)blockIdx.x : p.full_tokens + tail_cta / p.tail_splits;
+    const int split = whole ? 0 : tail_cta % p.tail_splits;
+    const int split_keys = whole ? p.K : p.K / p.tail_splits;
+    const int64_t piece = whole ? -1 : (int64_t)tail_cta;  // partial slot of a split token
     const int b = request_of(p.bt, t);
     const bool ok_tok = token_ok(p.bt, b, t, split == 0 ? p.status : nullptr);
     const int seq = __ldg(p.bt.seq_lens + b);
-    const int n_tiles = p.split_keys / kTileKeys;
-    const int slot0 = split * p.split_keys;
+    const int n_tiles = split_keys / kTileKeys;
+    const int slot0 = split * split_keys;
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = tid + kThreads * u;
-            s[u] = (ok_tok && k < p.split_keys) ? __ldg(p.indices + (int64_t)t * p.K + slot0 + k) : -1;
+            s[u] = (ok_tok && k < split_keys) ? __ldg(p.indices + (int64_t)t * p.K + slot0 + k) : -1;
         }
         const int32_t* table = p.bt.block_table + (int64_t)b * p.bt.max_pages;
 #pragma unroll
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int k = tid + kThreads * u;
-            if (k < p.split_keys) {
+            if (k < split_keys) {
                 int row = -1;
                 if (s[u] >= seq) {
                     record_error(p.status, DSA_ERR_DEVICE_CHECK);
@@ -598,14 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         // ---------------- end of softmax: per-head normaliser ----------------
         const bool ok = mbar_wait<kBudget>(&bars->done, 0, abort_flag);
         tc_fence_after();
-        const float scale_out = (p.splits == 1) ? p.kv_scale : 1.f;
+        const float scale_out = whole ? p.kv_scale : 1.f;
         sF[256 + h] = (l > 0.f) ? scale_out / l : 0.f;
         if (ok && ok_tok && h < kQRows) {
             const float lse2 = (l > 0.f) ? m_ref + log2f(l) : -INFINITY;
-            if (p.splits == 1) {
+            if (whole) {
                 if (p.lse) p.lse[(int64_t)t * kMlaHeads + h] = lse2 * 0.6931471805599453f;
             } else {
-                p.part_lse[((int64_t)t * p.splits + split) * kMlaHeads + h] = lse2;
+                p.part_lse[piece * kMlaHeads + h] = lse2;
             }
         }
     }
@@ -636,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 tmem_wait_ld();
                 // the per-head scales go to registers first: a shared load
                 // between the (possibly aliasing) stores would serialise them
-                if (p.splits == 1) {
+                if (whole) {
                     __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(sQ) + d;
 #pragma unroll
                     for (int hg = 0; hg < 3; ++hg) {
@@ -676,11 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
         }
         __syncthreads();
         if (write && tid == 0) {
-            if (p.splits == 1)
+            if (whole)
                 bulk_store_s2g(p.out + (int64_t)t * kMlaHeads * kVDim, sQ, (uint32_t)kOutBytes);
             else
-                bulk_store_s2g(p.part_o + ((int64_t)t * p.splits + split) * kVDim * kMlaHeads, sQ,
-                               (uint32_t)kOutBytes);
+                bulk_store_s2g(p.part_o + piece * kVDim * kMlaHeads, sQ, (uint32_t)kOutBytes);
         }
     }
 
@@ -700,14 +706,15 @@ constexpr int kMaxSplits = 16;
 constexpr int kCombineThreads = kCombineDims * (kMlaHeads / 8);  // 384
 __global__ void __launch_bounds__(kCombineThreads)
 sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __restrict__ part_lse,
-                          int splits, float kv_scale, __nv_bfloat16* __restrict__ out,
-                          float* __restrict__ lse) {
+                          int first_token, int splits, float kv_scale,
+                          __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     constexpr int kBlocksPerToken = kVDim / kCombineDims;  // 16
     __shared__ float s_w[kMaxSplits][kMlaHeads];
     __shared__ float s_inv[kMlaHeads];
     grid_dependents_launch();  // the next step's first kernel may start its setup
     grid_dependency_wait();  // the partials come from the previous kernel
-    const int t = blockIdx.x / kBlocksPerToken;
+    const int u = blockIdx.x / kBlocksPerToken;  // the u-th split token
+    const int t = first_token + u;
     const int dblk = blockIdx.x % kBlocksPerToken;
     const int tid = threadIdx.x;
     const int d = dblk * kCombineDims + (tid & (kCombineDims - 1));
@@ -717,14 +724,14 @@ sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __rest
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s)
         v[s] = (s < splits) ? __ldg(reinterpret_cast<const uint4*>(
-                                  part_o + (((int64_t)t * splits + s) * kVDim + d) * kMlaHeads + 8 * chunk))
+                                  part_o + (((int64_t)u * splits + s) * kVDim + d) * kMlaHeads + 8 * chunk))
                             : make_uint4(0u, 0u, 0u, 0u);
     if (tid < kMlaHeads) {
         const int h = tid;
         float ls[kMaxSplits];
 #pragma unroll
         for (int s = 0; s < kMaxSplits; ++s)
-            ls[s] = (s < splits) ? part_lse[((int64_t)t * splits + s) * kMlaHeads + h] : -INFINITY;
+            ls[s] = (s < splits) ? part_lse[((int64_t)u * splits + s) * kMlaHeads + h] : -INFINITY;
         float M = -INFINITY;
 #pragma unroll
         for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ls[s]);
@@ -763,43 +770,55 @@ sparse_mla_combine_kernel(const __half* __restrict__ part_o, const float* __rest
 
 }  // namespace
 
-// Index-slot splits per token: more CTAs per token when there are few tokens.
-// The count depends only on the number of query tokens, in steps, so a
-// request's result is bit-identical across batches within one step.
-int sparse_mla_splits(int total_q, int K) {
-    int splits;
-    if (total_q <= 9) splits = kMaxSplits;
-    else if (total_q <= 19) splits = 8;
-    else if (total_q <= 38) splits = 4;
-    else if (total_q <= 76) splits = 2;
-    else splits = 1;
-    while (splits > 1 && (K % (splits * kTileKeys)) != 0) splits >>= 1;
-    return splits;
+// The wave of CTAs the plan fills: one CTA per SM (the kernel's shared memory
+// admits one).  A fixed count, not the device's, so that the plan -- and with
+// it every token's result -- depends on the batch alone.
+constexpr int kWaveCtas = 152;
+
+// How a batch of T tokens runs: whole waves of one CTA per token, then the
+// remaining r tokens split into P pieces each, P the largest power of two
+// with r P <= kWaveCtas (at most 16, and dividing the slots into whole tiles).
+// For T < kWaveCtas this gives 16 splits up to 9 tokens, then 8, 4, 2, 1.
+struct MlaPlan {
+    int full_tokens, tail_splits;
+};
+
+MlaPlan mla_plan(int total_q, int K) {
+    MlaPlan pl;
+    const int r = total_q % kWaveCtas;
+    int P = 1;
+    while (r > 0 && 2 * P <= kMaxSplits && r * 2 * P <= kWaveCtas && (K % (2 * P * kTileKeys)) == 0)
+        P *= 2;
+    pl.tail_splits = P;
+    pl.full_tokens = (P > 1) ? total_q - r : total_q;
+    return pl;
 }
 
-// Workspace (split batches only): the f16 partial outputs [T, splits, 512, 96]
-// and their lse [T, splits, 96].
+// Workspace: the f16 partial outputs [split tokens, P, 512, 96] and their lse
+// [split tokens, P, 96].
 struct MlaWs {
     size_t part_o, part_lse, total;
 };
 
 MlaWs mla_ws_layout(int total_q, int K) {
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    const int splits = sparse_mla_splits(total_q, K);
+    const MlaPlan pl = mla_plan(total_q, K);
+    const size_t pieces = (size_t)(total_q - pl.full_tokens) * pl.tail_splits;
     MlaWs w;
     w.part_o = 0;
-    const size_t po = splits > 1 ? (size_t)total_q * splits * kMlaHeads * kVDim * sizeof(__half) : 0;
-    w.part_lse = up(po);
-    const size_t pl = splits > 1 ? (size_t)total_q * splits * kMlaHeads * sizeof(float) : 0;
-    w.total = w.part_lse + up(pl);
+    w.part_lse = up(pieces * kMlaHeads * kVDim * sizeof(__half));
+    w.total = w.part_lse + up(pieces * kMlaHeads * sizeof(float));
     return w;
 }
 
 size_t sparse_mla_workspace_bytes(int total_q, int K) { return mla_ws_layout(total_q, K).total; }
 
-// Kernels one sparse-MLA call launches: the MMA kernel and, for split
-// batches, the combine.
-int sparse_mla_launches(int total_q, int K) { return sparse_mla_splits(total_q, K) > 1 ? 2 : 1; }
+// Kernels one sparse-MLA call launches: the MMA kernel and, when some tokens
+// are split, the combine.
+int sparse_mla_launches(int total_q, int K) {
+    const MlaPlan pl = mla_plan(total_q, K);
+    return pl.full_tokens < total_q ? 2 : 1;
+}
 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
@@ -814,15 +833,17 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.latent_pages = static_cast<const uint8_t*>(latent_pages);
     p.indices = indices;
     p.K = K;
-    p.splits = sparse_mla_splits(bt.total_q, K);
-    p.split_keys = K / p.splits;
+    const MlaPlan pl = mla_plan(bt.total_q, K);
+    p.full_tokens = pl.full_tokens;
+    p.tail_splits = pl.tail_splits;
+    const int split_tokens = bt.total_q - pl.full_tokens;
     p.kv_scale = kv_scale;
     p.sm_scale = sm_scale;
     p.out = reinterpret_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     p.status = status;
-    p.part_o = p.splits > 1 ? reinterpret_cast<__half*>(wsb + w.part_o) : nullptr;
-    p.part_lse = p.splits > 1 ? reinterpret_cast<float*>(wsb + w.part_lse) : nullptr;
+    p.part_o = split_tokens > 0 ? reinterpret_cast<__half*>(wsb + w.part_o) : nullptr;
+    p.part_lse = split_tokens > 0 ? reinterpret_cast<float*>(wsb + w.part_lse) : nullptr;
     auto kernel = latent_format == DSA_LATENT_NVFP4
                       ? sparse_mla_tc_kernel<false, DSA_LATENT_NVFP4>
                       : (wait_test ? sparse_mla_tc_kernel<true, DSA_LATENT_FP8_E4M3>
@@ -830,12 +851,13 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemAlloc);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(kernel, dim3(bt.total_q * p.splits), dim3(kThreads), (size_t)kSmemAlloc,
-                      stream, pdl, 1, p);
-    if (e != cudaSuccess || p.splits == 1) return e;
-    return launch_kernel(sparse_mla_combine_kernel, dim3(bt.total_q * (kVDim / kCombineDims)),
+    e = launch_kernel(kernel, dim3(pl.full_tokens + split_tokens * pl.tail_splits), dim3(kThreads),
+                      (size_t)kSmemAlloc, stream, pdl, 1, p);
+    if (e != cudaSuccess || split_tokens == 0) return e;
+    return launch_kernel(sparse_mla_combine_kernel, dim3(split_tokens * (kVDim / kCombineDims)),
                          dim3(kCombineThreads), 0, stream, true, 1, (const __half*)p.part_o,
-                         (const float*)p.part_lse, p.splits, kv_scale, p.out, lse);
+                         (const float*)p.part_lse, pl.full_tokens, pl.tail_splits, kv_scale, p.out,
+                         lse);
 }
 
 }  // namespace dsa

@@ -232,3 +232,25 @@ def test_query_exponent_paths(log2_scale):
     ref_out, ref_lse = oracle.sparse_mla(batch_of(layer), q_scaled, layer.latent_pages,
                                          layer.kv_scale, sm_scale, idx.cpu().numpy())
     check_out(out, lse, ref_out, ref_lse, list(range(layer.total_q)))
+
+
+def test_mla_whole_waves_and_split_tail():
+    """160 query tokens: one wave of 152 tokens runs one CTA each, and the 8
+    tokens left over are split into 16 pieces each (a full second wave) whose
+    partials are merged; rows of both kinds, short rows with empty slots
+    among them, against the oracle."""
+    lens = [2100 + 613 * i for i in range(39)] + [1500]
+    counts = [4] * 40
+    layer = di.make_layer(lens, counts, seed=160, extra_pages=2)
+    gl = GpuLayer(layer)
+    st = gl.status()
+    out, lse, idx = gl.decode(st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = [0, 77, 151, 152, 153, 157, 158, 159]
+    ref_out, ref_lse = oracle.sparse_mla(batch_of(layer), layer.q_lat, layer.latent_pages,
+                                         layer.kv_scale, layer.sm_scale,
+                                         idx[rows].cpu().numpy(), rows=rows)
+    check_out(out, lse, ref_out, ref_lse, rows)
+    # the last rows see fewer than 2048 positions: their trailing slots are empty
+    assert (idx[159] < 0).any()
