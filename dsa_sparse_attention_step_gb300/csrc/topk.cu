@@ -569,12 +569,15 @@ topk_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld, int K,
 // Rows of at most 32768 visible positions: one CTA per query token, the whole
 // row resident in shared memory.
 //   A. Load the row once (every load in flight at the same time), store its
-//      order keys and build the histogram of their top 12 bits.
+//      order keys, and build a 12-bit histogram over the row's key range
+//      [kmin, kmax] (digit (key - kmin) >> sh, sh = bit length of kmax - kmin
+//      minus 12): bins spread over the values actually present, so that few
+//      lanes of a warp add to the same bin.
 //   B. Bin b holding the k-th largest key, and rem = how many keys bin b must
 //      still give.
-//   C. Two radix levels (10 + 10 bits) over the resident keys of bin b give
-//      tau, the k-th largest key, and eq_take, how many keys equal to tau are
-//      selected.
+//   C. Radix levels of up to 10 bits over the resident keys of bin b (the sh
+//      bits below it) give tau, the k-th largest key, and eq_take, how many
+//      keys equal to tau are selected.
 //   D. Thread i owns positions [32i, 32i + 32): it selects the keys above tau
 //      and, among those equal to tau, the lowest positions still needed (one
 //      block-wide scan of packed counts), and writes them in order.
@@ -586,6 +589,7 @@ struct ResSmem {
     alignas(16) uint32_t keys[kResidentMax];
     uint32_t hist[kBins];
     uint32_t warp_tot[kWarps + 1];
+    uint32_t wmin[kWarps], wmax[kWarps];
     uint32_t s_digit, s_rem, pad0, pad1;
 };
 
@@ -665,42 +669,74 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
     const int nchunk = (vis + 3) / 4;
     auto warp_live = [&](int u) { return 32 * warp + kThreads * u < nchunk; };
 
-    // ---- A. load, order keys, top-12-bit histogram ------------------------
+    // ---- A. load, order keys, key range, 12-bit histogram over the range ----
     {
-        float4 x[kChunksPerThread];
+        uint32_t k[kChunksPerThread][4];
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
         for (int u = 0; u < kChunksPerThread; ++u) {
             const int c = tid + kThreads * u;
             // positions 4c..4c+3 lie below round_up(vis, 4) <= ld
-            x[u] = (c < nchunk) ? __ldg(reinterpret_cast<const float4*>(row) + c)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 x = (c < nchunk) ? __ldg(reinterpret_cast<const float4*>(row) + c)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) k[u][e] = order_key(xv[e]);
         }
+#pragma unroll
+        for (int u = 0; u < kChunksPerThread; ++u) {
+            const int c = tid + kThreads * u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (4 * c + e < vis) {
+                    kmin = min(kmin, k[u][e]);
+                    kmax = max(kmax, k[u][e]);
+                }
+            }
+            if (warp_live(u))
+                *reinterpret_cast<uint4*>(&S.keys[4 * swz_chunk(c)]) =
+                    make_uint4(k[u][0], k[u][1], k[u][2], k[u][3]);
+        }
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        if ((tid & 31) == 0) {
+            S.wmin[warp] = kmin;
+            S.wmax[warp] = kmax;
+        }
+        __syncthreads();
+        kmin = 0xFFFFFFFFu;
+        kmax = 0u;
+#pragma unroll 8
+        for (int w = 0; w < kWarps; ++w) {
+            kmin = min(kmin, S.wmin[w]);
+            kmax = max(kmax, S.wmax[w]);
+        }
+        S.pad0 = kmin;  // every thread writes the same value
+        const int bits = 32 - __clz((int)(kmax - kmin));
+        const int sh = bits > 12 ? bits - 12 : 0;
+        S.pad1 = (uint32_t)sh;
 #pragma unroll
         for (int u = 0; u < kChunksPerThread; ++u) {
             if (!warp_live(u)) break;
             const int c = tid + kThreads * u;
-            const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-            uint32_t k4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const bool valid = 4 * c + e < vis;
-                k4[e] = valid ? order_key(xv[e]) : 0u;
-                if (valid) atomicAdd(&S.hist[k4[e] >> 20], 1u);
-            }
-            *reinterpret_cast<uint4*>(&S.keys[4 * swz_chunk(c)]) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+            for (int e = 0; e < 4; ++e)
+                if (4 * c + e < vis) atomicAdd(&S.hist[(k[u][e] - kmin) >> sh], 1u);
         }
     }
     __syncthreads();
 
     // ---- B. the bin of the k-th largest key --------------------------------
+    const uint32_t kbase = S.pad0;
+    int low = (int)S.pad1;  // bits of the key range below the bin
     res_find_digit(S, S.hist, kBins, (uint32_t)K);
-    uint32_t prefix = S.s_digit << 20;
+    uint32_t vpre = S.s_digit << low;  // key - kbase of the bin's lower edge
     uint32_t rem = S.s_rem;
 
-    // ---- C. two radix levels below the bin, over the resident keys --------
-    for (int level = 1; level < 3; ++level) {
-        const int shift = (level == 1) ? 10 : 0;
-        const uint32_t pshift = (level == 1) ? 20 : 10;
+    // ---- C. radix levels of up to 10 bits below the bin --------------------
+    while (low > 0) {
+        const int shift = low > 10 ? low - 10 : 0;
+        const int w = low - shift;
         for (int i = tid; i < 1024; i += kThreads) S.hist[i] = 0;
         __syncthreads();
 #pragma unroll
@@ -710,16 +746,19 @@ topk_resident_kernel(BatchArgs bt, const float* __restrict__ scores, int64_t ld,
             const uint4 kv = *reinterpret_cast<const uint4*>(&S.keys[4 * swz_chunk(c)]);
             const uint32_t k4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if ((k4[e] >> pshift) == (prefix >> pshift) && 4 * c + e < vis)
-                    atomicAdd(&S.hist[(k4[e] >> shift) & 0x3FFu], 1u);
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t v = k4[e] - kbase;
+                if (4 * c + e < vis && k4[e] >= kbase && (v >> low) == (vpre >> low))
+                    atomicAdd(&S.hist[(v >> shift) & ((1u << w) - 1u)], 1u);
+            }
         }
         __syncthreads();
         res_find_digit(S, S.hist, 1024, rem);
-        prefix |= S.s_digit << shift;
+        vpre |= S.s_digit << shift;
         rem = S.s_rem;
+        low = shift;
     }
-    const uint32_t tau = prefix;
+    const uint32_t tau = kbase + vpre;
     const uint32_t eq_take = rem;  // keys equal to tau that are selected (lowest positions)
 
     // ---- D. ordered output --------------------------------------------------
