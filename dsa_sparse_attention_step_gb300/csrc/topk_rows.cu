@@ -23,12 +23,14 @@
 //      candidate list (one global atomic per warp and unit reserves slots).
 //   3. rows_select_kernel, one CTA per row: when the row holds n candidates
 //      with k <= n <= kRowsCandMax, every key >= tau (the k-th largest key of
-//      the row) is among them, and tau is found by a radix select (digits of
-//      12, 10 and 10 bits) over the candidates; otherwise the same select
-//      runs over the whole row (exact fallback).  Keys above tau are taken;
-//      of the keys equal to tau, the rem lowest positions, found by a radix
-//      select over those positions (two 9-bit digits).  The selection is
-//      marked in a bitmap and written out in ascending position order.
+//      the row) is among them, and the candidates (held in registers) are
+//      digited, 8 bits at a time over [key_lo, max key], until the bin of
+//      tau holds at most 128 of them; those are ranked pairwise (key, then
+//      position), which gives tau and, among keys equal to it, the last
+//      position taken.  Otherwise the same select runs over the whole row
+//      (exact fallback; a bin of many equal keys is settled by a radix
+//      select over positions).  The selection is marked in a bitmap and each
+//      selected position is written at its rank (per-word prefix counts).
 // The sample only steers how many candidates there are: the result is exact
 // whatever it draws.
 #include <climits>
