@@ -23,11 +23,14 @@
 //
 // Roles: producer warps (each looks up pages and one lane issues the copies),
 // then MMA warps (the first allocates TMEM; lane 0 issues MMAs), then for
-// MXFP4 keys four converter warps, then eight epilogue warps in two sets of
-// four (one warp per TMEM lane quarter): with FP8 keys a set takes every
-// second unit and all of its tokens (so a unit's bookkeeping runs on four
-// warps, and the two sets drain different accumulators at once); with MXFP4
-// keys a set takes every second token.  With FP8 keys and query groups of one
+// MXFP4 keys four converter warps, then epilogue warps in sets of four (one
+// warp per TMEM lane quarter): with FP8 keys a set takes whole units and all
+// of their tokens -- three sets, one per TMEM accumulator, with one MMA
+// thread; two sets taking alternate units with two -- so every accumulator
+// is drained while the MMA fills another; with MXFP4 keys two sets each take
+// every second token.  A key of an absent page carries all-ones scale bits
+// (copied in place of the page's scales), so the epilogue needs no
+// block-table read.  With FP8 keys and query groups of one
 // or two tokens there are two producer and two MMA warps, each pair taking
 // alternate units: one thread spends about a thousand cycles of instruction
 // latency on a unit's copies (or on its waits, MMAs and commits), more than

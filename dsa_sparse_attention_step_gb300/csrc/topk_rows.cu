@@ -16,7 +16,7 @@
 //      chunk of the row (S >= 16, at most 128 chunks) and finds the bin of
 //      the n_s-th largest sampled key, n_s = ceil(1.5 k sampled / vis) + 16,
 //      among 4096 bins over the sampled key range (a second digit of 12 bits
-//      splits that bin when it holds more than 32 samples); key_lo is the
+//      splits that bin when it holds more than 8 samples); key_lo is the
 //      bin's lower edge.  Rows with vis <= k are written out at once.
 //   2. rows_candidates_kernel, two persistent CTAs per SM over the units of
 //      all rows: appends each key >= key_lo and its position to the row's
@@ -60,6 +60,7 @@ constexpr int kStreamThreads = 32 * (kConsWarps + 1);  // + one producer warp
 constexpr uint32_t kCountPoison = 1u << 30;  // a count above any row's length
 constexpr int kSelThreads = 256;
 constexpr int kSelPer = kRowsCandMax / kSelThreads;   // candidates per select thread
+constexpr int kRowVec = 8;                // 16-byte loads in flight per thread, whole-row select
 
 static_assert(kRowsCandMax % kSelThreads == 0, "candidates split evenly over the select threads");
 static_assert(kUnit == 128 * kLaneVec * kConsWarps, "units split evenly over the consumer lanes");
@@ -179,7 +180,7 @@ struct RadixResult {
 };
 
 template <int NT, int kDigit, bool kMerge, typename Src>
-__device__ RadixResult radix_select_desc(uint32_t* hist, int* wsum, uint32_t* res, const Src& src,
+__device__ __forceinline__ RadixResult radix_select_desc(uint32_t* hist, int* wsum, uint32_t* res, const Src& src,
                                          uint32_t base, int L, uint32_t rem, int max_levels) {
     const int tid = threadIdx.x;
     uint32_t hi = 0u, eq = 0u;
@@ -312,7 +313,7 @@ rows_threshold_kernel(RowsArgs a) {
     const RadixResult r = radix_select_desc<kThrThreads, 12, false>(
         S.hist, S.wsum, S.res, src, kmin, bit_length(kmax - kmin), need, 1);
     uint32_t key_lo = kmin + (r.value << r.low);  // the lower edge of the chosen bin
-    if (r.low > 0 && r.eq > 32u) {
+    if (r.low > 0 && r.eq > 8u) {
         const RadixResult r2 = radix_select_desc<kThrThreads, 12, false>(S.hist, S.wsum, S.res, src,
                                                                      key_lo, r.low, r.rem, 1);
         key_lo += r2.value << r2.low;
@@ -568,16 +569,16 @@ struct RowSource {
     template <typename F>
     __device__ __forceinline__ void each(F&& f) const {
         const int nvec = (vis + 3) / 4;
-        for (int v0 = 0; v0 < nvec; v0 += 4 * kSelThreads) {
-            float4 x[4];
+        for (int v0 = 0; v0 < nvec; v0 += kRowVec * kSelThreads) {
+            float4 x[kRowVec];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kRowVec; ++u) {
                 const int v = v0 + u * kSelThreads + threadIdx.x;
                 x[u] = (v < nvec) ? __ldg(reinterpret_cast<const float4*>(row) + v)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kRowVec; ++u) {
                 const int p = 4 * (v0 + u * kSelThreads + threadIdx.x);
                 f(order_key(x[u].x), p + 0, p + 0 < vis);
                 f(order_key(x[u].y), p + 1, p + 1 < vis);
