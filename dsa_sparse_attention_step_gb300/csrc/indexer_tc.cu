@@ -277,8 +277,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     // the older, unfinished phase for the awaited one.
     const int acc_cols = kMx ? 4 * N : N;
     const int nacc = kDual ? 6 : ((3 * acc_cols <= 512) ? 3 : 2);
-    auto acc_of = [&](int i) { return kDual ? 3 * (i & 1) + (i >> 1) % 3 : i % nacc; };
-    auto use_of = [&](int i) { return kDual ? (i >> 1) / 3 : i / nacc; };
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
@@ -514,6 +512,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             const uint64_t a0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
             const uint64_t b0 = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
             int gcount = 0, pb = -1, pg = -1;
+            // accumulator and its use count of this thread's next unit, kept
+            // as counters (the unit index divided by a run-time count costs
+            // tens of instructions): one thread cycles through nacc
+            // accumulators; with two, thread mw through its own three
+            const int a_period = kDual ? 3 : nacc;
+            const int a_base = kDual ? 3 * mw : 0;
+            int a_next = 0, u_next = 0;
             bool ok = true;
             for (int i = 0; i < n_units && ok; ++i) {
                 if (c.b != pb || c.g != pg) {
@@ -525,7 +530,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 }
                 if (ok && (C::kMmaWarps == 1 || i % C::kMmaWarps == mw)) {
                     const int st = i % C::kStages;
-                    const int acc = acc_of(i), use = use_of(i);
+                    const int acc = a_base + a_next, use = u_next;
+                    if (++a_next == a_period) {
+                        a_next = 0;
+                        ++u_next;
+                    }
                     ok = mbar_wait(&bars->full[st], (i / C::kStages) & 1, abort_flag);
                     if (ok && use >= 1) ok = mbar_wait(&bars->tempty[acc], (use - 1) & 1, abort_flag);
                     if (!ok) break;
@@ -587,18 +596,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
             int gcount = 0, pb = -1, pg = -1;
-            for (int i = 0; i < n_units; ++i) {
+            // FP8: the warp sets take whole units round robin (the per-unit
+            // bookkeeping runs on four warps, and the sets drain different
+            // accumulators at once): with one MMA thread set `half` takes the
+            // units i = half (mod nacc), all on accumulator `half` (a third
+            // set idles when only two accumulators fit); with two, the units
+            // of parity `half`, on MMA thread half's accumulators in turn.
+            // MXFP4: every set takes every unit.
+            const int step = kMx ? 1 : (kDual ? 2 : nacc);
+            const int first = kMx ? 0 : ((kDual || half < nacc) ? half : n_units);
+            const int a_period = kMx ? nacc : (kDual ? 3 : 1);
+            const int a_base = kMx ? 0 : (kDual ? 3 * half : half);
+            int a_next = 0, u_next = 0;
+            for (int k = 0; k < first && k < n_units; ++k) cursor_next(c, bt, G);
+            for (int i = first; i < n_units; i += step) {
                 const int gtok0 = c.g * G;                    // first token of the group
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
-                // FP8: the warp sets take whole units round robin (the
-                // per-unit bookkeeping runs on four warps, and the sets drain
-                // different accumulators at once); with one MMA thread there
-                // is a set per accumulator (a third set idles when only two
-                // accumulators fit)
-                if (!kMx && (kDual ? (i & 1) : (i % nacc)) != half) {
-                    cursor_next(c, bt, G);
-                    continue;
-                }
                 if (c.b != pb || c.g != pg) {
                     if (kMx) {
                         float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
@@ -628,8 +641,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                       : sW + half * (8 * kIdxHeads);
                 const int s = c.tile * kTile + quarter * 32 + lane;
                 const bool in_seq = s < c.seq;
-                const int acc = acc_of(i);
-                if (!mbar_wait(&bars->tfull[acc], use_of(i) & 1, abort_flag)) break;
+                const int acc = a_base + a_next, use = u_next;
+                if (++a_next == a_period) {
+                    a_next = 0;
+                    ++u_next;
+                }
+                if (!mbar_wait(&bars->tfull[acc], use & 1, abort_flag)) break;
                 tc_fence_after();
                 // the unit's scale words arrived with its keys (before tfull)
                 const uint32_t sw = reinterpret_cast<const uint32_t*>(
@@ -719,7 +736,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 }
                 tc_fence_before();
                 mbar_arrive(&bars->tempty[acc]);
-                cursor_next(c, bt, G);
+                for (int k = 0; k < step; ++k) cursor_next(c, bt, G);
             }
         }
     }
