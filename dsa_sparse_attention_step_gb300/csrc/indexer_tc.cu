@@ -35,6 +35,7 @@
 // alternate units: one thread spends about a thousand cycles of instruction
 // latency on a unit's copies (or on its waits, MMAs and commits), more than
 // the unit's share of the memory bandwidth allows.  Every wait is bounded.
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -665,6 +666,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     }
                 }
                 if (!kMx) {
+                    // the key's score cell of the group's first token, and the
+                    // number of visible positions the key needs (one more per
+                    // later token): a page-absent or out-of-range key is masked
+                    // as if no token saw it
+                    float* cell = p.scores + (int64_t)(c.q0 + gtok0) * p.ld + s;
+                    const int need = (in_seq && page_ok) ? s - (c.seq - c.nb + gtok0) : INT_MAX;
                     // tokens two at a time: both TMEM loads, then one wait
                     for (int j = 0; j < gr; j += 2) {
                         uint32_t v[2][32];
@@ -696,11 +703,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                                (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
                                               ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
                                                (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
-                            if (in_seq) {
-                                const int vis = c.seq - c.nb + gtok0 + j + jj + 1;
-                                p.scores[(int64_t)(c.q0 + gtok0 + j + jj) * p.ld + s] =
-                                    (s < vis && page_ok) ? sc : -INFINITY;
-                            }
+                            // token j + jj sees s when s < seq - nb + gtok0 + j + jj + 1
+                            if (in_seq) *cell = (need <= j + jj) ? sc : -INFINITY;
+                            cell += p.ld;
                         }
                     }
                 } else {
