@@ -70,7 +70,8 @@ def _scores(rng, T, ld, kind):
                                    ([131072], [1]),                      # one long row: split
                                    ([40000] * 5, [2] * 5),               # 10 tokens: many rows
                                    ([300000, 40000], [6, 4]),            # 10 tokens: clusters
-                                   ([9000] * 40, [2] * 40)])             # 80 tokens: one CTA each
+                                   ([9000] * 40, [2] * 40),              # 80 short rows: one CTA each
+                                   ([32768, 17000] * 9, [1] * 18)])      # 18 short rows: one CTA each
 def test_topk_crafted(kind, shape):
     lens, counts = shape
     rng = np.random.default_rng(len(lens) * 7 + sum(counts))
