@@ -530,7 +530,10 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the public API with host buffers --------------
     # per step: one pinned-host -> device copy of the step's inputs (queries
     # and request metadata packed in one staging buffer), the step, and one
-    # device -> pinned-host copy of its outputs (attention output and indices)
+    # device -> pinned-host copy of its outputs (attention output and indices).
+    # The copies run on their own streams, double-buffered, so that step i's
+    # outputs go back and step i + 1's inputs come in while step i + 1 (resp.
+    # step i) computes, as an engine pipelines them.
     e2e = None
     if rank == 0:
         def pack(tensors):
@@ -572,44 +575,71 @@ def run_ours(args, rank, world, local):
         dviews = [views(b) for b in din]
         dbatch = [dsa.Batch(v[4], v[5], v[6], layers[0].num_pages, lens, q_counts)
                   for v in dviews]
-        hout = torch.empty(obuf.numel(), dtype=torch.uint8).pin_memory()
+        # two output slots (attention output and indices in one buffer each)
+        obufs = [obuf, torch.empty_like(obuf)]
+        oviews = [(ob[:out_bytes].view(torch.bfloat16).view(T, 96, 512),
+                   ob[out_bytes:].view(torch.int32).view(T, dsa.TOPK)) for ob in obufs]
+        houts = [torch.empty(obuf.numel(), dtype=torch.uint8).pin_memory() for _ in range(2)]
         h2d = nbytes_in
         d2h = obuf.numel()
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]     # slot's inputs on the device
+        ev_done = [torch.cuda.Event() for _ in range(2)]   # slot's step finished
+        ev_out = [torch.cuda.Event() for _ in range(2)]    # slot's outputs back on the host
+        for e in ev_done + ev_out:
+            e.record(stream)
 
         def e2e_step(i):
             j = i % L
             slot = i % 2
             lay = layers[j]
-            din[slot].copy_(hin[j][0], non_blocking=True)
+            # inputs: once the step that last used this slot has finished
+            s_in.wait_event(ev_done[slot])
+            with torch.cuda.stream(s_in):
+                din[slot].copy_(hin[j][0], non_blocking=True)
+            ev_in[slot].record(s_in)
+            stream.wait_event(ev_in[slot])
+            stream.wait_event(ev_out[slot])  # the slot's previous outputs have left
             v = dviews[slot]
+            o_att, o_idx = oviews[slot]
             if append:
                 dsa.dsa_append_cache(dbatch[slot], v[7], v[8], lay.kv_scale,
                                      lay.index_pages, lay.latent_pages, fmt, status, stream=stream)
             # the block table copied in belongs to layer j's pools
             dsa.dsa_decode(dbatch[slot], v[0], v[1], v[2], lay.index_pages, fmt, v[3],
-                           lay.latent_pages, lay.kv_scale, lay.sm_scale, dsa.TOPK, out, lse, idx,
-                           ws, status, stream=stream)
-            hout.copy_(obuf, non_blocking=True)
+                           lay.latent_pages, lay.kv_scale, lay.sm_scale, dsa.TOPK, o_att, lse,
+                           o_idx, ws, status, stream=stream)
+            ev_done[slot].record(stream)
+            s_out.wait_event(ev_done[slot])
+            with torch.cuda.stream(s_out):
+                houts[slot].copy_(obufs[slot], non_blocking=True)
+            ev_out[slot].record(s_out)
 
-        with torch.cuda.stream(stream):
-            for i in range(max(3, min(args.warmup, 2 * L))):
-                e2e_step(i)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            stream.synchronize()
-            a.record(stream)
-            n_e2e = max(1, min(args.steps, 480))
-            for i in range(n_e2e):
-                e2e_step(i)
-            b.record(stream)
-        stream.synchronize()
+        for i in range(max(3, min(args.warmup, 2 * L))):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for ev in ev_done + ev_out:  # the first steps may start at once
+            ev.record(stream)
+        n_e2e = max(1, min(args.steps, 480))
+        for i in range(n_e2e):
+            e2e_step(i)
+        for ev in ev_out:  # the last outputs are on the host
+            stream.wait_event(ev)
+        b.record(stream)
+        torch.cuda.synchronize()
         te = a.elapsed_time(b) / 1000.0
         e2e = {"value": T * n_e2e / te, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "note": "per step: one pinned H2D copy of the packed queries and metadata" +
                        (" and the new tokens' keys and latents, dsa_append_cache" if append else "") +
                        ", dsa_decode (eager launches through the C ABI), one D2H copy of "
-                       "output and indices; caches resident"}
+                       "output and indices; copies on their own streams, double-buffered "
+                       "(step i's results return and step i+1's inputs arrive while a step "
+                       "computes); caches resident"}
 
     if rank == 0:
         step_b = wl.step_bytes(lens, q_counts, fmt)
