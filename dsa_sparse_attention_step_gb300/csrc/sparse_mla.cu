@@ -108,6 +108,39 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Pairs of fp32 in one 64-bit register (low word = first element) and their
+// packed arithmetic; f16 pairs in one 32-bit register.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// (lo, hi) fp32 -> f16 pair, round to nearest even
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(uint64_t v) {
+    __half2 h = __floats2half2_rn(lo_f32(v), hi_f32(v));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t v) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+    return pack_f32x2(f.x, f.y);
+}
+// 2^x of an f16 pair by the special-function unit (2^-inf = +0)
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -557,23 +590,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 // m_ref is -inf every slot so far was empty.
                 const float nm = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 const bool none = (m_ref == -INFINITY);
-                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                // two scores at a time: the exponent z - m_ref in fp32, rounded
+                // to an f16 pair, raised by one f16x2 2^x (P is stored in f16
+                // either way); the row sum adds the same f16 values in fp32
+                const uint64_t zs2 = pack_f32x2(zscale, zscale), nm2 = pack_f32x2(nm, nm);
+                uint64_t ps2[2] = {0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t ph[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int j = 8 * c + 2 * k;
-                        float p0 = ex2_approx(fmaf(__uint_as_float(r[j]), zscale, nm));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(r[j + 1]), zscale, nm));
-                        if (none) p0 = p1 = 0.f;
-                        ps[k] += p0 + p1;
-                        ph[k] = pack_half2(p0, p1);
+                        const uint64_t a2 = fma_f32x2(pack_f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                                      zs2, nm2);
+                        uint32_t e2 = ex2_f16x2(f32x2_to_f16x2(a2));
+                        if (none) e2 = 0u;
+                        ph[k] = e2;
+                        ps2[k & 1] = add_f32x2(ps2[k & 1], f16x2_to_f32x2(e2));
                     }
                     *reinterpret_cast<uint4*>(sP + sw128(h, 16 * c)) =
                         make_uint4(ph[0], ph[1], ph[2], ph[3]);
                 }
-                l = l * factor + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+                const uint64_t pst = add_f32x2(ps2[0], ps2[1]);
+                l = l * factor + (lo_f32(pst) + hi_f32(pst));
             }
             sF[h] = resc ? factor : 1.f;
             if (softmax_any(resc)) {
