@@ -510,9 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
             const uint64_t pd = smem_desc(smem_u32(sP), 16, 1024, kSwizzle128B);
             bool ok = true;
             for (int i = 0; i < n_used && ok; ++i) {
-                // S = Q . L^T, slab group by slab group as the producers fill them
+                // S = Q . L^T, slab group by slab group in the order the
+                // producers refill them: group 4 (dims 512-575, free once the
+                // previous S completed) first, then groups 0-3 as the previous
+                // O^T update releases them
 #pragma unroll
-                for (int g = 0; g < kGroups; ++g) {
+                for (int gi = 0; gi < kGroups; ++gi) {
+                    const int g = (gi == 0) ? 4 : gi - 1;
                     if (!mbar_wait<kBudget>(&bars->lfull[g], i & 1, abort_flag)) {
                         ok = false;
                         break;
@@ -525,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                             mma_f16(tmem + kColS,
                                     qd + (uint64_t)((s * kQSlabBytes + kk * 32) >> 4),
                                     ld + (uint64_t)((s * kLSlabBytes + kk * 32) >> 4), kIdescQK,
-                                    (s | kk) ? 1u : 0u);
+                                    (gi > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
                 mma_commit(&bars->lempty[4]);
