@@ -38,6 +38,7 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -278,6 +279,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     // the older, unfinished phase for the awaited one.
     const int acc_cols = kMx ? 4 * N : N;
     const int nacc = kDual ? 6 : ((3 * acc_cols <= 512) ? 3 : 2);
+    // FP8 with one MMA thread and only two accumulators (groups of 6-8
+    // tokens): three epilogue sets share the units by token halves, so that
+    // none idles; both halves' sets then drain an accumulator
+    const bool tsplit = !kMx && !kDual && nacc == 2;
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
@@ -291,8 +296,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         }
         for (int i = 0; i < 6; ++i) {
             mbar_init(&bars->tfull[i], 1);
-            // FP8: the set of four warps that takes the unit arrives
-            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : 128);
+            // FP8: the set of four warps that takes the unit arrives (the two
+            // sets of its token halves when they are split)
+            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : (tsplit ? 256 : 128));
         }
         for (int i = 0; i < kStgSlots; ++i) {
             mbar_init(&bars->sfull[i], 1);
@@ -593,7 +599,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter..+31
         const int half = (warp - C::kEpiWarp0) >> 2;  // warp set (FP8: unit parity, MXFP4: token parity)
         constexpr int kTS = C::kTokSplit;
-        if (n_units > 0) {
+        // the unit loop, specialised on token halves (kSplit) at compile time
+        auto drain = [&](auto split_tag) {
+            constexpr bool kSplit = decltype(split_tag)::value;
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
             int gcount = 0, pb = -1, pg = -1;
@@ -603,16 +611,27 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             // units i = half (mod nacc), all on accumulator `half` (a third
             // set idles when only two accumulators fit); with two, the units
             // of parity `half`, on MMA thread half's accumulators in turn.
-            // MXFP4: every set takes every unit.
+            // MXFP4: every set takes every unit.  With token halves (kSplit)
+            // the work items are (unit, half), taken round robin by the three
+            // sets; unit i uses accumulator i % 2 for the (i / 2)-th time.
             const int step = kMx ? 1 : (kDual ? 2 : nacc);
             const int first = kMx ? 0 : ((kDual || half < nacc) ? half : n_units);
             const int a_period = kMx ? nacc : (kDual ? 3 : 1);
             const int a_base = kMx ? 0 : (kDual ? 3 * half : half);
             int a_next = 0, u_next = 0;
-            for (int k = 0; k < first && k < n_units; ++k) cursor_next(c, bt, G);
-            for (int i = first; i < n_units; i += step) {
+            const int n_items = kSplit ? 2 * n_units : n_units;
+            const int item0 = kSplit ? half : first;
+            const int istep = kSplit ? C::kEpiSets : step;
+            int cur = 0;  // the unit the cursor is on
+            for (int it = item0; it < n_items; it += istep) {
+                const int i = kSplit ? (it >> 1) : it;
+                for (; cur < i; ++cur) cursor_next(c, bt, G);
                 const int gtok0 = c.g * G;                    // first token of the group
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
+                // this item's tokens [jlo, jhi) of the group
+                const int hg = kSplit ? (gr + 1) >> 1 : gr;
+                const int jlo = kSplit ? (it & 1) * hg : 0;
+                const int jhi = min(gr, jlo + hg);
                 if (c.b != pb || c.g != pg) {
                     if (kMx) {
                         float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
@@ -642,10 +661,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                       : sW + half * (8 * kIdxHeads);
                 const int s = c.tile * kTile + quarter * 32 + lane;
                 const bool in_seq = s < c.seq;
-                const int acc = a_base + a_next, use = u_next;
-                if (++a_next == a_period) {
-                    a_next = 0;
-                    ++u_next;
+                int acc, use;
+                if (kSplit) {
+                    acc = i & 1;
+                    use = i >> 1;
+                } else {
+                    acc = a_base + a_next;
+                    use = u_next;
+                    if (++a_next == a_period) {
+                        a_next = 0;
+                        ++u_next;
+                    }
                 }
                 if (!mbar_wait(&bars->tfull[acc], use & 1, abort_flag)) break;
                 tc_fence_after();
@@ -670,18 +696,18 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     // number of visible positions the key needs (one more per
                     // later token): a page-absent or out-of-range key is masked
                     // as if no token saw it
-                    float* cell = p.scores + (int64_t)(c.q0 + gtok0) * p.ld + s;
+                    float* cell = p.scores + (int64_t)(c.q0 + gtok0 + jlo) * p.ld + s;
                     const int need = (in_seq && page_ok) ? s - (c.seq - c.nb + gtok0) : INT_MAX;
                     // tokens two at a time: both TMEM loads, then one wait
-                    for (int j = 0; j < gr; j += 2) {
+                    for (int j = jlo; j < jhi; j += 2) {
                         uint32_t v[2][32];
                         tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * j), v[0]);
-                        if (j + 1 < gr)
+                        if (j + 1 < jhi)
                             tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * (j + 1)), v[1]);
                         tmem_wait_ld();
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
-                            if (j + jj >= gr) break;
+                            if (j + jj >= jhi) break;
                             const float4* w4 = reinterpret_cast<const float4*>(wq + (j + jj) * kIdxHeads);
                             // four independent packed (f32x2) partial sums
                             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
@@ -741,8 +767,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 }
                 tc_fence_before();
                 mbar_arrive(&bars->tempty[acc]);
-                for (int k = 0; k < step; ++k) cursor_next(c, bt, G);
             }
+        };
+        if (n_units > 0) {
+            if (tsplit) drain(std::integral_constant<bool, true>{});
+            else drain(std::integral_constant<bool, false>{});
         }
     }
     tc_fence_before();
