@@ -83,7 +83,8 @@ struct IdxCfg {
     // epilogue warps in sets of four (one warp per TMEM lane quarter).  FP8:
     // a set takes whole units, round robin (two sets with two MMA threads,
     // else one set per TMEM accumulator, so every accumulator is drained while
-    // the MMA fills another); MXFP4: two sets, each every second token
+    // the MMA fills another), or token halves of units; MXFP4: two sets, each
+    // every second token
     static constexpr int kEpiSets = (kMx || kDual) ? 2 : 3;
     static constexpr int kEpiWarps = 4 * kEpiSets;
     static constexpr int kEpiThreads = kEpiWarps * 32;
@@ -210,6 +211,15 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const BatchArgs& bt, int 
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
 }
+// Four consecutive fp32 of shared memory in one 128-bit load (a plain float4
+// read was issued as two 64-bit loads here).
+__device__ __forceinline__ float4 lds_f32x4(const float* p) {
+    float4 r;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
 __device__ __forceinline__ float lo_f32x2(uint64_t v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float hi_f32x2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
@@ -280,9 +290,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     const int acc_cols = kMx ? 4 * N : N;
     const int nacc = kDual ? 6 : ((3 * acc_cols <= 512) ? 3 : 2);
     // FP8 with one MMA thread and only two accumulators (groups of 6-8
-    // tokens): three epilogue sets share the units by token halves, so that
-    // none idles; both halves' sets then drain an accumulator
+    // tokens): the three epilogue sets share the units by token halves, and
+    // each half is an MMA of its own on its own barriers, so that an
+    // accumulator half waits only for its own drain (with three accumulators
+    // the extra MMAs and waits cost the one MMA thread more than they save)
     const bool tsplit = !kMx && !kDual && nacc == 2;
+    // with token halves, tokens [0, H) and [H, G) of a group are two MMAs on
+    // their own column ranges of the accumulator, with their own barriers
+    const int H = (G + 1) >> 1;
     volatile int* abort_flag = &bars->abort_flag;
 
     if (tid == 0) {
@@ -298,7 +313,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             mbar_init(&bars->tfull[i], 1);
             // FP8: the set of four warps that takes the unit arrives (the two
             // sets of its token halves when they are split)
-            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : (tsplit ? 256 : 128));
+            mbar_init(&bars->tempty[i], kMx ? C::kEpiThreads : 128);
         }
         for (int i = 0; i < kStgSlots; ++i) {
             mbar_init(&bars->sfull[i], 1);
@@ -514,6 +529,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             Cursor c;
             cursor_seek(c, bt, sReq, G, u_begin);
             const uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, 128, N, false, false);
+            const uint32_t idesc_h0 = make_idesc(kFmtE4M3, kFmtE4M3, 128, kIdxHeads * H, false, false);
+            const uint32_t idesc_h1 = make_idesc(kFmtE4M3, kFmtE4M3, 128, kIdxHeads * (G - H), false, false);
             // descriptors of stage 0 and query buffer 0; a byte offset o moves
             // the start-address field (16-byte units, 14 bits) by o >> 4
             const uint64_t a0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
@@ -543,21 +560,42 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         ++u_next;
                     }
                     ok = mbar_wait(&bars->full[st], (i / C::kStages) & 1, abort_flag);
-                    if (ok && use >= 1) ok = mbar_wait(&bars->tempty[acc], (use - 1) & 1, abort_flag);
                     if (!ok) break;
-                    tc_fence_after();
                     const uint64_t ad = a0 + (uint64_t)((st * kStageBytes) >> 4);
                     const uint64_t bd = b0 + (uint64_t)((((gcount - 1) & 1) * kQBufBytes) >> 4);
+                    if (tsplit) {
+                        // each token half waits only for the set that drained
+                        // the same half of this accumulator one use earlier;
+                        // its query rows start 32 H rows (of 128 B) further on
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int bi = 2 * acc + hh;
+                            if (use >= 1 && !mbar_wait(&bars->tempty[bi], (use - 1) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint64_t bh = bd + (uint64_t)((hh * H * kIdxHeads * kIdxDim) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (kMx)  // one accumulator per 32-element block
-                            mma_f8f6f4(tmem + acc * acc_cols + kk * N, ad + 2 * kk, bd + 2 * kk, idesc, 0u);
-                        else
-                            mma_f8f6f4(tmem + acc * acc_cols, ad + 2 * kk, bd + 2 * kk, idesc,
-                                       kk > 0 ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_f8f6f4(tmem + acc * acc_cols + hh * kIdxHeads * H, ad + 2 * kk, bh + 2 * kk,
+                                           hh ? idesc_h1 : idesc_h0, kk > 0 ? 1u : 0u);
+                            mma_commit(&bars->tfull[bi]);
+                        }
+                        if (!ok) break;
+                    } else {
+                        if (use >= 1 && !mbar_wait(&bars->tempty[acc], (use - 1) & 1, abort_flag)) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (kMx)  // one accumulator per 32-element block
+                                mma_f8f6f4(tmem + acc * acc_cols + kk * N, ad + 2 * kk, bd + 2 * kk, idesc, 0u);
+                            else
+                                mma_f8f6f4(tmem + acc * acc_cols, ad + 2 * kk, bd + 2 * kk, idesc,
+                                           kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->tfull[acc]);
                     }
                     mma_commit(&bars->empty[st]);
-                    mma_commit(&bars->tfull[acc]);
                 }
                 cursor_next(c, bt, G);
             }
@@ -608,12 +646,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             // FP8: the warp sets take whole units round robin (the per-unit
             // bookkeeping runs on four warps, and the sets drain different
             // accumulators at once): with one MMA thread set `half` takes the
-            // units i = half (mod nacc), all on accumulator `half` (a third
-            // set idles when only two accumulators fit); with two, the units
-            // of parity `half`, on MMA thread half's accumulators in turn.
-            // MXFP4: every set takes every unit.  With token halves (kSplit)
-            // the work items are (unit, half), taken round robin by the three
-            // sets; unit i uses accumulator i % 2 for the (i / 2)-th time.
+            // units i = half (mod nacc), all on accumulator `half`; with two,
+            // the units of parity `half`, on MMA thread half's accumulators in
+            // turn.  MXFP4: every set takes every unit.  With token halves
+            // (kSplit) the work items are (unit, half), taken round robin by
+            // the three sets; unit i uses accumulator i % 2 for the (i / 2)-th
+            // time.  A set waits for the MMA of (i, h) only once the previous
+            // phase of that barrier, (i - 2, h), has completed (else the
+            // parity wait could pass early): the set's previous item,
+            // (i - 2, 1) or (i - 1, 0), was issued by the one MMA thread after
+            // (i - 2, h).
             const int step = kMx ? 1 : (kDual ? 2 : nacc);
             const int first = kMx ? 0 : ((kDual || half < nacc) ? half : n_units);
             const int a_period = kMx ? nacc : (kDual ? 3 : 1);
@@ -629,9 +671,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 const int gtok0 = c.g * G;                    // first token of the group
                 const int gr = min(G, c.nb - gtok0);          // real tokens in the group
                 // this item's tokens [jlo, jhi) of the group
-                const int hg = kSplit ? (gr + 1) >> 1 : gr;
-                const int jlo = kSplit ? (it & 1) * hg : 0;
-                const int jhi = min(gr, jlo + hg);
+                const int jlo = kSplit ? (it & 1) * H : 0;
+                const int jhi = kSplit ? min(gr, jlo + H) : gr;
                 if (c.b != pb || c.g != pg) {
                     if (kMx) {
                         float* wdst = sW + (gcount & 1) * (8 * kIdxHeads);
@@ -673,7 +714,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         ++u_next;
                     }
                 }
-                if (!mbar_wait(&bars->tfull[acc], use & 1, abort_flag)) break;
+                // the barrier pair of the accumulator (of its token half)
+                const int bi = kSplit ? 2 * acc + (it & 1) : acc;
+                if (!mbar_wait(&bars->tfull[bi], use & 1, abort_flag)) break;
                 tc_fence_after();
                 // the unit's scale words arrived with its keys (before tfull)
                 const uint32_t sw = reinterpret_cast<const uint32_t*>(
@@ -698,41 +741,42 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     // as if no token saw it
                     float* cell = p.scores + (int64_t)(c.q0 + gtok0 + jlo) * p.ld + s;
                     const int need = (in_seq && page_ok) ? s - (c.seq - c.nb + gtok0) : INT_MAX;
+                    // one token's 32 head logits -> its weighted ReLU sum, stored
+                    auto score = [&](const uint32_t(&v)[32], int jt) {
+                        const float* wt = wq + jt * kIdxHeads;
+                        // four independent packed (f32x2) partial sums
+                        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 ww = lds_f32x4(wt + 4 * h4);
+                            acc2[(2 * h4) & 3] = fma_f32x2(
+                                pack_f32x2(ww.x, ww.y),
+                                pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f),
+                                           fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f)),
+                                acc2[(2 * h4) & 3]);
+                            acc2[(2 * h4 + 1) & 3] = fma_f32x2(
+                                pack_f32x2(ww.z, ww.w),
+                                pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f),
+                                           fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f)),
+                                acc2[(2 * h4 + 1) & 3]);
+                        }
+                        const float sc = (((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
+                                           (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
+                                          ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
+                                           (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
+                        // token jt sees s when s < seq - nb + gtok0 + jt + 1
+                        if (in_seq) *cell = (need <= jt) ? sc : -INFINITY;
+                        cell += p.ld;
+                    };
+                    const uint32_t tcol = tmem_addr(tmem, 32 * quarter, acc * acc_cols);
                     // tokens two at a time: both TMEM loads, then one wait
                     for (int j = jlo; j < jhi; j += 2) {
                         uint32_t v[2][32];
-                        tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * j), v[0]);
-                        if (j + 1 < jhi)
-                            tmem_ld32(tmem_addr(tmem, 32 * quarter, acc * acc_cols + 32 * (j + 1)), v[1]);
+                        tmem_ld32(tcol + 32 * j, v[0]);
+                        if (j + 1 < jhi) tmem_ld32(tcol + 32 * (j + 1), v[1]);
                         tmem_wait_ld();
-#pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            if (j + jj >= jhi) break;
-                            const float4* w4 = reinterpret_cast<const float4*>(wq + (j + jj) * kIdxHeads);
-                            // four independent packed (f32x2) partial sums
-                            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-                            for (int h4 = 0; h4 < 8; ++h4) {
-                                const float4 ww = w4[h4];
-                                acc2[(2 * h4) & 3] = fma_f32x2(
-                                    pack_f32x2(ww.x, ww.y),
-                                    pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 0]), 0.f),
-                                               fmaxf(__uint_as_float(v[jj][4 * h4 + 1]), 0.f)),
-                                    acc2[(2 * h4) & 3]);
-                                acc2[(2 * h4 + 1) & 3] = fma_f32x2(
-                                    pack_f32x2(ww.z, ww.w),
-                                    pack_f32x2(fmaxf(__uint_as_float(v[jj][4 * h4 + 2]), 0.f),
-                                               fmaxf(__uint_as_float(v[jj][4 * h4 + 3]), 0.f)),
-                                    acc2[(2 * h4 + 1) & 3]);
-                            }
-                            const float sc = (((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
-                                               (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
-                                              ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
-                                               (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
-                            // token j + jj sees s when s < seq - nb + gtok0 + j + jj + 1
-                            if (in_seq) *cell = (need <= j + jj) ? sc : -INFINITY;
-                            cell += p.ld;
-                        }
+                        score(v[0], j);
+                        if (j + 1 < jhi) score(v[1], j + 1);
                     }
                 } else {
                     for (int j = half; j < gr; j += kTS) {
@@ -766,7 +810,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&bars->tempty[acc]);
+                mbar_arrive(&bars->tempty[bi]);
             }
         };
         if (n_units > 0) {

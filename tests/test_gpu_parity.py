@@ -28,6 +28,9 @@ CASES = {
     # query groups of 6, 7 and 8 tokens (two TMEM accumulators, N >= 192) and
     # a request split into a group of 8 and a group of 1
     "wide_groups": ([3000, 2600, 1200, 5000], [6, 7, 8, 9], di.KEYS_FP8),
+    # groups of 6 (token halves of 3 + 3) and of 7 (4 + 3), with short groups
+    "groups_of_6": ([2500, 1400], [6, 5], di.KEYS_FP8),
+    "groups_of_7": ([2200, 3100, 900], [7, 3, 1], di.KEYS_FP8),
     # groups of at most two tokens: two producer and two MMA threads taking
     # alternate units (odd unit counts per CTA, a request boundary mid-range)
     "two_token": ([5000, 2049, 700, 9001], [2, 1, 2, 2], di.KEYS_FP8),
