@@ -58,6 +58,10 @@ def parse():
     ap.add_argument("--requests", type=int, default=0,
                     help="keep only the first N requests of the workload (profiling at a "
                          "smaller scale with the same per-request shape); 0 = all")
+    ap.add_argument("--query-tokens", type=int, default=0,
+                    help="keep the first N query tokens of each request, its context ending "
+                         "at the last kept token (profiling at a smaller scale with the same "
+                         "causal rows); 0 = all")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="bounded CPU-oracle sample for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -337,6 +341,9 @@ def run_ours(args, rank, world, local):
     lens, q_counts, fmt, seed = config_shape(args.config)
     if args.requests > 0:
         lens, q_counts = lens[:args.requests], q_counts[:args.requests]
+    if args.query_tokens > 0:
+        lens = [n - max(0, q - args.query_tokens) for n, q in zip(lens, q_counts)]
+        q_counts = [min(q, args.query_tokens) for q in q_counts]
     T = sum(q_counts)
     L = args.layers if args.layers > 0 else auto_layers(lens, fmt)
     dev = torch.device("cuda", local)
