@@ -66,17 +66,21 @@ constexpr int kMetaBytes = 2 * kPage * 4;        // 512: the 64 scale words of t
 // and each 32-element block gets its own accumulator (its E8M0 scale is
 // applied in the epilogue), which limits a query group to 2 tokens.
 // kDual (FP8 keys, query groups of one or two tokens, where the epilogue
-// has time to spare): two MMA warps taking alternate units as well.
-template <int kFmt, bool kDual>
+// has time to spare): two MMA warps taking alternate units as well.  kWide
+// (FP8 keys, query groups of 6-8 tokens): two accumulators of two token halves
+// each, MMA warp m filling accumulator m (the units of parity m), and four
+// epilogue sets, set s draining half s % 2 of accumulator s / 2.
+template <int kFmt, bool kDual, bool kWide = false>
 struct IdxCfg {
     static constexpr bool kMx = (kFmt == DSA_KEYS_MXFP4);
     static_assert(!(kMx && kDual), "MXFP4 keys use one producer and one MMA warp");
+    static_assert(!(kWide && (kMx || kDual)), "four epilogue sets only for FP8 groups of 6-8 tokens");
     // FP8 keys: two producer warps taking alternate units (one thread's copy
     // issue for a unit takes longer than the unit's keys take to arrive);
     // MXFP4 keys: one (the converters pace the stream)
     static constexpr int kProdWarps = kMx ? 1 : 2;
     static constexpr int kMmaWarp = kProdWarps;    // allocates TMEM
-    static constexpr int kMmaWarps = kDual ? 2 : 1;  // MMA-issuing threads (alternate units)
+    static constexpr int kMmaWarps = (kDual || kWide) ? 2 : 1;  // MMA-issuing threads (alternate units)
     static constexpr int kConvWarp0 = kMmaWarp + kMmaWarps;
     static constexpr int kConvWarps = kMx ? 4 : 0;
     static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
@@ -85,21 +89,24 @@ struct IdxCfg {
     // else one set per TMEM accumulator, so every accumulator is drained while
     // the MMA fills another), or token halves of units; MXFP4: two sets, each
     // every second token
-    static constexpr int kEpiSets = (kMx || kDual) ? 2 : 3;
+    static constexpr int kEpiSets = (kMx || kDual) ? 2 : (kWide ? 4 : 3);
     static constexpr int kEpiWarps = 4 * kEpiSets;
     static constexpr int kEpiThreads = kEpiWarps * 32;
     static constexpr int kTokSplit = 2;                        // MXFP4 token stride
-    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 384 (kDual), 480 or 448
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 384 (kDual), 480, 640 (kWide) or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
     // enough key bytes in flight per SM to cover the memory latency at full load
     static constexpr int kStages = kMx ? 6 : 8;
     // scale words of a unit: a slot is free again S + 3 units later (S + 6 with
-    // two MMA threads, whose accumulators repeat every sixth unit)
-    static constexpr int kMetaSlots = kStages + (kDual ? 6 : 3);
+    // two MMA threads, whose accumulators repeat every sixth unit; S + 4 with
+    // kWide: the MMA of unit i - S waited for the epilogue of unit i - S - 2 of
+    // the same parity, and each set drains its half's units in order, so an
+    // even distance of at least S + 2 is needed)
+    static constexpr int kMetaSlots = kStages + (kDual ? 6 : (kWide ? 4 : 3));
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
     static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
-    static constexpr int kOffReq = kOffW + 3 * 8 * kIdxHeads * 4;   // w x q_scale: [3][8][32]
+    static constexpr int kOffReq = kOffW + kEpiSets * 8 * kIdxHeads * 4;  // w x q_scale: [sets][8][32]
     static constexpr int kOffStg = (kOffReq + (kMaxReq + 1) * 4 + 1023) / 1024 * 1024;
     static constexpr int kOffMeta = kOffStg + (kMx ? kStgSlots * kStgBytes : 0);
     static constexpr int kOffBar = kOffMeta + kMetaSlots * kMetaBytes;
@@ -255,11 +262,11 @@ __device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w) {
     return r;
 }
 
-template <int kFmt, bool kDual>
-__global__ void __launch_bounds__(IdxCfg<kFmt, kDual>::kThreads, 1)
+template <int kFmt, bool kDual, bool kWide>
+__global__ void __launch_bounds__(IdxCfg<kFmt, kDual, kWide>::kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                   const __grid_constant__ CUtensorMap tm_q, const IdxParams p) {
-    using C = IdxCfg<kFmt, kDual>;
+    using C = IdxCfg<kFmt, kDual, kWide>;
     constexpr bool kMx = C::kMx;
     constexpr int kThreads = C::kThreads;
     grid_dependents_launch();  // the top-k may start its preamble
@@ -268,7 +275,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                                              ~static_cast<uintptr_t>(1023));
     uint8_t* sStage = sm + C::kOffStage;
     uint8_t* sQ = sm + C::kOffQ;
-    float* sW = reinterpret_cast<float*>(sm + C::kOffW);     // [3][8][32]
+    float* sW = reinterpret_cast<float*>(sm + C::kOffW);     // [sets][8][32]
     int* sReq = reinterpret_cast<int*>(sm + C::kOffReq);      // [B+1]
     uint8_t* sStg = sm + C::kOffStg;                          // MXFP4 staging ring
     uint8_t* sMeta = sm + C::kOffMeta;                        // scale words per unit
@@ -539,9 +546,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             // accumulator and its use count of this thread's next unit, kept
             // as counters (the unit index divided by a run-time count costs
             // tens of instructions): one thread cycles through nacc
-            // accumulators; with two, thread mw through its own three
-            const int a_period = kDual ? 3 : nacc;
-            const int a_base = kDual ? 3 * mw : 0;
+            // accumulators; kDual: thread mw through its own three; kWide:
+            // thread mw always fills accumulator mw
+            const int a_period = kDual ? 3 : (kWide ? 1 : nacc);
+            const int a_base = kDual ? 3 * mw : (kWide ? mw : 0);
             int a_next = 0, u_next = 0;
             bool ok = true;
             for (int i = 0; i < n_units && ok; ++i) {
@@ -650,12 +658,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             // the units of parity `half`, on MMA thread half's accumulators in
             // turn.  MXFP4: every set takes every unit.  With token halves
             // (kSplit) the work items are (unit, half), taken round robin by
-            // the three sets; unit i uses accumulator i % 2 for the (i / 2)-th
-            // time.  A set waits for the MMA of (i, h) only once the previous
-            // phase of that barrier, (i - 2, h), has completed (else the
-            // parity wait could pass early): the set's previous item,
-            // (i - 2, 1) or (i - 1, 0), was issued by the one MMA thread after
-            // (i - 2, h).
+            // the three sets (four with kWide); unit i uses accumulator i % 2
+            // for the (i / 2)-th time.  A set waits for the MMA of (i, h) only
+            // once the previous phase of that barrier, (i - 2, h), has
+            // completed (else the parity wait could pass early): with three
+            // sets the set's previous item, (i - 2, 1) or (i - 1, 0), was
+            // issued by the one MMA thread after (i - 2, h); with four, set s
+            // takes every half s % 2 of the units of parity s / 2, so (i - 2, h)
+            // was its own previous item.
             const int step = kMx ? 1 : (kDual ? 2 : nacc);
             const int first = kMx ? 0 : ((kDual || half < nacc) ? half : n_units);
             const int a_period = kMx ? nacc : (kDual ? 3 : 1);
@@ -769,14 +779,25 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         cell += p.ld;
                     };
                     const uint32_t tcol = tmem_addr(tmem, 32 * quarter, acc * acc_cols);
-                    // tokens two at a time: both TMEM loads, then one wait
-                    for (int j = jlo; j < jhi; j += 2) {
-                        uint32_t v[2][32];
-                        tmem_ld32(tcol + 32 * j, v[0]);
-                        if (j + 1 < jhi) tmem_ld32(tcol + 32 * (j + 1), v[1]);
-                        tmem_wait_ld();
-                        score(v[0], j);
-                        if (j + 1 < jhi) score(v[1], j + 1);
+                    if (kWide) {
+                        // one token per TMEM load (the register budget of 19
+                        // warps; four sets hide the load latency)
+                        for (int j = jlo; j < jhi; ++j) {
+                            uint32_t v[32];
+                            tmem_ld32(tcol + 32 * j, v);
+                            tmem_wait_ld();
+                            score(v, j);
+                        }
+                    } else {
+                        // tokens two at a time: both TMEM loads, then one wait
+                        for (int j = jlo; j < jhi; j += 2) {
+                            uint32_t v[2][32];
+                            tmem_ld32(tcol + 32 * j, v[0]);
+                            if (j + 1 < jhi) tmem_ld32(tcol + 32 * (j + 1), v[1]);
+                            tmem_wait_ld();
+                            score(v[0], j);
+                            if (j + 1 < jhi) score(v[1], j + 1);
+                        }
                     }
                 } else {
                     for (int j = half; j < gr; j += kTS) {
@@ -860,11 +881,11 @@ bool encode_rows128(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t b
 }
 
 
-template <int kFmt, bool kDual>
+template <int kFmt, bool kDual, bool kWide = false>
 cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscale, const float* w,
                       const void* pages, float* scores, int64_t ld, int32_t* status,
                       cudaStream_t stream) {
-    using C = IdxCfg<kFmt, kDual>;
+    using C = IdxCfg<kFmt, kDual, kWide>;
     IdxParams p;
     p.bt = bt;
     p.qscale = qscale;
@@ -883,7 +904,7 @@ cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscal
         return cudaErrorInvalidValue;
     if (!encode_rows128(&tm_q, q8, (uint64_t)bt.total_q * kIdxHeads, (uint32_t)p.N))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<kFmt, kDual>,
+    cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel<kFmt, kDual, kWide>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -892,7 +913,7 @@ cudaError_t launch_tc(const BatchArgs& bt, const uint8_t* q8, const float* qscal
         return e;
     // programmatic dependent launch is safe after any predecessor: the kernel
     // reads no global memory before its grid-dependency wait
-    return launch_kernel(indexer_tc_kernel<kFmt, kDual>, dim3(sms), dim3(C::kThreads),
+    return launch_kernel(indexer_tc_kernel<kFmt, kDual, kWide>, dim3(sms), dim3(C::kThreads),
                          (size_t)C::kSmemAlloc, stream, true, 1, tm_keys, tm_q, p);
 }
 
@@ -910,6 +931,11 @@ cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const fl
     // epilogue, bound the rate, so two threads issue each
     if (bt.max_q <= 2)
         return launch_tc<DSA_KEYS_FP8_E4M3, true>(bt, q8, qscale, w, pages, scores, ld, status, stream);
+    // groups of 6-8 tokens (two accumulators): four epilogue sets, one per
+    // accumulator half, since the epilogue bounds the rate there
+    if (bt.max_q >= 6)
+        return launch_tc<DSA_KEYS_FP8_E4M3, false, true>(bt, q8, qscale, w, pages, scores, ld, status,
+                                                          stream);
     return launch_tc<DSA_KEYS_FP8_E4M3, false>(bt, q8, qscale, w, pages, scores, ld, status, stream);
 }
 
