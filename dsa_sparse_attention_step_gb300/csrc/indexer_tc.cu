@@ -65,8 +65,11 @@ constexpr int kMetaBytes = 2 * kPage * 4;        // 512: the 64 scale words of t
 // MXFP4 keys are staged packed and expanded to E4M3 by four converter warps,
 // and each 32-element block gets its own accumulator (its E8M0 scale is
 // applied in the epilogue), which limits a query group to 2 tokens.
-// kDual (FP8 keys, query groups of one or two tokens, where the epilogue
-// has time to spare): two MMA warps taking alternate units as well.  kWide
+// FP8 keys: two MMA warps take alternate units (one thread's waits, MMAs and
+// commits of a unit take longer than the tensor pipe needs for them).  kDual
+// (query groups of one or two tokens, where the epilogue has time to spare):
+// six accumulators, three per MMA warp, and two epilogue sets.  Groups of 3-5
+// tokens: a ring of three accumulators shared by the two MMA warps.  kWide
 // (FP8 keys, query groups of 6-8 tokens): two accumulators of two token halves
 // each, MMA warp m filling accumulator m (the units of parity m), and four
 // epilogue sets, set s draining half s % 2 of accumulator s / 2.
@@ -80,7 +83,7 @@ struct IdxCfg {
     // MXFP4 keys: one (the converters pace the stream)
     static constexpr int kProdWarps = kMx ? 1 : 2;
     static constexpr int kMmaWarp = kProdWarps;    // allocates TMEM
-    static constexpr int kMmaWarps = (kDual || kWide) ? 2 : 1;  // MMA-issuing threads (alternate units)
+    static constexpr int kMmaWarps = kMx ? 1 : 2;  // MMA-issuing threads (alternate units)
     static constexpr int kConvWarp0 = kMmaWarp + kMmaWarps;
     static constexpr int kConvWarps = kMx ? 4 : 0;
     static constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
@@ -93,16 +96,17 @@ struct IdxCfg {
     static constexpr int kEpiWarps = 4 * kEpiSets;
     static constexpr int kEpiThreads = kEpiWarps * 32;
     static constexpr int kTokSplit = 2;                        // MXFP4 token stride
-    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 384 (kDual), 480, 640 (kWide) or 448
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 384 (kDual), 512, 640 (kWide) or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
     // enough key bytes in flight per SM to cover the memory latency at full load
     static constexpr int kStages = kMx ? 6 : 8;
-    // scale words of a unit: a slot is free again S + 3 units later (S + 6 with
-    // two MMA threads, whose accumulators repeat every sixth unit; S + 4 with
-    // kWide: the MMA of unit i - S waited for the epilogue of unit i - S - 2 of
-    // the same parity, and each set drains its half's units in order, so an
-    // even distance of at least S + 2 is needed)
-    static constexpr int kMetaSlots = kStages + (kDual ? 6 : (kWide ? 4 : 3));
+    // scale words of a unit: a slot is free again S + 3 units later with one
+    // MMA thread (MXFP4); S + 6 with kDual, whose accumulators repeat every
+    // sixth unit; S + 4 with kWide (the MMA of unit i - S waited for the
+    // epilogue of unit i - S - 2 of the same parity, and each set drains its
+    // half's units in order, so an even distance of at least S + 2 is
+    // needed); S + 7 with the ring of three (the argument is at the MMA loop)
+    static constexpr int kMetaSlots = kStages + (kMx ? 3 : (kDual ? 6 : (kWide ? 4 : 7)));
     static constexpr int kOffStage = 0;
     static constexpr int kOffQ = kOffStage + kStages * kStageBytes;
     static constexpr int kOffW = kOffQ + 2 * kQBufBytes;
@@ -296,12 +300,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     // the older, unfinished phase for the awaited one.
     const int acc_cols = kMx ? 4 * N : N;
     const int nacc = kDual ? 6 : ((3 * acc_cols <= 512) ? 3 : 2);
-    // FP8 with one MMA thread and only two accumulators (groups of 6-8
-    // tokens): the three epilogue sets share the units by token halves, and
-    // each half is an MMA of its own on its own barriers, so that an
-    // accumulator half waits only for its own drain (with three accumulators
-    // the extra MMAs and waits cost the one MMA thread more than they save)
-    const bool tsplit = !kMx && !kDual && nacc == 2;
+    // FP8 groups of 6-8 tokens (kWide; the host routes them here, and only
+    // two accumulators fit): each token half is an MMA of its own on its own
+    // barrier pair, drained by its own epilogue set, so that an accumulator
+    // half waits only for its own drain (with three accumulators the extra
+    // MMAs and waits cost the MMA threads more than they save)
+    const bool tsplit = kWide;
+    // FP8 groups of 3-5 tokens (the host routes 6-8 to kWide): the two MMA
+    // threads share a ring of three accumulators, unit i on accumulator i % 3
+    const bool ring3 = !kMx && !kDual && !kWide && nacc == 3;
     // with token halves, tokens [0, H) and [H, G) of a group are two MMAs on
     // their own column ranges of the accumulator, with their own barriers
     const int H = (G + 1) >> 1;
@@ -547,10 +554,27 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             // as counters (the unit index divided by a run-time count costs
             // tens of instructions): one thread cycles through nacc
             // accumulators; kDual: thread mw through its own three; kWide:
-            // thread mw always fills accumulator mw
+            // thread mw always fills accumulator mw; ring of three: unit i
+            // uses accumulator i % 3, so a thread's accumulator steps by 2.
+            //
+            // Ring of three, barrier pairing: tfull[a] completes once per unit
+            // on a, in unit order (the MMA of unit i waits for the epilogue of
+            // unit i - 3, which waited for tfull of i - 3), and set a, the only
+            // one draining a, waits for its units in that order.  The epilogue
+            // of unit j arrives on tempty[2 (j % 3) + (j & 1)], whose phase n is
+            // the unit j = 6 n + const; the thread of parity p waits at unit i
+            // for unit j = i - 3 there, and that barrier's previous phase (unit
+            // i - 9) has completed, since the same thread's unit i - 6 waited
+            // for it: the parity wait cannot alias.  Meta slots: the producer
+            // of unit i reuses the slot of unit i - S - 7 once the MMA of unit
+            // i - S has completed; that thread's units i - S, i - S - 2 and
+            // i - S - 4 waited for the epilogues of units i - S - 3, - 5 and
+            // - 7, one per accumulator, and each set drains its accumulator's
+            // units in order.
             const int a_period = kDual ? 3 : (kWide ? 1 : nacc);
             const int a_base = kDual ? 3 * mw : (kWide ? mw : 0);
             int a_next = 0, u_next = 0;
+            int r3 = mw;  // ring of three: this thread's next accumulator
             bool ok = true;
             for (int i = 0; i < n_units && ok; ++i) {
                 if (c.b != pb || c.g != pg) {
@@ -562,8 +586,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                 }
                 if (ok && (C::kMmaWarps == 1 || i % C::kMmaWarps == mw)) {
                     const int st = i % C::kStages;
-                    const int acc = a_base + a_next, use = u_next;
-                    if (++a_next == a_period) {
+                    const int acc = ring3 ? r3 : a_base + a_next, use = u_next;
+                    if (ring3) {
+                        r3 = (r3 == 0) ? 2 : r3 - 1;
+                    } else if (++a_next == a_period) {
                         a_next = 0;
                         ++u_next;
                     }
@@ -591,7 +617,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         }
                         if (!ok) break;
                     } else {
-                        if (use >= 1 && !mbar_wait(&bars->tempty[acc], (use - 1) & 1, abort_flag)) break;
+                        if (ring3) {
+                            if (i >= 3 && !mbar_wait(&bars->tempty[2 * acc + ((i - 3) & 1)], ((i - 3) / 6) & 1,
+                                                     abort_flag))
+                                break;
+                        } else if (use >= 1 && !mbar_wait(&bars->tempty[acc], (use - 1) & 1, abort_flag)) {
+                            break;
+                        }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -653,19 +685,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
             int gcount = 0, pb = -1, pg = -1;
             // FP8: the warp sets take whole units round robin (the per-unit
             // bookkeeping runs on four warps, and the sets drain different
-            // accumulators at once): with one MMA thread set `half` takes the
-            // units i = half (mod nacc), all on accumulator `half`; with two,
-            // the units of parity `half`, on MMA thread half's accumulators in
+            // accumulators at once): with the ring of three, set `half` takes
+            // the units i = half (mod 3), all on accumulator `half`; kDual: the
+            // units of parity `half`, on MMA thread half's accumulators in
             // turn.  MXFP4: every set takes every unit.  With token halves
-            // (kSplit) the work items are (unit, half), taken round robin by
-            // the three sets (four with kWide); unit i uses accumulator i % 2
-            // for the (i / 2)-th time.  A set waits for the MMA of (i, h) only
-            // once the previous phase of that barrier, (i - 2, h), has
-            // completed (else the parity wait could pass early): with three
-            // sets the set's previous item, (i - 2, 1) or (i - 1, 0), was
-            // issued by the one MMA thread after (i - 2, h); with four, set s
-            // takes every half s % 2 of the units of parity s / 2, so (i - 2, h)
-            // was its own previous item.
+            // (kSplit, kWide) the work items are (unit, half) and set s takes
+            // every half s % 2 of the units of parity s / 2 (accumulator
+            // s / 2, filled by MMA thread s / 2 for the (i / 2)-th time at
+            // unit i), so each barrier pair has one producer thread and one
+            // consuming set, and a set's previous item was the previous phase
+            // of the barrier it waits on.
             const int step = kMx ? 1 : (kDual ? 2 : nacc);
             const int first = kMx ? 0 : ((kDual || half < nacc) ? half : n_units);
             const int a_period = kMx ? nacc : (kDual ? 3 : 1);
@@ -724,8 +753,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                         ++u_next;
                     }
                 }
-                // the barrier pair of the accumulator (of its token half)
+                // the barriers of the accumulator (of its token half); with the
+                // ring of three, the drain barrier also by the unit's parity
                 const int bi = kSplit ? 2 * acc + (it & 1) : acc;
+                const int be = (!kSplit && ring3) ? 2 * acc + (i & 1) : bi;
                 if (!mbar_wait(&bars->tfull[bi], use & 1, abort_flag)) break;
                 tc_fence_after();
                 // the unit's scale words arrived with its keys (before tfull)
@@ -831,7 +862,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&bars->tempty[bi]);
+                mbar_arrive(&bars->tempty[be]);
             }
         };
         if (n_units > 0) {
@@ -931,8 +962,9 @@ cudaError_t launch_index_scores(const BatchArgs& bt, const uint8_t* q8, const fl
     // epilogue, bound the rate, so two threads issue each
     if (bt.max_q <= 2)
         return launch_tc<DSA_KEYS_FP8_E4M3, true>(bt, q8, qscale, w, pages, scores, ld, status, stream);
-    // groups of 6-8 tokens (two accumulators): four epilogue sets, one per
-    // accumulator half, since the epilogue bounds the rate there
+    // groups of 6-8 tokens (two accumulators): one MMA thread per accumulator
+    // and four epilogue sets, one per accumulator half; groups of 3-5: three
+    // accumulators shared by two MMA threads, one epilogue set each
     if (bt.max_q >= 6)
         return launch_tc<DSA_KEYS_FP8_E4M3, false, true>(bt, q8, qscale, w, pages, scores, ld, status,
                                                           stream);

@@ -120,19 +120,24 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 // (lo, hi) fp32 -> f16 pair, round to nearest even
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(uint64_t v) {
     __half2 h = __floats2half2_rn(lo_f32(v), hi_f32(v));
     return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t v) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
-    return pack_f32x2(f.x, f.y);
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// s_lo += lo(e), s_hi += hi(e) for an f16 pair e, each f16 value converted
+// exactly and added in fp32 with one rounding
+__device__ __forceinline__ void add_f16x2_to_f32(uint32_t e, float& s_lo, float& s_hi) {
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+        : "+f"(s_lo), "+f"(s_hi)
+        : "r"(e));
 }
 // 2^x of an f16 pair by the special-function unit (2^-inf = +0)
 __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
@@ -581,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 // the maximum of the raw accumulators (zscale > 0 keeps the order)
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < 64; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(r[j]));
+                for (int j = 0; j < 64; j += 2)
+                    mx[(j >> 1) & 3] = max3f(mx[(j >> 1) & 3], __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
                 const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * zscale;
                 if (mt > -INFINITY && (m_ref == -INFINITY || mt > m_ref + kRescaleLog2)) {
                     factor = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - mt);
@@ -596,27 +602,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_tc_kernel(const MlaPar
                 const bool none = (m_ref == -INFINITY);
                 // two scores at a time: the exponent z - m_ref in fp32, rounded
                 // to an f16 pair, raised by one f16x2 2^x (P is stored in f16
-                // either way); the row sum adds the same f16 values in fp32
+                // either way); the row sum adds the same f16 values in fp32,
+                // in four chains
                 const uint64_t zs2 = pack_f32x2(zscale, zscale), nm2 = pack_f32x2(nm, nm);
-                uint64_t ps2[2] = {0ull, 0ull};
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                if (none) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t ph[4];
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(sP + sw128(h, 16 * c)) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int j = 8 * c + 2 * k;
-                        const uint64_t a2 = fma_f32x2(pack_f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                                      zs2, nm2);
-                        uint32_t e2 = ex2_f16x2(f32x2_to_f16x2(a2));
-                        if (none) e2 = 0u;
-                        ph[k] = e2;
-                        ps2[k & 1] = add_f32x2(ps2[k & 1], f16x2_to_f32x2(e2));
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t ph[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int j = 8 * c + 2 * k;
+                            const uint64_t a2 = fma_f32x2(
+                                pack_f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), zs2, nm2);
+                            const uint32_t e2 = ex2_f16x2(f32x2_to_f16x2(a2));
+                            ph[k] = e2;
+                            add_f16x2_to_f32(e2, ps[2 * (k & 1)], ps[2 * (k & 1) + 1]);
+                        }
+                        *reinterpret_cast<uint4*>(sP + sw128(h, 16 * c)) =
+                            make_uint4(ph[0], ph[1], ph[2], ph[3]);
                     }
-                    *reinterpret_cast<uint4*>(sP + sw128(h, 16 * c)) =
-                        make_uint4(ph[0], ph[1], ph[2], ph[3]);
                 }
-                const uint64_t pst = add_f32x2(ps2[0], ps2[1]);
-                l = l * factor + (lo_f32(pst) + hi_f32(pst));
+                l = l * factor + ((ps[0] + ps[2]) + (ps[1] + ps[3]));
             }
             sF[h] = resc ? factor : 1.f;
             if (softmax_any(resc)) {
