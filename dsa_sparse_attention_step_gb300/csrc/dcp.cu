@@ -20,8 +20,12 @@
 // ascending.
 //
 // Kernels (launched in this order, each one CTA per query row):
-//   dcp_candidates_kernel<false>  every rank's top `cand` (radix select on
-//                                 (k << 16) | (0xFFFF - i), four 8-bit levels)
+//   dcp_candidates_kernel<false>  every rank's top `cand`: a list of the
+//                                 rank's tokens at or above a sampled key
+//                                 threshold (or all of them), then a radix
+//                                 select on (k << 16) | (0xFFFF - i), four
+//                                 8-bit levels, over the list (over the whole
+//                                 row when the list missed)
 //   dcp_merge_kernel<false>       the top-k of the gathered candidates (radix
 //                                 select on 48-bit (k, ~s) keys in shared
 //                                 memory); a rank all of whose candidates are
@@ -44,6 +48,8 @@ namespace {
 constexpr int kDcpThreads = 1024;
 constexpr int kDcpMaxWorld = 8;
 constexpr int kDcpMaxCand = kDcpMaxWorld * kTopK;  // 16384 gathered words, at most
+constexpr int kDcpPool = 24576;   // first round: candidate words of all ranks of a row (96 KB)
+constexpr int kDcpSamples = 4;    // first round: sampled positions per thread, at most
 
 // Order-preserving 16-bit key of a score rounded to BF16 (round to nearest
 // even), -0 folded onto +0.
@@ -112,6 +118,39 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool acti
     }
 }
 
+// Append `val` to rank r's list (pool + r * cap, count in lcnt[r]); words
+// past the list's capacity are counted but not stored.  (Few lanes append
+// at a time, so plain shared atomics do.)
+__device__ __forceinline__ void list_append(uint32_t* pool, int cap, int* lcnt, int r, uint32_t val) {
+    const int slot = atomicAdd(lcnt + r, 1);
+    if (slot < cap) pool[r * cap + slot] = val;
+}
+
+// Radix select by one warp of the c largest (unique) words of list[0, n),
+// four 8-bit levels with a histogram of the warp's own (hist, 256 bins);
+// returns the c-th largest word, tau, to every lane.
+__device__ __forceinline__ uint32_t warp_list_select(const uint32_t* list, int n, uint32_t c,
+                                                     uint32_t* hist, int lane) {
+    uint32_t prefix = 0u, need = c;
+    for (int level = 0; level < 4; ++level) {
+        const int shift = 24 - 8 * level;
+        const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+        for (int i = lane; i < 256; i += 32) hist[i] = 0u;
+        __syncwarp();
+        for (int j = lane; j < n; j += 32) {
+            const uint32_t wv = list[j];
+            if ((wv & hi_mask) == (prefix & hi_mask)) atomicAdd(hist + ((wv >> shift) & 255u), 1u);
+        }
+        __syncwarp();
+        uint32_t d, above;
+        find_digit(hist, need, lane, d, above);
+        prefix |= d << shift;
+        need -= above;
+        __syncwarp();
+    }
+    return prefix;
+}
+
 // Rank and rank-local index of position s (shifts when W is a power of two).
 __device__ __forceinline__ void rank_of(int s, int W, int lw, int& r, uint32_t& i) {
     if (lw >= 0) {
@@ -124,13 +163,30 @@ __device__ __forceinline__ void rank_of(int s, int W, int lw, int& r, uint32_t& 
 }
 
 // Local top-C of every rank of row t (kResend: only flagged ranks, C = K).
+//
+// First round: a rank with at most `cap` tokens lists them all; for a larger
+// rank, a sample of the row (every stride-th 32-position chunk) gives a BF16
+// key threshold at about the 2 C-th largest of its tokens, and one pass over
+// the row lists the rank's tokens at or above it.  The C best of a list are
+// found by a radix select over the list in shared memory.  A list that holds
+// fewer than C tokens or overflows falls back to the radix select over the
+// whole row, which the resend round (flagged ranks, C = K) always uses.  The
+// threshold only decides which path a rank takes: the result is exact either
+// way.
 template <bool kResend>
 __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpArgs a) {
+    extern __shared__ uint32_t s_pool[];  // first round: the ranks' candidate lists
     __shared__ uint32_t s_hist[kDcpMaxWorld][256];
     __shared__ uint32_t s_prefix[kDcpMaxWorld];
     __shared__ uint32_t s_need[kDcpMaxWorld];
     __shared__ int s_cnt[kDcpMaxWorld];
-    __shared__ int s_mode[kDcpMaxWorld];  // 0: idle, 1: radix select, 2: take all
+    __shared__ int s_lcnt[kDcpMaxWorld];          // tokens listed
+    __shared__ uint32_t s_keylo[kDcpMaxWorld];    // list threshold (16-bit key)
+    __shared__ uint32_t s_d1[kDcpMaxWorld], s_need2[kDcpMaxWorld];
+    // 0: idle, 1: select (first round: over its list; resend: over the row),
+    // 2: take all, 3: first round, select over the row
+    __shared__ int s_mode[kDcpMaxWorld];
+    __shared__ int s_samp[kDcpMaxWorld];          // threshold from the sample
     const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int W = a.world;
     const int C = kResend ? a.K : a.cand;
@@ -139,50 +195,203 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
     const int vis = visible_of(a.bt, b, t);
     const float* row = a.scores + (int64_t)t * a.ld;
     const int lw = (W & (W - 1)) == 0 ? __ffs(W) - 1 : -1;
+    const int cap = min(8 * C, kDcpPool / W);  // first round: list capacity per rank
     if (tid < W) {
         const int r = tid;
         const int n_r = vis > r ? (vis - 1 - r) / W + 1 : 0;
         const int c = min(C, n_r);
         const bool on = !kResend || a.flags[(int64_t)t * W + r] != 0;
         s_mode[r] = !on ? 0 : (c == n_r ? 2 : 1);
+        s_samp[r] = (!kResend && s_mode[r] == 1 && n_r > cap) ? 1 : 0;
         s_prefix[r] = 0u;
         s_need[r] = (uint32_t)c;
         s_cnt[r] = 0;
+        s_lcnt[r] = 0;
+        s_keylo[r] = 0u;
         if (on) (kResend ? a.full_n : a.sent_n)[(int64_t)t * W + r] = c;
     }
     __syncthreads();
-    bool any = false, radix = false;
+    bool any = false, radix = false, samp = false;
     for (int r = 0; r < W; ++r) {
         any |= s_mode[r] != 0;
         radix |= s_mode[r] == 1;
+        samp |= s_samp[r] != 0;
     }
     if (!any) return;
-    // radix select on comp = (k << 16) | (0xFFFF - i): the C largest are the
-    // best C of the rank (larger score, then lower position); the composite
-    // is unique per token, so the C-th largest, tau, selects exactly C
+    uint32_t* out = kResend ? a.full : a.sent;
+    const int stride = kResend ? a.K : a.cand;
+    // One pass over the row's visible positions: every thread loads two
+    // 16-byte vectors per round (rows are 16-byte aligned and score_ld is a
+    // multiple of 4, so a vector starting below vis stays in the row; values
+    // at or past vis are never used), then every lane calls body(s, f, valid,
+    // e) for each of its eight positions (e = s % 4), in step with the warp.
+    auto row_pass = [&](auto&& body) {
+        for (int base = 0; base < vis; base += 8 * kDcpThreads) {  // warp-uniform trip count
+            float4 v[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int s0 = base + 4 * (tid + q * kDcpThreads);
+                v[q] = s0 < vis ? __ldcg(reinterpret_cast<const float4*>(row + s0))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int s0 = base + 4 * (tid + q * kDcpThreads);
+                body(s0 + 0, v[q].x, s0 + 0 < vis, 0);
+                body(s0 + 1, v[q].y, s0 + 1 < vis, 1);
+                body(s0 + 2, v[q].z, s0 + 2 < vis, 2);
+                body(s0 + 3, v[q].w, s0 + 3 < vis, 3);
+            }
+        }
+    };
+    if (!kResend) {
+        if (samp) {
+            // ---- thresholds: the n_s-th largest sampled key of each sampling
+            // rank, n_s = ceil(3 c samples / n_r), found in two 8-bit levels
+            const int nch = (vis + 31) / 32;
+            const int cstride = max(8, (nch + 32 * kDcpSamples - 1) / (32 * kDcpSamples));
+            uint32_t key[kDcpSamples];
+            int rk[kDcpSamples];
+#pragma unroll
+            for (int u = 0; u < kDcpSamples; ++u) {
+                const int ch = (warp + 32 * u) * cstride;
+                const int sp = 32 * ch + lane;
+                rk[u] = -1;
+                key[u] = 0u;
+                if (ch < nch && sp < vis) {
+                    int r;
+                    uint32_t i;
+                    rank_of(sp, W, lw, r, i);
+                    if (s_samp[r]) {
+                        rk[u] = r;
+                        key[u] = bf16_key(__ldcg(row + sp));
+                    }
+                }
+            }
+            for (int i = tid; i < W * 256; i += kDcpThreads) (&s_hist[0][0])[i] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < kDcpSamples; ++u)
+                hist_add(&s_hist[0][0], (uint32_t)max(rk[u], 0) * 256u + (key[u] >> 8), rk[u] >= 0, lane);
+            __syncthreads();
+            if (warp < W && s_samp[warp]) {
+                uint32_t tot = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tot += s_hist[warp][8 * lane + j];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+                const int n_r = (vis - 1 - warp) / W + 1;
+                const uint32_t c = s_need[warp];
+                uint32_t ns = (uint32_t)((3ull * c * tot + (uint64_t)n_r - 1) / (uint64_t)n_r);
+                ns = max(1u, min(ns, tot));
+                uint32_t d = 0, above = 0;
+                if (tot > 0) find_digit(s_hist[warp], ns, lane, d, above);
+                if (lane == 0) {
+                    s_d1[warp] = d;
+                    s_need2[warp] = ns - above;
+                    if (tot == 0) s_samp[warp] = 0;  // no sample: list from key 0 (may overflow)
+                }
+            }
+            __syncthreads();
+            for (int i = tid; i < W * 256; i += kDcpThreads) (&s_hist[0][0])[i] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < kDcpSamples; ++u) {
+                const bool in = rk[u] >= 0 && s_samp[max(rk[u], 0)] && (key[u] >> 8) == s_d1[max(rk[u], 0)];
+                hist_add(&s_hist[0][0], (uint32_t)max(rk[u], 0) * 256u + (key[u] & 255u), in, lane);
+            }
+            __syncthreads();
+            if (warp < W && s_samp[warp]) {
+                uint32_t d, above;
+                find_digit(s_hist[warp], s_need2[warp], lane, d, above);
+                if (lane == 0) s_keylo[warp] = (s_d1[warp] << 8) | d;
+            }
+            __syncthreads();
+        }
+        // ---- one pass over the row: the lists, and every token of the
+        // take-all ranks written out.  With W a power of two a thread's four
+        // consecutive positions always fall on the same four ranks (vectors
+        // start at multiples of 4, rounds at multiples of 8192), whose mode
+        // and threshold it keeps in registers (threshold 0x10000: no list).
+        uint32_t klo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int r = lw >= 0 ? ((4 * tid + e) & (W - 1)) : 0;
+            klo[e] = s_mode[r] == 1 ? s_keylo[r] : (s_mode[r] == 2 ? 0u : 0x10000u);
+        }
+        row_pass([&](int s, float f, bool valid, int e) {
+            if (!valid) return;
+            int r;
+            uint32_t i;
+            rank_of(s, W, lw, r, i);
+            const uint32_t k = bf16_key(f);
+            const uint32_t lo = lw >= 0 ? klo[e]
+                                        : (s_mode[r] == 1 ? s_keylo[r] : (s_mode[r] == 2 ? 0u : 0x10000u));
+            if (k < lo) return;
+            if (s_mode[r] == 2) {
+                const int slot = atomicAdd(&s_cnt[r], 1);
+                if (slot < stride) out[((int64_t)t * W + r) * stride + slot] = (k << 16) | i;
+            } else {
+                list_append(s_pool, cap, s_lcnt, r, (k << 16) | (0xFFFFu - i));
+            }
+        });
+        __syncthreads();
+        // a list that missed: the rank selects over the whole row instead
+        if (tid < W && s_mode[tid] == 1 && (s_lcnt[tid] < (int)s_need[tid] || s_lcnt[tid] > cap))
+            s_mode[tid] = 3;
+        __syncthreads();
+        // ---- the c largest words of each list: warp r selects on list r
+        // (histogram in its row of s_hist), then the CTA writes them out
+        if (warp < W && s_mode[warp] == 1) {
+            const uint32_t tau =
+                warp_list_select(s_pool + warp * cap, s_lcnt[warp], s_need[warp], s_hist[warp], lane);
+            if (lane == 0) s_prefix[warp] = tau;
+        }
+        __syncthreads();
+        for (int r = 0; r < W; ++r) {
+            if (s_mode[r] != 1) continue;
+            const int n = s_lcnt[r];
+            const uint32_t tau = s_prefix[r];
+            for (int j = tid; j < n; j += kDcpThreads) {
+                const uint32_t wv = s_pool[r * cap + j];
+                if (wv >= tau) {
+                    const int slot = atomicAdd(&s_cnt[r], 1);
+                    if (slot < stride)
+                        out[((int64_t)t * W + r) * stride + slot] = (wv & 0xFFFF0000u) | (0xFFFFu - (wv & 0xFFFFu));
+                }
+            }
+        }
+        radix = false;
+        for (int r = 0; r < W; ++r) radix |= s_mode[r] == 3;
+    }
+    // ---- radix select over the whole row (resend round; first-round ranks
+    // whose list missed), on comp = (k << 16) | (0xFFFF - i): the C largest
+    // are the best C of the rank (larger score, then lower position); the
+    // composite is unique per token, so the C-th largest, tau, selects
+    // exactly C
+    const int kRow = kResend ? 1 : 3;
     for (int level = 0; radix && level < 4; ++level) {
         const int shift = 24 - 8 * level;
         const uint32_t hi_mask = level == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
         for (int i = tid; i < W * 256; i += kDcpThreads) (&s_hist[0][0])[i] = 0u;
         __syncthreads();
-        for (int base = 0; base < vis; base += kDcpThreads) {  // warp-uniform trip count
-            const int s = base + tid;
+        row_pass([&](int s, float f, bool valid, int) {
             bool act = false;
             uint32_t bin = 0;
-            if (s < vis) {
+            if (valid) {
                 int r;
                 uint32_t i;
                 rank_of(s, W, lw, r, i);
-                if (s_mode[r] == 1) {
-                    const uint32_t comp = (bf16_key(__ldcg(row + s)) << 16) | (0xFFFFu - i);
+                if (s_mode[r] == kRow) {
+                    const uint32_t comp = (bf16_key(f) << 16) | (0xFFFFu - i);
                     act = (comp & hi_mask) == (s_prefix[r] & hi_mask);
                     bin = (uint32_t)r * 256u + ((comp >> shift) & 255u);
                 }
             }
             hist_add(&s_hist[0][0], bin, act, lane);
-        }
+        });
         __syncthreads();
-        if (warp < W && s_mode[warp] == 1) {
+        if (warp < W && s_mode[warp] == kRow) {
             uint32_t d, above;
             find_digit(s_hist[warp], s_need[warp], lane, d, above);
             if (lane == 0) {
@@ -192,22 +401,24 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
         }
         __syncthreads();
     }
-    // output: every token of an active rank with comp >= tau (tau = 0 takes all)
-    uint32_t* out = kResend ? a.full : a.sent;
-    const int stride = kResend ? a.K : a.cand;
-    for (int s = tid; s < vis; s += kDcpThreads) {
+    // output: every token of a row-select rank with comp >= tau, and (resend
+    // round) every token of a take-all rank
+    if (!radix && !kResend) return;
+    row_pass([&](int s, float f, bool valid, int) {
+        if (!valid) return;
         int r;
         uint32_t i;
         rank_of(s, W, lw, r, i);
-        if (s_mode[r] == 0) continue;
-        const uint32_t k = bf16_key(__ldcg(row + s));
+        const int mode = s_mode[r];
+        if (mode == 0 || (!kResend && mode != 3)) return;
+        const uint32_t k = bf16_key(f);
         const uint32_t comp = (k << 16) | (0xFFFFu - i);
-        const uint32_t tau = s_mode[r] == 2 ? 0u : s_prefix[r];
+        const uint32_t tau = mode == 2 ? 0u : s_prefix[r];
         if (comp >= tau) {
             const int slot = atomicAdd(&s_cnt[r], 1);
             if (slot < stride) out[((int64_t)t * W + r) * stride + slot] = (k << 16) | i;
         }
-    }
+    });
 }
 
 // Block-wide exclusive scan of one int per thread (1024 threads); returns the
@@ -500,7 +711,11 @@ cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
     const dim3 grid((unsigned)bt.total_q);
     if (e == cudaSuccess)
-        e = launch_kernel(dcp_candidates_kernel<false>, grid, dim3(kDcpThreads), 0, stream, false, 1, a);
+        e = cudaFuncSetAttribute(dcp_candidates_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kDcpPool * sizeof(uint32_t)));
+    if (e == cudaSuccess)
+        e = launch_kernel(dcp_candidates_kernel<false>, grid, dim3(kDcpThreads),
+                          (size_t)kDcpPool * sizeof(uint32_t), stream, false, 1, a);
     if (e == cudaSuccess)
         e = launch_kernel(dcp_merge_kernel<false>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
     if (e == cudaSuccess)
