@@ -222,8 +222,8 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const BatchArgs& bt, int 
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
     return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
 }
-// Four consecutive fp32 of shared memory in one 128-bit load (a plain float4
-// read was issued as two 64-bit loads here).
+// Four consecutive fp32 of shared memory in one 128-bit load (plain float4
+// reads here executed twice as many shared-load instructions).
 __device__ __forceinline__ float4 lds_f32x4(const float* p) {
     float4 r;
     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -291,13 +291,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
     const int G = p.G, N = p.N;
     // TMEM accumulators: columns per unit, and three buffers when they fit in
     // the 512 columns (the MMA then runs two units ahead of the epilogue).
-    // With two MMA threads (kDual, N <= 64) each thread owns three of six
-    // buffers and cycles through them in its own unit order: unit i uses
-    // buffer 3 (i % 2) + (i / 2) % 3 for the (i / 6)-th time.  Were the
-    // buffers shared, the thread at unit i could reach its wait for the
-    // epilogue of unit i - 3 while that of unit i - 6 (issued by the same
-    // thread, same buffer) is still running, and the parity wait would take
-    // the older, unfinished phase for the awaited one.
+    // kDual (N <= 64): each MMA thread owns three of six buffers and cycles
+    // through them in its own unit order: unit i uses buffer
+    // 3 (i % 2) + (i / 2) % 3 for the (i / 6)-th time.  Were a buffer shared
+    // by the two threads with one drain barrier, the thread at unit i could
+    // reach its wait for the epilogue of unit i - 3 while that of unit i - 6
+    // (issued by the same thread, same buffer) is still running, and the
+    // parity wait would take the older, unfinished phase for the awaited
+    // one; the ring of three below shares its buffers and therefore splits
+    // the drain barrier by unit parity.
     const int acc_cols = kMx ? 4 * N : N;
     const int nacc = kDual ? 6 : ((3 * acc_cols <= 512) ? 3 : 2);
     // FP8 groups of 6-8 tokens (kWide; the host routes them here, and only
@@ -393,10 +395,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         // the read's latency never stalls the copies; lane 0 issues the copies.
         // Stage and meta-slot reuse: unit i waits for the MMA of unit i - S
         // (S = key stages, a multiple of 2, so the same producer and MMA
-        // thread), which itself waited for unit i - S's keys and for the
-        // epilogue of the unit before it on its accumulator: i - S - 3 (or
-        // - 2) with one MMA thread, i - S - 6 with two; meta slot i % (S + 3)
-        // (S + 6) is therefore free.
+        // thread), which itself waited for unit i - S's keys and for earlier
+        // epilogues; the meta ring (kMetaSlots, set per variant with its
+        // argument) is long enough that the slot of unit i is then free.
         const int pw = warp;
         bool ok = true;
         int gcount = 0, pb = -1, pg = -1;
@@ -533,7 +534,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
         // ---------------- MMA issue ----------------
         // FP8 keys: two issuing threads (lane 0 of two warps) take alternate
         // units, since one thread's waits, MMAs and commits of a unit take
-        // longer than the unit's keys take to arrive.  Both follow every
+        // longer than the unit's keys take to arrive or the tensor pipe needs
+        // for the unit's MMAs.  Both follow every
         // query-group change: each releases the old query buffer with its own
         // commit (the buffer's barrier counts both) and waits for the new one.
         // Each unit's stage, accumulator and scale slot belong to that unit
