@@ -40,8 +40,11 @@
 #include <climits>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace dsa {
+
+using namespace sm100;
 
 namespace {
 
@@ -50,6 +53,16 @@ constexpr int kDcpMaxWorld = 8;
 constexpr int kDcpMaxCand = kDcpMaxWorld * kTopK;  // 16384 gathered words, at most
 constexpr int kDcpPool = 24576;   // first round: candidate words of all ranks of a row (96 KB)
 constexpr int kDcpSamples = 4;    // first round: sampled positions per thread, at most
+constexpr int kStageRounds = 3;   // row passes: rounds of vectors in flight per thread
+// dynamic shared memory of the candidate kernel: the first round's list pool,
+// then the row passes' staging ring (two 16-byte vectors per thread and round)
+constexpr size_t kCandSmem = (size_t)kDcpPool * 4 + (size_t)kStageRounds * 2 * 16 * kDcpThreads;
+
+// Wait until at most n of this thread's cp.async groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
 
 // Order-preserving 16-bit key of a score rounded to BF16 (round to nearest
 // even), -0 folded onto +0.
@@ -175,7 +188,8 @@ __device__ __forceinline__ void rank_of(int s, int W, int lw, int& r, uint32_t& 
 // way.
 template <bool kResend>
 __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpArgs a) {
-    extern __shared__ uint32_t s_pool[];  // first round: the ranks' candidate lists
+    extern __shared__ uint4 s_dyn[];      // kCandSmem bytes
+    uint32_t* s_pool = reinterpret_cast<uint32_t*>(s_dyn);  // first round: the ranks' candidate lists
     __shared__ uint32_t s_hist[kDcpMaxWorld][256];
     __shared__ uint32_t s_prefix[kDcpMaxWorld];
     __shared__ uint32_t s_need[kDcpMaxWorld];
@@ -225,15 +239,30 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
     // multiple of 4, so a vector starting below vis stays in the row; values
     // at or past vis are never used), then every lane calls body(s, f, valid,
     // e) for each of its eight positions (e = s % 4), in step with the warp.
+    // The vectors go through a ring of kStageRounds rounds in shared memory
+    // (cp.async, each thread into slots of its own, so only its own waits
+    // order them): a round is consumed while the next two are in flight.
+    float4* stg = reinterpret_cast<float4*>(s_pool + kDcpPool);  // [round % 3][2][threads]
     auto row_pass = [&](auto&& body) {
-        for (int base = 0; base < vis; base += 8 * kDcpThreads) {  // warp-uniform trip count
-            float4 v[2];
+        constexpr int kRound = 8 * kDcpThreads;
+        const int nround = (vis + kRound - 1) / kRound;
+        auto issue = [&](int rd) {  // every thread commits one group per round, maybe empty
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const int s0 = base + 4 * (tid + q * kDcpThreads);
-                v[q] = s0 < vis ? __ldcg(reinterpret_cast<const float4*>(row + s0))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                const int s0 = rd * kRound + 4 * (tid + q * kDcpThreads);
+                if (rd < nround && s0 < vis)
+                    cp_async16(stg + ((rd % kStageRounds) * 2 + q) * kDcpThreads + tid, row + s0);
             }
+            cp_async_commit();
+        };
+        for (int rd = 0; rd < kStageRounds - 1; ++rd) issue(rd);
+        for (int rd = 0; rd < nround; ++rd) {  // warp-uniform trip count
+            cp_async_wait_group<kStageRounds - 2>();  // round rd has landed
+            float4 v[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) v[q] = stg[((rd % kStageRounds) * 2 + q) * kDcpThreads + tid];
+            issue(rd + kStageRounds - 1);  // into the slots of round rd - 1, already read
+            const int base = rd * kRound;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int s0 = base + 4 * (tid + q * kDcpThreads);
@@ -243,6 +272,7 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_candidates_kernel(const DcpAr
                 body(s0 + 3, v[q].w, s0 + 3 < vis, 3);
             }
         }
+        cp_async_wait_group<0>();  // no copy lands after the pass
     };
     if (!kResend) {
         if (samp) {
@@ -712,14 +742,18 @@ cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld
     const dim3 grid((unsigned)bt.total_q);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(dcp_candidates_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kDcpPool * sizeof(uint32_t)));
+                                 (int)kCandSmem);
     if (e == cudaSuccess)
-        e = launch_kernel(dcp_candidates_kernel<false>, grid, dim3(kDcpThreads),
-                          (size_t)kDcpPool * sizeof(uint32_t), stream, false, 1, a);
+        e = cudaFuncSetAttribute(dcp_candidates_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kCandSmem);
+    if (e == cudaSuccess)
+        e = launch_kernel(dcp_candidates_kernel<false>, grid, dim3(kDcpThreads), kCandSmem, stream, false,
+                          1, a);
     if (e == cudaSuccess)
         e = launch_kernel(dcp_merge_kernel<false>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
     if (e == cudaSuccess)
-        e = launch_kernel(dcp_candidates_kernel<true>, grid, dim3(kDcpThreads), 0, stream, false, 1, a);
+        e = launch_kernel(dcp_candidates_kernel<true>, grid, dim3(kDcpThreads), kCandSmem, stream, false, 1,
+                          a);
     if (e == cudaSuccess)
         e = launch_kernel(dcp_merge_kernel<true>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
     return e;
