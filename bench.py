@@ -69,6 +69,9 @@ def parse():
                     help="extra untimed replay while GPU clocks are sampled")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the NVFP4 / DCP / fused-front measurements")
+    ap.add_argument("--batch-invariant", action="store_true",
+                    help="run the sparse MLA under the batch-invariant plan (every token "
+                         "whole; dsa_set_batch_invariant)")
     return ap.parse_args()
 
 
@@ -337,6 +340,8 @@ def run_ours(args, rank, world, local):
     import dsa_sparse_attention_step_gb300 as dsa
     from dsa_sparse_attention_step_gb300 import workload as wl
     dsa.load()
+    if args.batch_invariant:
+        dsa.dsa_set_batch_invariant(True)
 
     lens, q_counts, fmt, seed = config_shape(args.config)
     if args.requests > 0:
@@ -664,7 +669,9 @@ def run_ours(args, rank, world, local):
                            "timing": "CUDA graphs of the timed steps, replayed back to back",
                            "step": "dsa_append_cache + dsa_decode" if args.config == "c4_prefill_append"
                                    else "dsa_decode",
-                           "parallelism": "replicas" if world > 1 else "single"},
+                           "parallelism": "replicas" if world > 1 else "single",
+                           "mla_plan": "batch-invariant (every token whole)"
+                                       if args.batch_invariant else "default (split last wave)"},
                 "step_hbm_gbs": step_b / (elapsed / args.steps) / 1e9,
                 "step_frac": step_b / (elapsed / args.steps) / 1e9 / hbm,
                 "step_bytes": step_b,

@@ -12,7 +12,8 @@ import os
 import torch
 
 __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path", "load",
-           "dsa_status_string", "dsa_launch_count", "dsa_index_scores", "dsa_topk",
+           "dsa_status_string", "dsa_launch_count", "dsa_set_batch_invariant",
+           "dsa_index_scores", "dsa_topk",
            "dsa_topk_workspace_size", "dsa_sparse_mla", "dsa_sparse_mla_workspace_size",
            "dsa_decode", "dsa_decode_workspace_size", "dsa_decode_noalloc",
            "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards",
@@ -72,6 +73,7 @@ _bp = ctypes.POINTER(_CBatch)
 _SIGS = {
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dsa_launch_count": (ctypes.c_uint64, []),
+    "dsa_set_batch_invariant": (ctypes.c_int32, [ctypes.c_int32]),
     "dsa_index_scores": (ctypes.c_int, [_bp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _i64, _vp, _vp]),
     "dsa_topk_workspace_size": (_sz, [_bp, _i32]),
     "dsa_topk": (ctypes.c_int, [_bp, _vp, _i64, _i32, _vp, _vp, _sz, _vp]),
@@ -132,6 +134,12 @@ def dsa_status_string(s):
 
 def dsa_launch_count():
     return int(load().dsa_launch_count())
+
+
+def dsa_set_batch_invariant(enabled):
+    """Process-wide batch-invariant attention plan on (True) or off; returns
+    the previous setting."""
+    return bool(load().dsa_set_batch_invariant(1 if enabled else 0))
 
 
 def _check(rc, what):

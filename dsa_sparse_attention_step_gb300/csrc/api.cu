@@ -19,9 +19,10 @@ bool topk_supported(int max_seq);
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
-                              cudaStream_t stream, bool wait_test = false, int latent_format = 0);
+                              cudaStream_t stream, bool wait_test, int latent_format,
+                              bool whole_only);
 size_t sparse_mla_workspace_bytes(int total_q, int K);
-int sparse_mla_launches(int total_q, int K);
+int sparse_mla_launches(int total_q, int K, bool whole_only);
 cudaError_t launch_append_cache(const BatchArgs& bt, const float* keys, const float* lat,
                                 float kv_scale, void* index_pages, void* latent_pages,
                                 int32_t* status, cudaStream_t stream);
@@ -44,6 +45,7 @@ cudaError_t launch_indexer_front(const BatchArgs& bt, const uint16_t* q_c, const
                                  float* q_f32, float* k_f32, int32_t* status, cudaStream_t stream);
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int32_t> g_batch_invariant{0};  // dsa_set_batch_invariant
 }  // namespace dsa
 
 using namespace dsa;
@@ -136,6 +138,10 @@ const char* dsa_status_string(dsa_status s) {
     return "unknown status";
 }
 
+int32_t dsa_set_batch_invariant(int32_t enabled) {
+    return g_batch_invariant.exchange(enabled != 0 ? 1 : 0);
+}
+
 uint64_t dsa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 dsa_status dsa_index_scores(const dsa_batch* batch, const uint8_t* q_fp8, const float* q_scale,
@@ -203,11 +209,13 @@ dsa_status dsa_sparse_mla_ex(const dsa_batch* batch, const uint16_t* q_lat,
     const size_t need = dsa_sparse_mla_workspace_size(batch, topk);
     if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return DSA_ERR_WORKSPACE;
     if (batch->total_q == 0) return DSA_OK;
-    g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk),
+    const bool whole_only = g_batch_invariant.load(std::memory_order_relaxed) != 0;
+    g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk, whole_only),
                          std::memory_order_relaxed);
     return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
                                          indices, topk, out, lse, ws, dev_status, false,
-                                         (cudaStream_t)stream, false, (int)latent_format));
+                                         (cudaStream_t)stream, false, (int)latent_format,
+                                         whole_only));
 }
 
 size_t dsa_decode_workspace_size(const dsa_batch* batch, int32_t topk) {
@@ -253,8 +261,9 @@ dsa_status dsa_decode_ex(const dsa_batch* batch, const uint8_t* q_fp8, const flo
     uint8_t* base = static_cast<uint8_t*>(ws);
     const size_t off_topk = align_up((size_t)batch->total_q * ld * sizeof(float), 256);
     const size_t off_mla = off_topk + align_up(dsa_topk_workspace_size(batch, topk), 256);
+    const bool whole_only = g_batch_invariant.load(std::memory_order_relaxed) != 0;
     g_launches.fetch_add(1 + (uint64_t)topk_launches(batch->total_q, batch->max_seq_len) +
-                             (uint64_t)sparse_mla_launches(batch->total_q, topk),
+                             (uint64_t)sparse_mla_launches(batch->total_q, topk, whole_only),
                          std::memory_order_relaxed);
     cudaError_t e = launch_index_scores(a, q_fp8, q_scale, w, index_pages, (int)key_format,
                                         scores, ld, dev_status, s);
@@ -263,7 +272,8 @@ dsa_status dsa_decode_ex(const dsa_batch* batch, const uint8_t* q_fp8, const flo
     if (e == cudaSuccess) e = launch_topk(a, scores, ld, topk, indices, base + off_topk, true, s);
     if (e == cudaSuccess)
         e = launch_sparse_mla(a, q_lat, latent_pages, kv_scale, sm_scale, indices, topk, out, lse,
-                              base + off_mla, dev_status, true, s, false, (int)latent_format);
+                              base + off_mla, dev_status, true, s, false, (int)latent_format,
+                              whole_only);
     return cuda_status(e);
 }
 
@@ -345,11 +355,11 @@ dsa_status dsa_test_sparse_mla_wait_timeout(const dsa_batch* batch, const uint16
     const size_t need = dsa_sparse_mla_workspace_size(batch, topk);
     if (ws_bytes < need || (need > 0 && (!ws || !aligned16(ws)))) return DSA_ERR_WORKSPACE;
     if (batch->total_q == 0) return DSA_OK;
-    g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk),
+    g_launches.fetch_add((uint64_t)sparse_mla_launches(batch->total_q, topk, false),
                          std::memory_order_relaxed);
     return cuda_status(launch_sparse_mla(to_args(batch), q_lat, latent_pages, kv_scale, sm_scale,
                                          indices, topk, out, lse, ws, dev_status, false,
-                                         (cudaStream_t)stream, true));
+                                         (cudaStream_t)stream, true, DSA_LATENT_FP8_E4M3, false));
 }
 
 dsa_status dsa_append_cache(const dsa_batch* batch, const float* new_keys,

@@ -833,15 +833,17 @@ constexpr int kWaveCtas = 152;
 // remaining r tokens split into P pieces each, P the largest power of two
 // with r P <= kWaveCtas (at most 16, and dividing the slots into whole tiles).
 // For T < kWaveCtas this gives 16 splits up to 9 tokens, then 8, 4, 2, 1.
+// The batch-invariant plan (whole_only) runs every token as one CTA.
 struct MlaPlan {
     int full_tokens, tail_splits;
 };
 
-MlaPlan mla_plan(int total_q, int K) {
+MlaPlan mla_plan(int total_q, int K, bool whole_only = false) {
     MlaPlan pl;
     const int r = total_q % kWaveCtas;
     int P = 1;
-    while (r > 0 && 2 * P <= kMaxSplits && r * 2 * P <= kWaveCtas && (K % (2 * P * kTileKeys)) == 0)
+    while (!whole_only && r > 0 && 2 * P <= kMaxSplits && r * 2 * P <= kWaveCtas &&
+           (K % (2 * P * kTileKeys)) == 0)
         P *= 2;
     pl.tail_splits = P;
     pl.full_tokens = (P > 1) ? total_q - r : total_q;
@@ -849,7 +851,8 @@ MlaPlan mla_plan(int total_q, int K) {
 }
 
 // Workspace: the f16 partial outputs [split tokens, P, 512, 96] and their lse
-// [split tokens, P, 96].
+// [split tokens, P, 96], sized for the default plan (the batch-invariant plan
+// needs none).
 struct MlaWs {
     size_t part_o, part_lse, total;
 };
@@ -869,15 +872,16 @@ size_t sparse_mla_workspace_bytes(int total_q, int K) { return mla_ws_layout(tot
 
 // Kernels one sparse-MLA call launches: the MMA kernel and, when some tokens
 // are split, the combine.
-int sparse_mla_launches(int total_q, int K) {
-    const MlaPlan pl = mla_plan(total_q, K);
+int sparse_mla_launches(int total_q, int K, bool whole_only) {
+    const MlaPlan pl = mla_plan(total_q, K, whole_only);
     return pl.full_tokens < total_q ? 2 : 1;
 }
 
 cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const void* latent_pages,
                               float kv_scale, float sm_scale, const int32_t* indices, int K,
                               uint16_t* out, float* lse, void* ws, int32_t* status, bool pdl,
-                              cudaStream_t stream, bool wait_test, int latent_format) {
+                              cudaStream_t stream, bool wait_test, int latent_format,
+                              bool whole_only) {
     if (bt.total_q == 0) return cudaSuccess;
     MlaParams p;
     p.bt = bt;
@@ -887,7 +891,7 @@ cudaError_t launch_sparse_mla(const BatchArgs& bt, const uint16_t* q_lat, const 
     p.latent_pages = static_cast<const uint8_t*>(latent_pages);
     p.indices = indices;
     p.K = K;
-    const MlaPlan pl = mla_plan(bt.total_q, K);
+    const MlaPlan pl = mla_plan(bt.total_q, K, whole_only);
     p.full_tokens = pl.full_tokens;
     p.tail_splits = pl.tail_splits;
     const int split_tokens = bt.total_q - pl.full_tokens;

@@ -120,6 +120,21 @@ const char* dsa_status_string(dsa_status s);
 /* Number of kernels this library has launched in this process (monotonic). */
 uint64_t dsa_launch_count(void);
 
+/* ---- batch-invariant plan ----------------------------------------------------
+ * Section "Zero-mismatch RL" (a switch under which a token's result does not
+ * depend on the batch it runs in; the page's top-k is batch-invariant by
+ * design).  The indexer and the exact top-k of this library always are.  The
+ * sparse MLA by default runs whole waves of one CTA per token and splits each
+ * token of a last, partial wave into pieces merged by log-sum-exp, the piece
+ * count set by the batch size, so a token's out and lse can differ in rounding
+ * between batches.  With enabled != 0 every token runs whole: out and lse of a
+ * token depend on its own inputs alone, and equal the default plan's wherever
+ * that plan runs the token whole.  Small batches then use fewer SMs.
+ * Process-wide; read once by each later call of dsa_sparse_mla(_ex),
+ * dsa_decode(_ex) and dsa_decode_noalloc.  Workspace sizes do not change.
+ * Returns the previous setting (0 or 1); the default is 0. */
+int32_t dsa_set_batch_invariant(int32_t enabled);
+
 /* ---- indexer -------------------------------------------------------------
  * Section "What changed" (32 heads x 128 dims, FP8 key with its scale, every
  * earlier token scored) and, for MXFP4 keys, section "Native MXFP4 indexer"

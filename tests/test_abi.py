@@ -38,6 +38,17 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_batch_invariant_switch_returns_the_previous_setting(lib):
+    import dsa_sparse_attention_step_gb300 as dsa
+    prev = dsa.dsa_set_batch_invariant(True)
+    try:
+        assert dsa.dsa_set_batch_invariant(True) is True
+        assert dsa.dsa_set_batch_invariant(False) is True
+        assert dsa.dsa_set_batch_invariant(False) is False
+    finally:
+        dsa.dsa_set_batch_invariant(prev)
+
+
 def test_status_strings(lib):
     import dsa_sparse_attention_step_gb300 as dsa
     assert dsa.dsa_status_string(0) == "ok"

@@ -152,6 +152,46 @@ def test_batch_invariance():
             assert torch.equal(x[b:b + 1], y)
 
 
+def test_batch_invariant_plan():
+    """Under the batch-invariant plan a token's attention is bit-identical in a
+    batch whose last, partial wave the default plan splits (200 tokens: the
+    last 48 in two pieces) and alone (where the default plan takes 16 pieces);
+    the tokens the default plan runs whole are unchanged by the switch, and the
+    result matches the oracle."""
+    n, nq = 40, 5
+    lens = [2600 + 37 * b for b in range(n)]
+    layer = di.make_layer(lens, nq, seed=21)
+    gl = GpuLayer(layer)
+    _, _, idx = gl.decode()
+    out_d, lse_d = gl.mla(idx)
+    b = n - 1
+    d = dict(layer.__dict__)
+    lo = nq * b
+    d.update(q_offsets=torch.tensor([0, nq], dtype=torch.int32),
+             seq_lens=layer.seq_lens[b:b + 1].clone(), block_table=layer.block_table[b:b + 1].clone(),
+             q8=layer.q8[lo:lo + nq], qscale=layer.qscale[lo:lo + nq], w=layer.w[lo:lo + nq],
+             q_lat=layer.q_lat[lo:lo + nq], seq_lens_host=[lens[b]], q_counts_host=[nq])
+    one = GpuLayer(di.Layer(**d))
+    prev = dsa.dsa_set_batch_invariant(True)
+    try:
+        out_i, lse_i = gl.mla(idx)
+        out_1, lse_1 = one.mla(idx[lo:lo + nq].contiguous())
+        dec_out, dec_lse, dec_idx = one.decode()
+        assert dsa.dsa_set_batch_invariant(True)
+    finally:
+        dsa.dsa_set_batch_invariant(prev)
+    torch.cuda.synchronize()
+    assert torch.equal(out_i[lo:lo + nq], out_1) and torch.equal(lse_i[lo:lo + nq], lse_1)
+    assert torch.equal(dec_idx, idx[lo:lo + nq])
+    assert torch.equal(dec_out, out_1) and torch.equal(dec_lse, lse_1)
+    assert torch.equal(out_i[:152], out_d[:152]) and torch.equal(lse_i[:152], lse_d[:152])
+    rows = [0, 151, 152, 170, lo, lo + nq - 1]
+    ref_out, ref_lse = oracle.sparse_mla(batch_of(layer), layer.q_lat, layer.latent_pages,
+                                         layer.kv_scale, layer.sm_scale,
+                                         idx[rows].cpu().numpy(), rows=rows)
+    check_out(out_i, lse_i, ref_out, ref_lse, rows)
+
+
 def test_bad_page_id_sets_device_status():
     layer = di.make_layer([3000], 1, seed=13)
     layer.block_table[0, 5] = layer.num_pages + 10
