@@ -50,7 +50,6 @@ namespace {
 
 constexpr int kDcpThreads = 1024;
 constexpr int kDcpMaxWorld = 8;
-constexpr int kDcpMaxCand = kDcpMaxWorld * kTopK;  // 16384 gathered words, at most
 constexpr int kDcpPool = 24576;   // first round: candidate words of all ranks of a row (96 KB)
 constexpr int kDcpSamples = 4;    // first round: sampled positions per thread, at most
 constexpr int kStageRounds = 3;   // row passes: rounds of vectors in flight per thread
@@ -481,8 +480,10 @@ __device__ __forceinline__ int block_scan(int v, int* s_warp, int* total) {
     return r;
 }
 
+// Shared memory of the merge: this struct, then the candidate area -- the
+// gathered keys (k << 32) | (0xFFFFFFFF - s), later the row's position bitmap
+// -- sized per round by merge_cand_bytes.
 struct MergeSmem {
-    unsigned long long cand[kDcpMaxCand];  // (k << 32) | (0xFFFFFFFF - s)
     int pos[kTopK];                        // selected positions, sorted
     uint32_t hist[256];
     int warp_tot[33];
@@ -494,6 +495,16 @@ struct MergeSmem {
     int count;
     int any_flag;
 };
+constexpr size_t kMergeFixed = (sizeof(MergeSmem) + 15) / 16 * 16;
+
+// Candidate-area bytes of a merge round: its gathered words (round 1: at most
+// `cand` per rank; round 2: a flagged rank's full top-K) or the bitmap of the
+// longest row, whichever is larger.
+size_t merge_cand_bytes(bool second, int world, int cand, int K, int max_seq) {
+    const size_t words = (size_t)world * (second ? K : cand) * sizeof(unsigned long long);
+    const size_t bitmap = (size_t)(max_seq + 31) / 32 * sizeof(uint32_t);
+    return ((words > bitmap ? words : bitmap) + 15) / 16 * 16;
+}
 
 // Top-K of the gathered candidates of row t.  Round 1 (kSecond = false): all
 // ranks' candidates; ranks whose candidates were all selected while they hold
@@ -503,6 +514,7 @@ template <bool kSecond>
 __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     MergeSmem& sm = *reinterpret_cast<MergeSmem*>(smem_raw);
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(smem_raw + kMergeFixed);
     const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int W = a.world;
     const int b = request_of(a.bt, t);
@@ -534,7 +546,7 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a)
         for (int j = tid; j < n; j += kDcpThreads) {
             const uint32_t w = __ldcg(src + j);
             const uint32_t s = (w & 0xFFFFu) * (uint32_t)W + (uint32_t)r;
-            sm.cand[sm.off[r] + j] = ((unsigned long long)(w >> 16) << 32) | (0xFFFFFFFFu - s);
+            cand[sm.off[r] + j] = ((unsigned long long)(w >> 16) << 32) | (0xFFFFFFFFu - s);
         }
     }
     const int K = min(a.K, N);
@@ -550,7 +562,7 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a)
             __syncthreads();
             for (int base = 0; base < N; base += kDcpThreads) {  // warp-uniform trip count
                 const int j = base + tid;
-                const unsigned long long c = j < N ? sm.cand[j] : 0ull;
+                const unsigned long long c = j < N ? cand[j] : 0ull;
                 const bool act = j < N && (c & hi_mask) == (sm.prefix & hi_mask);
                 hist_add(sm.hist, (uint32_t)((c >> shift) & 255u), act, lane);
             }
@@ -568,7 +580,7 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a)
     }
     const unsigned long long tau = K < N ? sm.prefix : 0ull;
     for (int j = tid; j < N; j += kDcpThreads) {
-        const unsigned long long c = sm.cand[j];
+        const unsigned long long c = cand[j];
         if (c >= tau) {
             const int s = (int)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFull));
             const int slot = atomicAdd(&sm.count, 1);
@@ -593,23 +605,28 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpArgs a)
         __syncthreads();
         if (sm.any_flag) return;  // round 2 finishes this row
     }
-    // the K positions in ascending order: bitonic sort of 2048 (padded)
-    for (int j = K + tid; j < kTopK; j += kDcpThreads) sm.pos[j] = INT_MAX;
-    __syncthreads();
-    for (int size = 2; size <= kTopK; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int j = tid; j < kTopK / 2; j += kDcpThreads) {
-                const int lo = 2 * j - (j & (stride - 1));
-                const int hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const int x = sm.pos[lo], y = sm.pos[hi];
-                if ((x > y) == up) {
-                    sm.pos[lo] = y;
-                    sm.pos[hi] = x;
-                }
-            }
-            __syncthreads();
+    // the K positions in ascending order: marked in a bitmap of the row's
+    // positions (in the candidate area, no longer read), then every thread
+    // ranks the set bits of its run of words by one block-wide scan
+    {
+        uint32_t* bm = reinterpret_cast<uint32_t*>(cand);
+        const int nwords = (vis + 31) >> 5;  // the area holds the longest row's bitmap
+        for (int j = tid; j < nwords; j += kDcpThreads) bm[j] = 0u;
+        __syncthreads();
+        for (int j = tid; j < K; j += kDcpThreads) {
+            const int s = sm.pos[j];
+            atomicOr(bm + (s >> 5), 1u << (s & 31));
         }
+        __syncthreads();
+        const int per = (nwords + kDcpThreads - 1) / kDcpThreads;
+        const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+        int mine = 0;
+        for (int j = w0; j < w1; ++j) mine += __popc(bm[j]);
+        int total;
+        int o = block_scan(mine, sm.warp_tot, &total);
+        for (int j = w0; j < w1; ++j)
+            for (uint32_t m = bm[j]; m != 0u; m &= m - 1u) sm.pos[o++] = 32 * j + __ffs(m) - 1;
+        __syncthreads();
     }
     for (int j = tid; j < a.K; j += kDcpThreads)
         a.indices[(int64_t)t * a.K + j] = j < K ? sm.pos[j] : -1;
@@ -733,12 +750,13 @@ cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld
     a.indices = indices;
     a.rank_indices = rank_indices;
     a.resent = resent;
-    const size_t msmem = sizeof(MergeSmem);
+    const size_t msmem1 = kMergeFixed + merge_cand_bytes(false, world, cand, K, bt.max_seq);
+    const size_t msmem2 = kMergeFixed + merge_cand_bytes(true, world, cand, K, bt.max_seq);
     cudaError_t e = cudaFuncSetAttribute(dcp_merge_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem1);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(dcp_merge_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem2);
     const dim3 grid((unsigned)bt.total_q);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(dcp_candidates_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -750,12 +768,12 @@ cudaError_t launch_dcp_topk(const BatchArgs& bt, const float* scores, int64_t ld
         e = launch_kernel(dcp_candidates_kernel<false>, grid, dim3(kDcpThreads), kCandSmem, stream, false,
                           1, a);
     if (e == cudaSuccess)
-        e = launch_kernel(dcp_merge_kernel<false>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
+        e = launch_kernel(dcp_merge_kernel<false>, grid, dim3(kDcpThreads), msmem1, stream, false, 1, a);
     if (e == cudaSuccess)
         e = launch_kernel(dcp_candidates_kernel<true>, grid, dim3(kDcpThreads), kCandSmem, stream, false, 1,
                           a);
     if (e == cudaSuccess)
-        e = launch_kernel(dcp_merge_kernel<true>, grid, dim3(kDcpThreads), msmem, stream, false, 1, a);
+        e = launch_kernel(dcp_merge_kernel<true>, grid, dim3(kDcpThreads), msmem2, stream, false, 1, a);
     return e;
 }
 
