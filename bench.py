@@ -27,6 +27,7 @@ same workload on its own GPU with no data-path collective (weak scaling); the
 timing takes the maximum over ranks.
 """
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -73,6 +74,21 @@ def parse():
                     help="run the sparse MLA under the batch-invariant plan (every token "
                          "whole; dsa_set_batch_invariant)")
     return ap.parse_args()
+
+
+def cuda_runtime():
+    """The CUDA runtime library through ctypes (for the end-to-end leg's
+    copies and event waits), or None when it cannot be loaded."""
+    for name in ("libcudart.so.13", "libcudart.so",
+                 os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcudart.so")):
+        try:
+            rt = ctypes.CDLL(name)
+        except OSError:
+            continue
+        for fn in ("cudaSetDevice", "cudaMemcpyAsync", "cudaEventRecord", "cudaStreamWaitEvent"):
+            getattr(rt, fn).restype = ctypes.c_int
+        return rt
+    return None
 
 
 def dist_env():
@@ -599,10 +615,57 @@ def run_ours(args, rank, world, local):
         ev_in = [torch.cuda.Event() for _ in range(2)]     # slot's inputs on the device
         ev_done = [torch.cuda.Event() for _ in range(2)]   # slot's step finished
         ev_out = [torch.cuda.Event() for _ in range(2)]    # slot's outputs back on the host
-        for e in ev_done + ev_out:
+        for e in ev_in + ev_done + ev_out:
             e.record(stream)
+        # the step as a user's serving loop issues it: the library's calls
+        # prepared once per (layer, slot), the copies and event waits as plain
+        # CUDA runtime calls on the same streams and events
+        calls = [[dsa.prepare_decode(dbatch[slot], dviews[slot][0], dviews[slot][1],
+                                     dviews[slot][2], layers[j].index_pages, fmt, dviews[slot][3],
+                                     layers[j].latent_pages, layers[j].kv_scale,
+                                     layers[j].sm_scale, dsa.TOPK, oviews[slot][0], lse,
+                                     oviews[slot][1], ws, status, stream=stream)
+                  for slot in range(2)] for j in range(L)]
+        acalls = [[dsa.prepare_append_cache(dbatch[slot], dviews[slot][7], dviews[slot][8],
+                                            layers[j].kv_scale, layers[j].index_pages,
+                                            layers[j].latent_pages, fmt, status, stream=stream)
+                   for slot in range(2)] for j in range(L)] if append else None
+        rt = cuda_runtime()
+        if rt is not None and rt.cudaSetDevice(ctypes.c_int(dev.index or 0)) != 0:
+            rt = None
 
-        def e2e_step(i):
+        def e2e_step_rt(i):
+            j = i % L
+            slot = i % 2
+            h_in, h_done, h_out = rt_ev_in[slot], rt_ev_done[slot], rt_ev_out[slot]
+            ok = (rt.cudaStreamWaitEvent(rt_s_in, h_done, 0) == 0 and
+                  rt.cudaMemcpyAsync(rt_din[slot], rt_hin[j], rt_nin, 1, rt_s_in) == 0 and
+                  rt.cudaEventRecord(h_in, rt_s_in) == 0 and
+                  rt.cudaStreamWaitEvent(rt_s, h_in, 0) == 0 and
+                  rt.cudaStreamWaitEvent(rt_s, h_out, 0) == 0)
+            if append:
+                acalls[j][slot]()
+            calls[j][slot]()
+            ok = ok and (rt.cudaEventRecord(h_done, rt_s) == 0 and
+                         rt.cudaStreamWaitEvent(rt_s_out, h_done, 0) == 0 and
+                         rt.cudaMemcpyAsync(rt_hout[slot], rt_obuf[slot], rt_nout, 2, rt_s_out) == 0 and
+                         rt.cudaEventRecord(h_out, rt_s_out) == 0)
+            if not ok:
+                raise RuntimeError("CUDA runtime call failed in the end-to-end step")
+
+        if rt is not None:
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            rt_s, rt_s_in, rt_s_out = (vp(x.cuda_stream) for x in (stream, s_in, s_out))
+            rt_ev_in = [vp(e.cuda_event) for e in ev_in]
+            rt_ev_done = [vp(e.cuda_event) for e in ev_done]
+            rt_ev_out = [vp(e.cuda_event) for e in ev_out]
+            rt_din = [vp(b.data_ptr()) for b in din]
+            rt_hin = [vp(h[0].data_ptr()) for h in hin]
+            rt_hout = [vp(b.data_ptr()) for b in houts]
+            rt_obuf = [vp(b.data_ptr()) for b in obufs]
+            rt_nin, rt_nout = sz(nbytes_in), sz(obuf.numel())
+
+        def e2e_step_torch(i):
             j = i % L
             slot = i % 2
             lay = layers[j]
@@ -628,6 +691,7 @@ def run_ours(args, rank, world, local):
                 houts[slot].copy_(obufs[slot], non_blocking=True)
             ev_out[slot].record(s_out)
 
+        e2e_step = e2e_step_rt if rt is not None else e2e_step_torch
         for i in range(max(3, min(args.warmup, 2 * L))):
             e2e_step(i)
         torch.cuda.synchronize()
@@ -648,10 +712,11 @@ def run_ours(args, rank, world, local):
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "note": "per step: one pinned H2D copy of the packed queries and metadata" +
                        (" and the new tokens' keys and latents, dsa_append_cache" if append else "") +
-                       ", dsa_decode (eager launches through the C ABI), one D2H copy of "
-                       "output and indices; copies on their own streams, double-buffered "
-                       "(step i's results return and step i+1's inputs arrive while a step "
-                       "computes); caches resident"}
+                       ", dsa_decode (eager launches through the C ABI, arguments prepared "
+                       "once per layer and slot), one D2H copy of output and indices; copies "
+                       "on their own streams, double-buffered (step i's results return and "
+                       "step i+1's inputs arrive while a step computes); caches resident" +
+                       ("" if rt is not None else "; copies and event waits through PyTorch")}
 
     if rank == 0:
         step_b = wl.step_bytes(lens, q_counts, fmt)

@@ -19,7 +19,8 @@ __all__ = ["DsaError", "Batch", "KEYS_FP8", "KEYS_MXFP4", "TOPK", "library_path"
            "NOALLOC_SCRATCH_BYTES", "dsa_append_cache", "ShardPart", "dsa_plan_token_shards",
            "dsa_dcp_topk_workspace_size", "dsa_dcp_topk", "dsa_lse_combine",
            "LATENT_FP8", "LATENT_NVFP4", "dsa_sparse_mla_ex", "dsa_decode_ex",
-           "dsa_indexer_front", "FRONT_QLAT_DIM", "FRONT_HIDDEN_DIM"]
+           "dsa_indexer_front", "FRONT_QLAT_DIM", "FRONT_HIDDEN_DIM", "PreparedCall",
+           "prepare_decode", "prepare_append_cache"]
 
 KEYS_FP8 = 0
 KEYS_MXFP4 = 1
@@ -303,6 +304,54 @@ def dsa_decode(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_
                            _ptr(ws), nbytes, _ptr(dev_status, torch.int32, "dev_status"),
                            _stream(stream))
     _check(rc, "dsa_decode")
+
+
+class PreparedCall:
+    """One entry point with its arguments checked and converted once, for a
+    step repeated on the same buffers (a serving loop): each call issues the
+    same C-ABI call as the function it was prepared from, without the
+    per-call argument handling in Python.  It keeps the tensors it was given
+    alive; their storage must not move."""
+
+    def __init__(self, name, fn, args, keep):
+        self._name, self._fn, self._args, self._keep = name, fn, args, keep
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != 0:
+            raise DsaError(rc, self._name)
+
+
+def prepare_decode(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages,
+                   kv_scale, sm_scale, topk, out, lse, indices, ws, dev_status=None, stream=None):
+    """dsa_decode as a PreparedCall (same arguments)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    args = (batch.ref(), _ptr(q_fp8, torch.uint8, "q_fp8"), _ptr(q_scale, torch.float32, "q_scale"),
+            _ptr(w, torch.float32, "w"), _ptr(index_pages, torch.uint8, "index_pages"),
+            int(key_format), _ptr(q_lat, (torch.bfloat16, torch.int16), "q_lat"),
+            _ptr(latent_pages, torch.uint8, "latent_pages"), float(kv_scale), float(sm_scale),
+            int(topk), _ptr(out, (torch.bfloat16, torch.int16), "out"),
+            _ptr(lse, torch.float32, "lse"), _ptr(indices, torch.int32, "indices"), _ptr(ws),
+            ws.numel() * ws.element_size(), _ptr(dev_status, torch.int32, "dev_status"),
+            _stream(stream))
+    keep = (batch, q_fp8, q_scale, w, index_pages, q_lat, latent_pages, out, lse, indices, ws,
+            dev_status, stream)
+    return PreparedCall("dsa_decode", load().dsa_decode, args, keep)
+
+
+def prepare_append_cache(batch, new_keys, new_latent, kv_scale, index_pages, latent_pages,
+                         key_format, dev_status=None, stream=None):
+    """dsa_append_cache as a PreparedCall (same arguments)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    args = (batch.ref(), _ptr(new_keys, torch.float32, "new_keys"),
+            _ptr(new_latent, torch.float32, "new_latent"), float(kv_scale),
+            _ptr(index_pages, torch.uint8, "index_pages"),
+            _ptr(latent_pages, torch.uint8, "latent_pages"), int(key_format),
+            _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    keep = (batch, new_keys, new_latent, index_pages, latent_pages, dev_status, stream)
+    return PreparedCall("dsa_append_cache", load().dsa_append_cache, args, keep)
 
 
 def dsa_decode_noalloc(batch, q_fp8, q_scale, w, index_pages, key_format, q_lat, latent_pages,

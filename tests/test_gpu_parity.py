@@ -192,6 +192,34 @@ def test_batch_invariant_plan():
     check_out(out_i, lse_i, ref_out, ref_lse, rows)
 
 
+def test_prepared_decode_matches_the_direct_call():
+    """A PreparedCall of dsa_decode issues the same call: identical results,
+    and an error status raised the same way."""
+    layer = di.make_layer([5000, 2600], [3, 2], seed=23)
+    gl = GpuLayer(layer)
+    out, lse, idx = gl.decode()
+    g = gl.g
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    idx2 = torch.empty_like(idx)
+    ws = torch.empty(dsa.dsa_decode_workspace_size(gl.batch), dtype=torch.uint8, device="cuda:0")
+    st = gl.status()
+    call = dsa.prepare_decode(gl.batch, g.q8, g.qscale, g.w, g.index_pages, layer.key_format,
+                              g.q_lat, g.latent_pages, layer.kv_scale, layer.sm_scale, dsa.TOPK,
+                              out2, lse2, idx2, ws, st)
+    call()
+    call()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2) and torch.equal(idx, idx2)
+    bad = dsa.prepare_decode(gl.batch, g.q8, g.qscale, g.w, g.index_pages, layer.key_format,
+                             g.q_lat, g.latent_pages, layer.kv_scale, layer.sm_scale, dsa.TOPK,
+                             out2, lse2, idx2, ws[:16], st)
+    with pytest.raises(dsa.DsaError) as e:
+        bad()
+    assert e.value.status == 3  # DSA_ERR_WORKSPACE
+
+
 def test_bad_page_id_sets_device_status():
     layer = di.make_layer([3000], 1, seed=13)
     layer.block_table[0, 5] = layer.num_pages + 10
