@@ -231,6 +231,20 @@ __device__ __forceinline__ float4 lds_f32x4(const float* p) {
                  : "r"(smem_u32(p)));
     return r;
 }
+// (max(a, 0), max(b, 0)) as a pair, formed in the pair's own registers
+__device__ __forceinline__ uint64_t relu_pair(uint32_t a, uint32_t b) {
+    uint64_t d;
+    asm("{\n\t.reg .f32 x, y;\n\tmax.f32 x, %1, 0f00000000;\n\tmax.f32 y, %2, 0f00000000;\n\t"
+        "mov.b64 %0, {x, y};\n\t}"
+        : "=l"(d)
+        : "f"(__uint_as_float(a)), "f"(__uint_as_float(b)));
+    return d;
+}
+__device__ __forceinline__ uint64_t pair_f32(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
 __device__ __forceinline__ float lo_f32x2(uint64_t v) { return __uint_as_float((uint32_t)v); }
 __device__ __forceinline__ float hi_f32x2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
@@ -787,26 +801,32 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_keys,
                     // one token's 32 head logits -> its weighted ReLU sum, stored
                     auto score = [&](const uint32_t(&v)[32], int jt) {
                         const float* wt = wq + jt * kIdxHeads;
-                        // four independent packed (f32x2) partial sums
-                        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+                        // two independent packed (f32x2) partial sums, heads
+                        // (4i, 4i+1) and (4i+2, 4i+3)
+                        uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
                         for (int h4 = 0; h4 < 8; ++h4) {
                             const float4 ww = lds_f32x4(wt + 4 * h4);
-                            acc2[(2 * h4) & 3] = fma_f32x2(
-                                pack_f32x2(ww.x, ww.y),
-                                pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f),
-                                           fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f)),
-                                acc2[(2 * h4) & 3]);
-                            acc2[(2 * h4 + 1) & 3] = fma_f32x2(
-                                pack_f32x2(ww.z, ww.w),
-                                pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f),
-                                           fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f)),
-                                acc2[(2 * h4 + 1) & 3]);
+                            if constexpr (kWide) {
+                                acc2[0] = fma_f32x2(pair_f32(ww.x, ww.y),
+                                                    relu_pair(v[4 * h4 + 0], v[4 * h4 + 1]), acc2[0]);
+                                acc2[1] = fma_f32x2(pair_f32(ww.z, ww.w),
+                                                    relu_pair(v[4 * h4 + 2], v[4 * h4 + 3]), acc2[1]);
+                            } else {
+                                acc2[0] = fma_f32x2(
+                                    pack_f32x2(ww.x, ww.y),
+                                    pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f),
+                                               fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f)),
+                                    acc2[0]);
+                                acc2[1] = fma_f32x2(
+                                    pack_f32x2(ww.z, ww.w),
+                                    pack_f32x2(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f),
+                                               fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f)),
+                                    acc2[1]);
+                            }
                         }
-                        const float sc = (((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
-                                           (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) +
-                                          ((lo_f32x2(acc2[2]) + hi_f32x2(acc2[2])) +
-                                           (lo_f32x2(acc2[3]) + hi_f32x2(acc2[3])))) * kscale;
+                        const float sc = ((lo_f32x2(acc2[0]) + hi_f32x2(acc2[0])) +
+                                          (lo_f32x2(acc2[1]) + hi_f32x2(acc2[1]))) * kscale;
                         // token jt sees s when s < seq - nb + gtok0 + jt + 1
                         if (in_seq) *cell = (need <= jt) ? sc : -INFINITY;
                         cell += p.ld;
