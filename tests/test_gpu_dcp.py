@@ -53,7 +53,7 @@ def _check_against_oracle(gl, S, idx, ridx, resent, world, cand, rows=None):
     return want_resend
 
 
-@pytest.mark.parametrize("world", [8, 4, 2, 1])
+@pytest.mark.parametrize("world", [8, 6, 4, 3, 2, 1])
 def test_dcp_topk_on_indexer_scores(world):
     layer = di.make_layer([40000, 23000, 2500, 9000], [2, 1, 3, 1], seed=500 + world, extra_pages=2)
     gl = GpuLayer(layer)

@@ -220,6 +220,22 @@ def test_prepared_decode_matches_the_direct_call():
     assert e.value.status == 3  # DSA_ERR_WORKSPACE
 
 
+def test_prepared_append_matches_the_direct_call():
+    """A PreparedCall of dsa_append_cache writes the same cache bytes."""
+    layer = di.make_layer([130, 3000], [5, 2], seed=43, extra_pages=1)
+    keys, lat = di.append_payload(layer, seed=4)
+    a, b = GpuLayer(layer), GpuLayer(layer)
+    k_dev, l_dev = keys.cuda(), lat.cuda()
+    dsa.dsa_append_cache(a.batch, k_dev, l_dev, layer.kv_scale, a.g.index_pages,
+                         a.g.latent_pages, di.KEYS_FP8, a.status())
+    call = dsa.prepare_append_cache(b.batch, k_dev, l_dev, layer.kv_scale, b.g.index_pages,
+                                    b.g.latent_pages, di.KEYS_FP8, b.status())
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(a.g.index_pages, b.g.index_pages)
+    assert torch.equal(a.g.latent_pages, b.g.latent_pages)
+
+
 def test_bad_page_id_sets_device_status():
     layer = di.make_layer([3000], 1, seed=13)
     layer.block_table[0, 5] = layer.num_pages + 10
