@@ -26,9 +26,10 @@
  *   - All pointers except the dsa_batch struct itself are DEVICE pointers owned
  *     by the caller.  The library allocates nothing, keeps no state between
  *     calls (apart from a launch counter, the batch-invariant switch and the
- *     fixed scratch array of dsa_decode_noalloc) and is safe to call from several host threads on
- *     different streams, except dsa_decode_noalloc calls whose executions
- *     overlap on the GPU (they share that array; see below).
+ *     fixed scratch array of dsa_decode_noalloc) and is safe to call from
+ *     several host threads on different streams, except dsa_decode_noalloc
+ *     calls whose executions overlap on the GPU (they share that array; see
+ *     below).
  *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
  *     NULL = legacy default stream).  Argument errors the host can see are
  *     returned before anything is launched; nothing is written then.
