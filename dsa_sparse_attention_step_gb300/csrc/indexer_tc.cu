@@ -116,6 +116,7 @@ struct IdxCfg {
     static constexpr int kOffBar = kOffMeta + kMetaSlots * kMetaBytes;
     static constexpr int kSmemAlloc = kOffBar + 512 + 1024;
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(kStages <= kMaxStages, "the barrier arrays cover every key stage");
 };
 
 // Scale words of a page that is absent (past the sequence) or out of range:
