@@ -53,7 +53,7 @@ using namespace sm100;
 namespace {
 
 constexpr int kTile = 128;                     // keys per unit
-constexpr int kMaxStages = 8;                  // key-tile ring: 8 stages (FP8), 6 (MXFP4)
+constexpr int kMaxStages = 8;                  // key-tile ring: at most 8 stages
 constexpr int kStageBytes = kTile * kIdxDim;   // 16384: E4M3 A operand of one unit
 constexpr int kQBufBytes = 8 * kIdxHeads * kIdxDim;  // 32768: up to 8 tokens x 32 heads
 constexpr int kMaxReq = 4096;
@@ -98,8 +98,10 @@ struct IdxCfg {
     static constexpr int kTokSplit = 2;                        // MXFP4 token stride
     static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 384 (kDual), 512, 640 (kWide) or 448
     static constexpr int kMaxG = kMx ? 2 : 8;                  // tokens per group
-    // enough key bytes in flight per SM to cover the memory latency at full load
-    static constexpr int kStages = kMx ? 6 : 8;
+    // enough key bytes in flight per SM to cover the memory latency at full
+    // load: six stages (96 KB) on the paths of groups of 3-8 tokens (six ran
+    // 1-2 % faster than eight there, four slower), eight for groups of 1-2
+    static constexpr int kStages = (kMx || !kDual) ? 6 : 8;
     // scale words of a unit: a slot is free again S + 3 units later with one
     // MMA thread (MXFP4); S + 6 with kDual, whose accumulators repeat every
     // sixth unit; S + 4 with kWide (the MMA of unit i - S waited for the
