@@ -14,27 +14,27 @@
 // A persistent grid splits the unit list into equal contiguous ranges, so the
 // keys, not the queries, are balanced across SMs.  Per unit:
 //   D[128 keys x N] = K8[128 x 128] . Q8[N x 128]^T,  N = 32 heads x G tokens,
-// tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM, two or
-// three buffers, or three per MMA thread when two threads issue).  Key pages arrive by TMA (128-byte swizzle) into an 8-stage ring
-// (their 64 scale words by bulk copy beside them), the query group by TMA
-// into a double buffer.  The epilogue warps read the accumulator (thread =
-// key), apply ReLU, the weighted head sum, the key scale and the causal mask,
-// and store fp32 scores.
+// tcgen05.mma kind::f8f6f4 (E4M3 x E4M3, fp32 accumulator in TMEM).  Key pages
+// arrive by TMA (128-byte swizzle) into a ring of six stages (eight for query
+// groups of one or two tokens), their 64 scale words by bulk copy beside them,
+// and the query group by TMA into a double buffer.  The epilogue warps read the
+// accumulator (thread = key), apply ReLU, the weighted head sum, the key scale
+// and the causal mask, and store fp32 scores.
 //
 // Roles: producer warps (each looks up pages and one lane issues the copies),
 // then MMA warps (the first allocates TMEM; lane 0 issues MMAs), then for
 // MXFP4 keys four converter warps, then epilogue warps in sets of four (one
-// warp per TMEM lane quarter): with FP8 keys a set takes whole units and all
-// of their tokens -- three sets, one per TMEM accumulator, with one MMA
-// thread; two sets taking alternate units with two -- so every accumulator
-// is drained while the MMA fills another; with MXFP4 keys two sets each take
-// every second token.  A key of an absent page carries all-ones scale bits
-// (copied in place of the page's scales), so the epilogue needs no
-// block-table read.  With FP8 keys and query groups of one
-// or two tokens there are two producer and two MMA warps, each pair taking
-// alternate units: one thread spends about a thousand cycles of instruction
-// latency on a unit's copies (or on its waits, MMAs and commits), more than
-// the unit's share of the memory bandwidth allows.  Every wait is bounded.
+// warp per TMEM lane quarter).  With FP8 keys two producer and two MMA warps
+// take alternate units (one thread spends about a thousand cycles of
+// instruction latency on a unit's copies, or on its waits, MMAs and commits,
+// more than the unit's share of the memory bandwidth allows), and the
+// accumulators depend on the query-group size (IdxCfg below): six for groups
+// of one or two tokens, a ring of three for groups of 3-5, two accumulators of
+// two token halves for groups of 6-8.  With MXFP4 keys one MMA thread feeds
+// four accumulators per token and two epilogue sets each take every second
+// token.  A key of an absent page carries all-ones scale bits (copied in place
+// of the page's scales), so the epilogue needs no block-table read.  Every
+// wait is bounded.
 #include <climits>
 #include <cstring>
 #include <mutex>
